@@ -1,0 +1,24 @@
+"""Shared pytest configuration.
+
+Tests marked ``gpu`` need a CUDA device and the compiled library; everything
+else runs on the CPU (oracle pins, host-side logic, ABI symbol checks)."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: long CPU sweep")
+
+
+@pytest.fixture(scope="session")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
