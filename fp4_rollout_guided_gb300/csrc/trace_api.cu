@@ -1,0 +1,392 @@
+// trace_api.cu - the C ABI declared in include/trace_fp4.h: handle life
+// cycle, argument validation, scratch ordering, the built-in profiler, and
+// the calls that enqueue the kernels of trace_kernels.cu.
+//
+// Method: "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts",
+// section "TRACE Core Concept" (rollout-side record, training-side guided
+// rounding, compact record of mantissa bit and scale).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "trace_fp4.h"
+#include "trace_internal.h"
+
+namespace {
+
+constexpr int kMaxTimed = 4096;
+
+struct TimedLaunch {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct trace_ctx {
+  int device = 0;
+  int sm_count = 0;
+  tfp4::Scratch scratch = {};
+  cudaEvent_t order = nullptr;  // orders calls on the handle's scratch
+  int last_error = 0;
+  bool profiling = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> spare;  // recycled timing events
+};
+
+namespace {
+
+// Makes the handle's device current for the duration of a call.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&old_) == cudaSuccess && old_ != dev) {
+      if (cudaSetDevice(dev) == cudaSuccess) switched_ = true;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(old_);
+  }
+
+ private:
+  int old_ = -1;
+  bool switched_ = false;
+};
+
+trace_status_t cuda_fail(trace_ctx* h, cudaError_t e) {
+  if (h) h->last_error = (int)e;
+  cudaGetLastError();  // clear the sticky-free error state for the next call
+  return TRACE_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// Shape rules shared by every call.
+trace_status_t check_shape(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return TRACE_ERR_INVALID_ARG;
+  if (rows >= (int64_t(1) << 31)) return TRACE_ERR_INVALID_ARG;
+  if (rows > 0 && cols / 32 > (int64_t(1) << 31) / rows) return TRACE_ERR_INVALID_ARG;
+  if (rows * (cols / 32) >= (int64_t(1) << 31)) return TRACE_ERR_INVALID_ARG;
+  return TRACE_OK;
+}
+
+trace_status_t check_tensor(const void* p) {
+  if (!p) return TRACE_ERR_INVALID_ARG;
+  if (!aligned(p, 16)) return TRACE_ERR_ALIGNMENT;
+  return TRACE_OK;
+}
+
+// Host segment table -> kernel parameter (validated, narrowed to int32).
+trace_status_t make_segments(const trace_segments_t& in, int64_t rows, tfp4::SegParam* out) {
+  if (!in.row_offsets) {
+    out->n = 1;
+    out->off[0] = 0;
+    out->off[1] = (int32_t)rows;
+    return TRACE_OK;
+  }
+  if (in.n_seg < 1 || in.n_seg > TRACE_MAX_SEGMENTS) return TRACE_ERR_INVALID_ARG;
+  const int64_t* o = in.row_offsets;
+  if (o[0] != 0 || o[in.n_seg] != rows) return TRACE_ERR_INVALID_ARG;
+  for (int32_t s = 0; s < in.n_seg; ++s)
+    if (o[s + 1] < o[s]) return TRACE_ERR_INVALID_ARG;
+  out->n = in.n_seg;
+  for (int32_t s = 0; s <= in.n_seg; ++s) out->off[s] = (int32_t)o[s];
+  return TRACE_OK;
+}
+
+cudaEvent_t take_event(trace_ctx* h) {
+  if (!h->spare.empty()) {
+    cudaEvent_t e = h->spare.back();
+    h->spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+// Runs one launcher, bracketed by timing events when profiling is on.
+template <typename F>
+cudaError_t timed(trace_ctx* h, int kernel, cudaStream_t st, F&& launch) {
+  if (!h->profiling || (int)h->timed.size() >= kMaxTimed) return launch();
+  cudaEvent_t a = take_event(h), b = take_event(h);
+  if (!a || !b) {
+    if (a) h->spare.push_back(a);
+    if (b) h->spare.push_back(b);
+    return launch();
+  }
+  cudaEventRecord(a, st);
+  const cudaError_t e = launch();
+  cudaEventRecord(b, st);
+  h->timed.push_back({kernel, a, b});
+  return e;
+}
+
+// Orders this call after the previous user of the handle's scratch.
+cudaError_t begin_call(trace_ctx* h, cudaStream_t st) { return cudaStreamWaitEvent(st, h->order, 0); }
+cudaError_t end_call(trace_ctx* h, cudaStream_t st) { return cudaEventRecord(h->order, st); }
+
+}  // namespace
+
+extern "C" {
+
+int trace_version(void) { return 100; }
+
+const char* trace_status_string(trace_status_t s) {
+  switch (s) {
+    case TRACE_OK: return "ok";
+    case TRACE_ERR_INVALID_ARG: return "invalid argument";
+    case TRACE_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case TRACE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case TRACE_ERR_CUDA: return "CUDA error";
+    case TRACE_ERR_OOM: return "out of device memory";
+    case TRACE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int trace_last_cuda_error(trace_handle_t h) { return h ? h->last_error : 0; }
+
+trace_status_t trace_create(trace_handle_t* out, int device) {
+  if (!out) return TRACE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+    cudaGetLastError();
+    return TRACE_ERR_UNSUPPORTED_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+    cudaGetLastError();
+    return TRACE_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (prop.major != 10 || prop.minor != 3) return TRACE_ERR_UNSUPPORTED_DEVICE;
+  trace_ctx* h = new (std::nothrow) trace_ctx;
+  if (!h) return TRACE_ERR_OOM;
+  h->device = device;
+  h->sm_count = prop.multiProcessorCount;
+  DeviceGuard g(device);
+  // one allocation: amax words, ticket (padded to 256 B), training scales
+  const size_t seg_bytes = sizeof(uint32_t) * TRACE_MAX_SEGMENTS;
+  const size_t bytes = seg_bytes + 256 + seg_bytes;
+  char* base = nullptr;
+  if (cudaMalloc(&base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return TRACE_ERR_OOM;
+  }
+  if (cudaMemset(base, 0, bytes) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->order, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(base);
+    delete h;
+    return TRACE_ERR_CUDA;
+  }
+  h->scratch.amax_bits = (uint32_t*)base;
+  h->scratch.done = (uint32_t*)(base + seg_bytes);
+  h->scratch.gs_train = (float*)(base + seg_bytes + 256);
+  *out = h;
+  return TRACE_OK;
+}
+
+trace_status_t trace_destroy(trace_handle_t h) {
+  if (!h) return TRACE_OK;
+  DeviceGuard g(h->device);
+  for (auto& t : h->timed) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  for (auto e : h->spare) cudaEventDestroy(e);
+  if (h->order) cudaEventDestroy(h->order);
+  cudaFree(h->scratch.amax_bits);
+  cudaGetLastError();
+  delete h;
+  return TRACE_OK;
+}
+
+trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                   int64_t cols, trace_segments_t seg, void* codes_u8,
+                                   void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
+                                   trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  for (const void* p : {x_bf16, (const void*)codes_u8, (const void*)bs_e4m3})
+    if ((s = check_tensor(p)) != TRACE_OK) return s;
+  if (guide_bits && (s = check_tensor(guide_bits)) != TRACE_OK) return s;
+  if (!gs_f32) return TRACE_ERR_INVALID_ARG;
+  if (!aligned(gs_f32, 4)) return TRACE_ERR_ALIGNMENT;
+  static thread_local tfp4::SegParam sp;
+  if ((s = make_segments(seg, rows, &sp)) != TRACE_OK) return s;
+
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = begin_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  const int64_t nchunks = rows * (cols / 32);
+  const int32_t cpr = (int32_t)(cols / 32);
+  if (nchunks == 0) {
+    e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
+  } else {
+    e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
+      return tfp4::launch_amax(x_bf16, nchunks, cpr, sp, h->scratch, gs_f32, h->sm_count, st);
+    });
+    if (e == cudaSuccess)
+      e = timed(h, TRACE_KERNEL_ROLLOUT_QUANT, st, [&] {
+        return tfp4::launch_rollout_quant(x_bf16, nchunks, cpr, sp, gs_f32, codes_u8, bs_e4m3,
+                                          guide_bits, h->sm_count, st);
+      });
+  }
+  const cudaError_t e2 = end_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (e2 != cudaSuccess) return cuda_fail(h, e2);
+  return TRACE_OK;
+}
+
+trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,
+                                int64_t cols, uint32_t* guide_bits, trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  if ((s = check_tensor(codes_u8)) != TRACE_OK) return s;
+  if ((s = check_tensor(guide_bits)) != TRACE_OK) return s;
+  const int64_t nchunks = rows * (cols / 32);
+  if (nchunks == 0) return TRACE_OK;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = timed(h, TRACE_KERNEL_GUIDE_PACK, st, [&] {
+    return tfp4::launch_guide_pack(codes_u8, nchunks, guide_bits, h->sm_count, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
+                                  const uint32_t* guide_bits, const void* bs_r,
+                                  const float* gs_r, trace_segments_t seg_r, int64_t rows,
+                                  int64_t cols, void* codes_u8, trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  for (const void* p : {x_ref_bf16, (const void*)guide_bits, bs_r, (const void*)codes_u8})
+    if ((s = check_tensor(p)) != TRACE_OK) return s;
+  if (!gs_r) return TRACE_ERR_INVALID_ARG;
+  if (!aligned(gs_r, 4)) return TRACE_ERR_ALIGNMENT;
+  static thread_local tfp4::SegParam sp;
+  if ((s = make_segments(seg_r, rows, &sp)) != TRACE_OK) return s;
+  const int64_t nchunks = rows * (cols / 32);
+  if (nchunks == 0) return TRACE_OK;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = timed(h, TRACE_KERNEL_GUIDE_UNPACK, st, [&] {
+    return tfp4::launch_guide_unpack(x_ref_bf16, guide_bits, bs_r, gs_r, nchunks,
+                                     (int32_t)(cols / 32), sp, codes_u8, h->sm_count, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                     int64_t cols, trace_segments_t seg_t,
+                                     trace_guide_kind_t kind, const void* guide,
+                                     const void* bs_r, const float* gs_r,
+                                     trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
+                                     void* codes_t_u8, trace_stats_t* stats_dev,
+                                     trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  if (kind != TRACE_GUIDE_NONE && kind != TRACE_GUIDE_FULL && kind != TRACE_GUIDE_COMPACT)
+    return TRACE_ERR_INVALID_ARG;
+  if ((s = check_tensor(x_bf16)) != TRACE_OK) return s;
+  if ((s = check_tensor(y_bf16)) != TRACE_OK) return s;
+  if (ste_mask && (s = check_tensor(ste_mask)) != TRACE_OK) return s;
+  if (codes_t_u8 && (s = check_tensor(codes_t_u8)) != TRACE_OK) return s;
+  if (stats_dev && !aligned(stats_dev, 8)) return TRACE_ERR_ALIGNMENT;
+  static thread_local tfp4::SegParam spt, spr;
+  if ((s = make_segments(seg_t, rows, &spt)) != TRACE_OK) return s;
+  if (kind != TRACE_GUIDE_NONE) {
+    if ((s = check_tensor(guide)) != TRACE_OK) return s;
+    if ((s = check_tensor(bs_r)) != TRACE_OK) return s;
+    if (!gs_r) return TRACE_ERR_INVALID_ARG;
+    if (!aligned(gs_r, 4)) return TRACE_ERR_ALIGNMENT;
+    if ((s = make_segments(seg_r, rows, &spr)) != TRACE_OK) return s;
+  } else {
+    spr.n = 1;
+    spr.off[0] = 0;
+    spr.off[1] = (int32_t)rows;
+  }
+  const int64_t nchunks = rows * (cols / 32);
+  if (nchunks == 0) return TRACE_OK;
+
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = begin_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  const int32_t cpr = (int32_t)(cols / 32);
+  e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
+    return tfp4::launch_amax(x_bf16, nchunks, cpr, spt, h->scratch, h->scratch.gs_train,
+                             h->sm_count, st);
+  });
+  if (e == cudaSuccess) {
+    tfp4::FakequantArgs a;
+    a.x = x_bf16;
+    a.nchunks = nchunks;
+    a.cpr = cpr;
+    a.gs_t = h->scratch.gs_train;
+    a.kind = (int)kind;
+    a.guide = guide;
+    a.bs_r = bs_r;
+    a.gs_r = gs_r;
+    a.y = y_bf16;
+    a.mask = ste_mask;
+    a.codes_t = codes_t_u8;
+    a.stats = stats_dev;
+    e = timed(h, TRACE_KERNEL_FAKEQUANT, st,
+              [&] { return tfp4::launch_fakequant(a, spt, spr, h->sm_count, st); });
+  }
+  const cudaError_t e2 = end_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (e2 != cudaSuccess) return cuda_fail(h, e2);
+  return TRACE_OK;
+}
+
+trace_status_t trace_profile_enable(trace_handle_t h, int enable) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  h->profiling = enable != 0;
+  return TRACE_OK;
+}
+
+trace_status_t trace_profile_collect(trace_handle_t h, trace_kernel_time_t* out) {
+  if (!h || !out) return TRACE_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  for (int k = 0; k < TRACE_KERNEL_COUNT; ++k) {
+    out[k].launches = 0;
+    out[k].total_ms = 0.0;
+  }
+  cudaError_t first = cudaSuccess;
+  for (auto& t : h->timed) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+    if (e == cudaSuccess) {
+      out[t.kernel].launches += 1;
+      out[t.kernel].total_ms += ms;
+    } else if (first == cudaSuccess) {
+      first = e;
+    }
+    h->spare.push_back(t.start);
+    h->spare.push_back(t.stop);
+  }
+  h->timed.clear();
+  if (first != cudaSuccess) return cuda_fail(h, first);
+  return TRACE_OK;
+}
+
+}  // extern "C"

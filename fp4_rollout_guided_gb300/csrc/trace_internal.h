@@ -1,0 +1,88 @@
+// trace_internal.h - launch interface between the C ABI (trace_api.cu) and
+// the sm_103a kernels (trace_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "trace_fp4.h"
+
+namespace tfp4 {
+
+// Segment table as a kernel parameter: row offsets narrowed to int32 (rows
+// are validated to fit), passed by value in the parameter bank so that calls
+// need no device copy of the table and stay stream-ordered by construction.
+struct SegParam {
+  int32_t n;
+  int32_t off[TRACE_MAX_SEGMENTS + 1];
+};
+
+// Unsigned division by a runtime constant (chunk index -> row) without a
+// hardware divide: q = (mulhi(n, mul) + n) >> shift with shift = ceil(log2 d)
+// and mul = floor(2^32 * (2^shift - d) / d) + 1, exact for every 32-bit n.
+struct FastDivU {
+  uint32_t mul, shift;
+  explicit FastDivU(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    shift = l;
+    mul = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi(n, mul);
+#else
+    const uint32_t t = (uint32_t)(((uint64_t)n * mul) >> 32);
+#endif
+    return (uint32_t)(((uint64_t)t + n) >> shift);
+  }
+};
+
+// Device scratch owned by a handle.  amax_bits holds per-segment maxima as
+// binary32 bit patterns (non-negative floats order like unsigned integers);
+// the amax kernel's last CTA converts them to global scales and re-zeroes
+// them, so the array is all-zero between calls.
+struct Scratch {
+  uint32_t* amax_bits;  // [TRACE_MAX_SEGMENTS]
+  uint32_t* done;       // completion ticket of the amax kernel
+  float* gs_train;      // [TRACE_MAX_SEGMENTS] training-side global scales
+};
+
+// a1: per-segment amax of x, then gs[s] = amax/2688 written to gs_out.
+cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
+                        const Scratch& s, float* gs_out, int sm_count, cudaStream_t st);
+
+// a2: RTN codes, block scales, compact words (guide may be null).
+cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
+                                 const SegParam& seg, const float* gs, void* codes, void* bs,
+                                 uint32_t* guide, int sm_count, cudaStream_t st);
+
+// a3: codes -> compact words.
+cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,
+                              int sm_count, cudaStream_t st);
+
+// a4: compact words + reference values -> codes.
+cudaError_t launch_guide_unpack(const void* x_ref, const uint32_t* guide, const void* bs_r,
+                                const float* gs_r, int64_t nchunks, int32_t cpr,
+                                const SegParam& seg_r, void* codes, int sm_count,
+                                cudaStream_t st);
+
+// a5 + a6: training-side guided fake quantisation.
+struct FakequantArgs {
+  const void* x;
+  int64_t nchunks;
+  int32_t cpr;
+  const float* gs_t;  // per training segment
+  int kind;
+  const void* guide;
+  const void* bs_r;
+  const float* gs_r;
+  void* y;
+  uint32_t* mask;
+  void* codes_t;
+  trace_stats_t* stats;
+};
+cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
+                             const SegParam& seg_r, int sm_count, cudaStream_t st);
+
+}  // namespace tfp4

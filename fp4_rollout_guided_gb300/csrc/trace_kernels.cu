@@ -1,0 +1,891 @@
+// trace_kernels.cu - sm_103a kernels of the guided-NVFP4 hot path of TRACE.
+//
+// Sources: "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts",
+// section "TRACE Core Concept" (rollout records FP4 results; training-side
+// fake quantisation picks the adjacent E2M1 point closer to the rollout's;
+// a compact record of mantissa bit + scale sets the direction) and the
+// worked example of section "Why Does FP4 Rollout 'Break' RL Training?".
+//
+// Work decomposition.  Every kernel streams a flat sequence of 32-element
+// "chunks" (two 16-element NVFP4 blocks, one STE mask word).  Rows hold
+// cols/32 chunks, so a chunk never straddles a row or a segment.  A CTA of
+// 256 threads handles a "step" of 256 consecutive chunks (16 KiB of bf16),
+// one chunk per thread, and owns a contiguous range of steps; the next
+// step's loads are issued before the current step is computed.  Segments
+// are looked up once per step (uniform across the CTA); only a step that
+// straddles a segment boundary resolves segments per thread.
+//
+// Arithmetic.  All of it is binary32 with round-to-nearest-even (explicit
+// __f*_rn intrinsics so nothing is contracted into an FMA; no flush to zero),
+// in the same operation order as the method's definition:
+//   gs = amax / 2688;  bs = e4m3(bamax / (gs * 6));  S = dec(bs) * gs;
+//   inv = 1 / S (0 if S == 0 or the reciprocal overflows);  t = |x| * inv.
+// E2M1 rounding uses directed-rounding adds against a constant C whose ulp
+// equals the E2M1 spacing of t's binade (C = 1.5 * 2^(22+e), 2^e the binade
+// of max(t, 1), t clamped to 6): fl_rz(t + C) - C, fl_rp(t + C) - C and
+// fl_rn(t + C) - C are exactly the lower, upper and nearest E2M1 points
+// (ties go to the even index because C is an even number of ulps), and the
+// last significand bit of fl_rz(t + C) is the parity of the lower index.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "trace_internal.h"
+
+namespace tfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint32_t kAbs2 = 0x7FFF7FFFu;
+
+// ---------------------------------------------------------------------------
+// memory access
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream2(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
+  unsigned short v;
+  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_stream1(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ void st_stream_u16(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)a) : "memory");
+}
+
+struct Chunk {
+  uint32_t w[16];  // 32 bf16: element 2i in the low half of w[i]
+};
+
+__device__ __forceinline__ void load_chunk(Chunk& c, const uint8_t* base, uint32_t chunk) {
+  const uint8_t* p = base + (uint64_t)chunk * 64u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = ld_stream(p + 16 * q);
+    c.w[4 * q + 0] = v.x;
+    c.w[4 * q + 1] = v.y;
+    c.w[4 * q + 2] = v.z;
+    c.w[4 * q + 3] = v.w;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// segments
+// ---------------------------------------------------------------------------
+
+// Largest s with off[s] <= row (off[n] = rows > row); with empty segments the
+// non-empty one is found.
+__device__ __forceinline__ int seg_search(const SegParam& p, uint32_t row) {
+  int lo = 0, hi = p.n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)p.off[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int seg_advance(const SegParam& p, int s, uint32_t row) {
+  while ((uint32_t)p.off[s + 1] <= row) ++s;
+  return s;
+}
+
+// Per-step segment resolution: `cur` follows the step's first row; update()
+// returns true when the whole step lies inside segment `cur`.
+struct StepSeg {
+  int cur;
+  __device__ __forceinline__ bool update(const SegParam& p, uint32_t r0, uint32_t r1) {
+    cur = seg_advance(p, cur, r0);
+    return (uint32_t)p.off[cur + 1] > r1;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// scales
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Eight words of masked bf16 magnitudes -> binary32 bits of their maximum.
+__device__ __forceinline__ float block_amax8(const uint32_t* a) {
+  uint32_t m0 = max_u16x2(a[0], a[1]);
+  const uint32_t m1 = max_u16x2(a[2], a[3]);
+  const uint32_t m2 = max_u16x2(a[4], a[5]);
+  const uint32_t m3 = max_u16x2(a[6], a[7]);
+  m0 = max_u16x2(max_u16x2(m0, m1), max_u16x2(m2, m3));
+  const uint32_t hi = m0 >> 16, lo = m0 & 0xFFFFu;
+  return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
+// E4M3 code -> binary32: placing the 7 magnitude bits at bit 20 gives the
+// value times 2^-120 (normal and subnormal codes alike); scaling by 2^120 is
+// exact.
+__device__ __forceinline__ float e4m3_decode(uint32_t code) {
+  return __fmul_rn(__uint_as_float(code << 20), 0x1p120f);
+}
+
+__device__ __forceinline__ float global_scale_of(uint32_t amax_bits) {
+  const float amax = __uint_as_float(amax_bits);
+  if (!(amax > 0.0f)) return 0.0f;
+  const float gs = __fdiv_rn(amax, 2688.0f);
+  return gs > 0.0f ? gs : 0.0f;
+}
+
+struct PairScale {
+  uint32_t codes;  // byte 0: block 0, byte 1: block 1
+  float S[2];
+  float inv[2];
+};
+
+__device__ __forceinline__ void real_scale(uint32_t code, float gs, float& S, float& inv) {
+  S = __fmul_rn(e4m3_decode(code), gs);
+  float r = 0.0f;
+  if (S > 0.0f) {
+    r = __frcp_rn(S);
+    if (r == __int_as_float(0x7F800000)) r = 0.0f;  // reciprocal overflow: flush
+  }
+  inv = r;
+}
+
+// Both blocks' E4M3 scales from their maxima and the segment scale.
+__device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, float gs) {
+  float q0 = 0.0f, q1 = 0.0f;
+  if (gs > 0.0f) {
+    const float den = __fmul_rn(gs, 6.0f);
+    q0 = __fdiv_rn(bamax0, den);
+    q1 = __fdiv_rn(bamax1, den);
+  }
+  unsigned short c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(q1), "f"(q0));
+  PairScale p;
+  p.codes = c;
+  real_scale(c & 0xFFu, gs, p.S[0], p.inv[0]);
+  real_scale((uint32_t)c >> 8, gs, p.S[1], p.inv[1]);
+  return p;
+}
+
+// Real scales of two stored E4M3 codes (the rollout side's record).
+__device__ __forceinline__ PairScale pair_scale_stored(uint32_t codes, float gs) {
+  PairScale p;
+  p.codes = codes;
+  real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
+  real_scale((codes >> 8) & 0xFFu, gs, p.S[1], p.inv[1]);
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1
+// ---------------------------------------------------------------------------
+
+// Two signed binary32 values -> one byte of two E2M1 nibbles (lo = first).
+// Hardware RTN, ties to even, saturating at +-6, sign kept.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %1, %2; cvt.u32.u8 %0, b; }"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The rounding constant for t in [0, 6]: 1.5 * 2^(22 + e) with 2^e the
+// binade of max(t, 1).
+__device__ __forceinline__ float magic_of(float tc) {
+  uint32_t e = __float_as_uint(tc) & 0x7F800000u;
+  e = e > 0x3F800000u ? e : 0x3F800000u;
+  return __uint_as_float(e + 0x0B400000u);
+}
+
+// Rollout-frame decode of one element from the compact record: the bracket
+// member of t_r whose index parity equals bit 0 of `lsb_word` (a point
+// bracket ignores the bit).  Returns the E2M1 magnitude.
+__device__ __forceinline__ float decode_compact(float tr, uint32_t lsb_word) {
+  const float tc = fminf(tr, 6.0f);
+  const float C = magic_of(tc);
+  const uint32_t uz = __float_as_uint(__fadd_rz(tc, C));
+  const uint32_t up = __float_as_uint(__fadd_ru(tc, C));
+  const uint32_t us = uz + ((uz ^ lsb_word) & (up - uz));
+  return __fsub_rn(__uint_as_float(us), C);
+}
+
+// ---------------------------------------------------------------------------
+// a1: segment amax + global scales
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t chunk_amax_bits(const Chunk& c) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = max_u16x2(m, c.w[i] & kAbs2);
+  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+  return (hi > lo ? hi : lo) << 16;  // binary32 bits of the largest |x|
+}
+
+// CTA-wide max of v, folded into *dst with one atomic (called uniformly).
+__device__ __forceinline__ void cta_flush_max(uint32_t v, uint32_t* dst, uint32_t* red) {
+  v = __reduce_max_sync(0xFFFFFFFFu, v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) m = red[i] > m ? red[i] : m;
+    if (m) atomicMax(dst, m);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_amax(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
+           uint32_t steps_per_cta, const __grid_constant__ SegParam seg,
+           uint32_t* __restrict__ amax_bits, uint32_t* __restrict__ done,
+           float* __restrict__ gs_out) {
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ int is_last;
+  const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+
+  StepSeg ss;
+  ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
+  int open = -1;  // segment whose running max this CTA holds
+  uint32_t run = 0;
+
+  Chunk cur, nxt;
+  if (step < step_end) {
+    const uint32_t c = step * kThreads + threadIdx.x;
+    if (c < nchunks) load_chunk(cur, x, c);
+  }
+  for (; step < step_end; ++step) {
+    const uint32_t c0 = step * kThreads;
+    const uint32_t c = c0 + threadIdx.x;
+    if (step + 1 < step_end) {
+      const uint32_t cn = c + kThreads;
+      if (cn < nchunks) load_chunk(nxt, x, cn);
+    }
+    const uint32_t last = min(c0 + kThreads, nchunks) - 1;
+    const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+    const uint32_t m = c < nchunks ? chunk_amax_bits(cur) : 0u;
+    if (uniform) {
+      if (ss.cur != open) {
+        if (open >= 0) cta_flush_max(run, amax_bits + open, red);
+        open = ss.cur;
+        run = 0;
+      }
+      run = m > run ? m : run;
+    } else {
+      if (open >= 0) cta_flush_max(run, amax_bits + open, red);
+      open = -1;
+      run = 0;
+      if (c < nchunks && m) atomicMax(amax_bits + seg_advance(seg, ss.cur, cpr.div(c)), m);
+    }
+    cur = nxt;
+  }
+  if (open >= 0) cta_flush_max(run, amax_bits + open, red);
+
+  // The last CTA to finish turns maxima into global scales and re-zeroes the
+  // maxima for the next call.  No CTA ever waits for another.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t ticket = atomicAdd(done, 1u);
+    is_last = (ticket == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    for (int s = threadIdx.x; s < seg.n; s += kThreads) {
+      const uint32_t a = atomicExch(amax_bits + s, 0u);
+      gs_out[s] = global_scale_of(a);
+    }
+    if (threadIdx.x == 0) atomicExch(done, 0u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compact word helpers
+// ---------------------------------------------------------------------------
+
+// Eight nibbles -> the 8 bits found at nibble bit `b` (0: index LSB, 3: sign).
+__device__ __forceinline__ uint32_t gather_nibble_bit(uint32_t w, int b) {
+  uint32_t v = (w >> b) & 0x11111111u;
+  v = (v | (v >> 3)) & 0x03030303u;
+  v = (v | (v >> 6)) & 0x000F000Fu;
+  v = (v | (v >> 12)) & 0x000000FFu;
+  return v;
+}
+
+// Sixteen nibbles (one block, two words) -> compact word.
+__device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
+  const uint32_t sgn = gather_nibble_bit(c0, 3) | (gather_nibble_bit(c1, 3) << 8);
+  const uint32_t lsb = gather_nibble_bit(c0, 0) | (gather_nibble_bit(c1, 0) << 8);
+  return sgn | (lsb << 16);
+}
+
+// ---------------------------------------------------------------------------
+// a2: rollout quantisation
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads)
+    k_rollout_quant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
+                    uint32_t steps_per_cta, const __grid_constant__ SegParam seg,
+                    const float* __restrict__ gs, uint8_t* __restrict__ codes,
+                    uint8_t* __restrict__ bs, uint8_t* __restrict__ guide) {
+  const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+  StepSeg ss;
+  ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
+
+  Chunk cur, nxt;
+  if (step < step_end) {
+    const uint32_t c = step * kThreads + threadIdx.x;
+    if (c < nchunks) load_chunk(cur, x, c);
+  }
+  for (; step < step_end; ++step) {
+    const uint32_t c0 = step * kThreads;
+    const uint32_t c = c0 + threadIdx.x;
+    if (step + 1 < step_end) {
+      const uint32_t cn = c + kThreads;
+      if (cn < nchunks) load_chunk(nxt, x, cn);
+    }
+    const uint32_t last = min(c0 + kThreads, nchunks) - 1;
+    const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+    if (c < nchunks) {
+      const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
+      const float g = gs[s];
+      uint32_t a[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
+      const PairScale ps = pair_scale(block_amax8(a), block_amax8(a + 8), g);
+      uint32_t out[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float inv = ps.inv[q >> 1];
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w = cur.w[4 * q + k];
+          // signed x * inv keeps the input's sign in the nibble
+          const uint32_t b = e2m1x2(__fmul_rn(__uint_as_float(w << 16), inv),
+                                    __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv));
+          word |= b << (8 * k);
+        }
+        out[q] = word;
+      }
+      st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
+      st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
+      if (guide)
+        st_stream2(guide + (uint64_t)c * 8u, compact_word(out[0], out[1]),
+                   compact_word(out[2], out[3]));
+    }
+    cur = nxt;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a3: guide pack
+// ---------------------------------------------------------------------------
+
+constexpr int kPackPerThread = 4;  // 4 x 16 B of codes in flight per thread
+
+__global__ void __launch_bounds__(kThreads)
+    k_guide_pack(const uint8_t* __restrict__ codes, uint32_t nchunks, uint32_t steps_per_cta,
+                 uint8_t* __restrict__ guide) {
+  constexpr uint32_t kStep = kThreads * kPackPerThread;
+  const uint32_t nsteps = (nchunks + kStep - 1) / kStep;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+  for (; step < step_end; ++step) {
+    uint4 v[kPackPerThread];
+#pragma unroll
+    for (int k = 0; k < kPackPerThread; ++k) {
+      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
+      if (c < nchunks) v[k] = ld_stream(codes + (uint64_t)c * 16u);
+    }
+#pragma unroll
+    for (int k = 0; k < kPackPerThread; ++k) {
+      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
+      if (c < nchunks)
+        st_stream2(guide + (uint64_t)c * 8u, compact_word(v[k].x, v[k].y),
+                   compact_word(v[k].z, v[k].w));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a4: guide unpack
+// ---------------------------------------------------------------------------
+
+// Two elements of one bf16x2 word -> one byte of rollout codes.  j0 is the
+// index of the word's low element inside its 16-element block.
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t gw, int j0) {
+  const float a0 = __uint_as_float((w << 16) & 0x7FFF0000u);
+  const float a1 = __uint_as_float(w & 0x7FFF0000u);
+  float g0 = decode_compact(__fmul_rn(a0, inv), gw >> (16 + j0));
+  float g1 = decode_compact(__fmul_rn(a1, inv), gw >> (17 + j0));
+  g0 = __uint_as_float(__float_as_uint(g0) | ((gw << (31 - j0)) & 0x80000000u));
+  g1 = __uint_as_float(__float_as_uint(g1) | ((gw << (30 - j0)) & 0x80000000u));
+  return e2m1x2(g0, g1);  // exact grid points: the conversion yields the index
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_guide_unpack(const uint8_t* __restrict__ x, const uint8_t* __restrict__ guide,
+                   const uint8_t* __restrict__ bs_r, const float* __restrict__ gs_r,
+                   uint32_t nchunks, FastDivU cpr, uint32_t steps_per_cta,
+                   const __grid_constant__ SegParam seg, uint8_t* __restrict__ codes) {
+  const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+  StepSeg ss;
+  ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
+
+  Chunk cur, nxt;
+  uint2 gcur = make_uint2(0, 0), gnxt = make_uint2(0, 0);
+  uint32_t bcur = 0, bnxt = 0;
+  if (step < step_end) {
+    const uint32_t c = step * kThreads + threadIdx.x;
+    if (c < nchunks) {
+      load_chunk(cur, x, c);
+      gcur = ld_stream2(guide + (uint64_t)c * 8u);
+      bcur = ld_stream_u16(bs_r + (uint64_t)c * 2u);
+    }
+  }
+  for (; step < step_end; ++step) {
+    const uint32_t c0 = step * kThreads;
+    const uint32_t c = c0 + threadIdx.x;
+    if (step + 1 < step_end) {
+      const uint32_t cn = c + kThreads;
+      if (cn < nchunks) {
+        load_chunk(nxt, x, cn);
+        gnxt = ld_stream2(guide + (uint64_t)cn * 8u);
+        bnxt = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
+      }
+    }
+    const uint32_t last = min(c0 + kThreads, nchunks) - 1;
+    const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+    if (c < nchunks) {
+      const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
+      const PairScale ps = pair_scale_stored(bcur, gs_r[s]);
+      uint32_t out[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int b = q >> 1;
+        const uint32_t gw = b ? gcur.y : gcur.x;
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j0 = (q & 1) * 8 + 2 * k;
+          word |= unpack_pair(cur.w[4 * q + k], ps.inv[b], gw, j0) << (8 * k);
+        }
+        out[q] = word;
+      }
+      st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
+    }
+    cur = nxt;
+    gcur = gnxt;
+    bcur = bnxt;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a5 + a6: training-side guided fake quantisation
+// ---------------------------------------------------------------------------
+
+// Signed E2M1 values of a byte's two nibbles (hardware E2M1 -> f16 decode).
+__device__ __forceinline__ void e2m1x2_values(uint32_t byte, float& v0, float& v1) {
+  uint32_t h;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(h) : "r"(byte));
+  const unsigned short lo = (unsigned short)(h & 0xFFFFu), hi = (unsigned short)(h >> 16);
+  asm("cvt.f32.f16 %0, %1;" : "=f"(v0) : "h"(lo));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(v1) : "h"(hi));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct Counters {
+  uint32_t mm_rtn, mm_g, h_rtn[4], h_g[4];
+};
+
+// exact signed grid value -> signed E2M1 index (+0 and -0 both give 0)
+__device__ __forceinline__ int signed_index(float g_signed) {
+  const uint32_t n = e2m1x2(g_signed, 0.0f) & 0xFu;
+  const int m = (int)(n & 7u);
+  return (n & 8u) ? -m : m;
+}
+
+__device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) {
+  int d0 = k_rtn - k_r, d1 = k_g - k_r;
+  d0 = d0 < 0 ? -d0 : d0;
+  d1 = d1 < 0 ? -d1 : d1;
+  k.mm_rtn += d0 != 0;
+  k.mm_g += d1 != 0;
+  k.h_rtn[0] += d0 == 0;
+  k.h_rtn[1] += d0 == 1;
+  k.h_rtn[2] += d0 == 2;
+  k.h_rtn[3] += d0 >= 3;
+  k.h_g[0] += d1 == 0;
+  k.h_g[1] += d1 == 1;
+  k.h_g[2] += d1 == 2;
+  k.h_g[3] += d1 >= 3;
+}
+
+// One training element.  ax = |x|, sx = x's sign bit (0 or 0x80000000);
+// vr_rel is the rollout's reconstructed value with its sign taken relative
+// to x (negated when the signs differ), so the candidate distances are formed
+// on magnitudes: |(+-v_c) - v_r| = |v_c - vr_rel| exactly (round-to-nearest
+// is symmetric).  Returns the signed output; g_out / g_rtn receive the chosen
+// and the RTN magnitudes.
+template <bool GUIDED>
+__device__ __forceinline__ float train_element(float ax, uint32_t sx, float inv_t, float S_t,
+                                               float vr_rel, float& g_out, float& g_rtn) {
+  const float t = __fmul_rn(ax, inv_t);
+  const float tc = fminf(t, 6.0f);
+  const float C = magic_of(tc);
+  const float s_rn = __fadd_rn(tc, C);
+  float y;
+  if (!GUIDED) {
+    const float g = __fsub_rn(s_rn, C);
+    g_out = g;
+    g_rtn = g;
+    y = __fmul_rn(g, S_t);
+  } else {
+    const float s_rz = __fadd_rz(tc, C);
+    const float s_rp = __fadd_ru(tc, C);
+    const float g_lo = __fsub_rn(s_rz, C);
+    const float g_hi = __fsub_rn(s_rp, C);
+    const float v_lo = __fmul_rn(g_lo, S_t);
+    const float v_hi = __fmul_rn(g_hi, S_t);
+    const float d_lo = fabsf(__fsub_rn(v_lo, vr_rel));
+    const float d_hi = fabsf(__fsub_rn(v_hi, vr_rel));
+    const bool rtn_hi = s_rn != s_rz;
+    const bool hi = (d_hi < d_lo) || (!(d_lo < d_hi) && rtn_hi);
+    y = hi ? v_hi : v_lo;
+    g_out = hi ? g_hi : g_lo;
+    g_rtn = rtn_hi ? g_hi : g_lo;
+  }
+  return __uint_as_float(__float_as_uint(y) | sx);
+}
+
+template <int KIND, bool MASK, bool CODES, bool STATS>
+__global__ void __launch_bounds__(kThreads)
+    k_fakequant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
+                uint32_t steps_per_cta, const __grid_constant__ SegParam seg_t,
+                const float* __restrict__ gs_t, const __grid_constant__ SegParam seg_r,
+                const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
+                const float* __restrict__ gs_r, uint8_t* __restrict__ y,
+                uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
+                trace_stats_t* __restrict__ stats) {
+  constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
+  const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+  StepSeg st, sr;
+  st.cur = 0;
+  sr.cur = 0;
+  if (step < step_end) {
+    const uint32_t r0 = cpr.div(step * kThreads);
+    st.cur = seg_search(seg_t, r0);
+    if (GUIDED) sr.cur = seg_search(seg_r, r0);
+  }
+  Counters cnt = {};
+  uint32_t n_done = 0;
+
+  Chunk cur, nxt;
+  uint4 gcur = make_uint4(0, 0, 0, 0), gnxt = make_uint4(0, 0, 0, 0);
+  uint32_t bcur = 0, bnxt = 0;
+  if (step < step_end) {
+    const uint32_t c = step * kThreads + threadIdx.x;
+    if (c < nchunks) {
+      load_chunk(cur, x, c);
+      if (KIND == TRACE_GUIDE_COMPACT) {
+        const uint2 v = ld_stream2(guide + (uint64_t)c * 8u);
+        gcur.x = v.x;
+        gcur.y = v.y;
+      } else if (KIND == TRACE_GUIDE_FULL) {
+        gcur = ld_stream(guide + (uint64_t)c * 16u);
+      }
+      if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)c * 2u);
+    }
+  }
+  for (; step < step_end; ++step) {
+    const uint32_t c0 = step * kThreads;
+    const uint32_t c = c0 + threadIdx.x;
+    if (step + 1 < step_end) {
+      const uint32_t cn = c + kThreads;
+      if (cn < nchunks) {
+        load_chunk(nxt, x, cn);
+        if (KIND == TRACE_GUIDE_COMPACT) {
+          const uint2 v = ld_stream2(guide + (uint64_t)cn * 8u);
+          gnxt.x = v.x;
+          gnxt.y = v.y;
+        } else if (KIND == TRACE_GUIDE_FULL) {
+          gnxt = ld_stream(guide + (uint64_t)cn * 16u);
+        }
+        if (GUIDED) bnxt = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
+      }
+    }
+    const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kThreads, nchunks) - 1);
+    const bool uni_t = st.update(seg_t, r0, r1);
+    const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
+    if (c < nchunks) {
+      int s_t = st.cur, s_r = sr.cur;
+      if (!uni_t || !uni_r) {
+        const uint32_t row = cpr.div(c);
+        if (!uni_t) s_t = seg_advance(seg_t, st.cur, row);
+        if (GUIDED && !uni_r) s_r = seg_advance(seg_r, sr.cur, row);
+      }
+      uint32_t a[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
+      const PairScale pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
+      PairScale pr = {};
+      if (GUIDED) pr = pair_scale_stored(bcur, gs_r[s_r]);
+      float six[2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        six[b] = pt.S[b] > 0.0f ? __fmul_rn(6.0f, pt.S[b]) : __int_as_float(0x7F800000);
+
+      uint32_t ybits[16];
+      uint32_t cbytes[16];
+      uint32_t kept = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int b = i >> 3;        // block of this word
+        const int j0 = (i & 7) * 2;  // index of its low element in the block
+        const uint32_t w = cur.w[i];
+        float gfull[2] = {0.0f, 0.0f};
+        if (KIND == TRACE_GUIDE_FULL) {
+          const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
+          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, gfull[0], gfull[1]);
+        }
+        float outv[2], gsel[2], grtn[2], gr_signed[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t xb = h ? (w & 0xFFFF0000u) : (w << 16);
+          const float ax = __uint_as_float(xb & 0x7FFFFFFFu);
+          const uint32_t sx = xb & 0x80000000u;
+          float vr_rel = 0.0f;
+          gr_signed[h] = 0.0f;
+          if (KIND == TRACE_GUIDE_COMPACT) {
+            const int j = j0 + h;
+            const uint32_t gw = b ? gcur.y : gcur.x;
+            const float g_r = decode_compact(__fmul_rn(ax, pr.inv[b]), gw >> (16 + j));
+            const float v_r = __fmul_rn(g_r, pr.S[b]);
+            const uint32_t sr_bit = (gw << (31 - j)) & 0x80000000u;
+            vr_rel = __uint_as_float(__float_as_uint(v_r) | (sx ^ sr_bit));
+            gr_signed[h] = __uint_as_float(__float_as_uint(g_r) | sr_bit);
+          } else if (KIND == TRACE_GUIDE_FULL) {
+            const float v_r = __fmul_rn(gfull[h], pr.S[b]);
+            vr_rel = __uint_as_float(__float_as_uint(v_r) ^ sx);
+            gr_signed[h] = gfull[h];
+          }
+          outv[h] = train_element<GUIDED>(ax, sx, pt.inv[b], pt.S[b], vr_rel, gsel[h], grtn[h]);
+          if (MASK) kept |= (ax > six[b] ? 0u : 1u) << (2 * i + h);
+        }
+        ybits[i] = bf16x2_rn(outv[0], outv[1]);
+        if (CODES || STATS) {
+          const uint32_t s0 = (w << 16) & 0x80000000u, s1 = w & 0x80000000u;
+          const float g0 = __uint_as_float(__float_as_uint(gsel[0]) | s0);
+          const float g1 = __uint_as_float(__float_as_uint(gsel[1]) | s1);
+          if (CODES) cbytes[i] = e2m1x2(g0, g1);
+          if (STATS && GUIDED) {
+            count(cnt, signed_index(gr_signed[0]),
+                  signed_index(__uint_as_float(__float_as_uint(grtn[0]) | s0)), signed_index(g0));
+            count(cnt, signed_index(gr_signed[1]),
+                  signed_index(__uint_as_float(__float_as_uint(grtn[1]) | s1)), signed_index(g1));
+          }
+        }
+      }
+      uint8_t* yp = y + (uint64_t)c * 64u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_stream(yp + 16 * q, ybits[4 * q], ybits[4 * q + 1], ybits[4 * q + 2], ybits[4 * q + 3]);
+      if (MASK) st_stream1(mask + (uint64_t)c * 4u, kept);
+      if (CODES) {
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = cbytes[4 * q] | (cbytes[4 * q + 1] << 8) | (cbytes[4 * q + 2] << 16) |
+                 (cbytes[4 * q + 3] << 24);
+        st_stream(codes_t + (uint64_t)c * 16u, o[0], o[1], o[2], o[3]);
+      }
+      if (STATS) n_done += 32;
+    }
+    cur = nxt;
+    gcur = gnxt;
+    bcur = bnxt;
+  }
+  if (STATS) {
+    const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
+                            cnt.h_rtn[1], cnt.h_rtn[2], cnt.h_rtn[3], cnt.h_g[0],
+                            cnt.h_g[1],   cnt.h_g[2],   cnt.h_g[3]};
+    unsigned long long* dst = reinterpret_cast<unsigned long long*>(stats);
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      if (!GUIDED && k > 0) break;
+      const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, v[k]);
+      if ((threadIdx.x & 31) == 0 && tot) atomicAdd(dst + k, (unsigned long long)tot);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launch planning: persistent grids of (occupancy x SM count) CTAs, each
+// owning a contiguous range of steps
+// ---------------------------------------------------------------------------
+
+struct Plan {
+  int grid;
+  uint32_t steps_per_cta;
+};
+
+int occupancy_of(const void* kernel) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(kernel);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (n < 1) n = 1;
+  cache[kernel] = n;
+  return n;
+}
+
+Plan plan_for(const void* kernel, int64_t nsteps, int sm_count) {
+  int64_t g = (int64_t)sm_count * occupancy_of(kernel);
+  if (nsteps < g) g = nsteps;
+  if (g < 1) g = 1;
+  Plan p;
+  p.grid = (int)g;
+  p.steps_per_cta = (uint32_t)((nsteps + g - 1) / g);
+  return p;
+}
+
+int64_t steps_of(int64_t nchunks, int64_t per_step) { return (nchunks + per_step - 1) / per_step; }
+
+template <int KIND, bool MASK, bool CODES, bool STATS>
+cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegParam& seg_r,
+                      int sm_count, cudaStream_t st) {
+  auto kern = k_fakequant<KIND, MASK, CODES, STATS>;
+  const Plan p = plan_for((const void*)kern, steps_of(a.nchunks, kThreads), sm_count);
+  kern<<<p.grid, kThreads, 0, st>>>((const uint8_t*)a.x, (uint32_t)a.nchunks,
+                                    FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
+                                    seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
+                                    a.gs_r, (uint8_t*)a.y, (uint8_t*)a.mask,
+                                    (uint8_t*)a.codes_t, a.stats);
+  return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t fq_dispatch(const FakequantArgs& a, const SegParam& t, const SegParam& r, int sm,
+                        cudaStream_t st) {
+  const int sel = ((a.mask != nullptr) << 2) | ((a.codes_t != nullptr) << 1) | (a.stats != nullptr);
+  switch (sel) {
+    case 0: return fq_launch<KIND, false, false, false>(a, t, r, sm, st);
+    case 1: return fq_launch<KIND, false, false, true>(a, t, r, sm, st);
+    case 2: return fq_launch<KIND, false, true, false>(a, t, r, sm, st);
+    case 3: return fq_launch<KIND, false, true, true>(a, t, r, sm, st);
+    case 4: return fq_launch<KIND, true, false, false>(a, t, r, sm, st);
+    case 5: return fq_launch<KIND, true, false, true>(a, t, r, sm, st);
+    case 6: return fq_launch<KIND, true, true, false>(a, t, r, sm, st);
+    default: return fq_launch<KIND, true, true, true>(a, t, r, sm, st);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
+                        const Scratch& s, float* gs_out, int sm_count, cudaStream_t st) {
+  const Plan p = plan_for((const void*)k_amax, steps_of(nchunks, kThreads), sm_count);
+  k_amax<<<p.grid, kThreads, 0, st>>>((const uint8_t*)x, (uint32_t)nchunks,
+                                      FastDivU((uint32_t)cpr), p.steps_per_cta, seg,
+                                      s.amax_bits, s.done, gs_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
+                                 const SegParam& seg, const float* gs, void* codes, void* bs,
+                                 uint32_t* guide, int sm_count, cudaStream_t st) {
+  const Plan p = plan_for((const void*)k_rollout_quant, steps_of(nchunks, kThreads), sm_count);
+  k_rollout_quant<<<p.grid, kThreads, 0, st>>>((const uint8_t*)x, (uint32_t)nchunks,
+                                               FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
+                                               (uint8_t*)codes, (uint8_t*)bs, (uint8_t*)guide);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,
+                              int sm_count, cudaStream_t st) {
+  const Plan p = plan_for((const void*)k_guide_pack,
+                          steps_of(nchunks, (int64_t)kThreads * kPackPerThread), sm_count);
+  k_guide_pack<<<p.grid, kThreads, 0, st>>>((const uint8_t*)codes, (uint32_t)nchunks,
+                                            p.steps_per_cta, (uint8_t*)guide);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_guide_unpack(const void* x_ref, const uint32_t* guide, const void* bs_r,
+                                const float* gs_r, int64_t nchunks, int32_t cpr,
+                                const SegParam& seg_r, void* codes, int sm_count,
+                                cudaStream_t st) {
+  const Plan p = plan_for((const void*)k_guide_unpack, steps_of(nchunks, kThreads), sm_count);
+  k_guide_unpack<<<p.grid, kThreads, 0, st>>>(
+      (const uint8_t*)x_ref, (const uint8_t*)guide, (const uint8_t*)bs_r, gs_r,
+      (uint32_t)nchunks, FastDivU((uint32_t)cpr), p.steps_per_cta, seg_r, (uint8_t*)codes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
+                             const SegParam& seg_r, int sm_count, cudaStream_t st) {
+  switch (a.kind) {
+    case TRACE_GUIDE_FULL: return fq_dispatch<TRACE_GUIDE_FULL>(a, seg_t, seg_r, sm_count, st);
+    case TRACE_GUIDE_COMPACT:
+      return fq_dispatch<TRACE_GUIDE_COMPACT>(a, seg_t, seg_r, sm_count, st);
+    default: return fq_dispatch<TRACE_GUIDE_NONE>(a, seg_t, seg_r, sm_count, st);
+  }
+}
+
+}  // namespace tfp4

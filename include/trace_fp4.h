@@ -1,0 +1,216 @@
+/*
+ * trace_fp4.h - C ABI of libtrace_fp4.so, the GB300 (sm_103a) hot path of
+ * TRACE: rollout-side NVFP4 quantisation with a compact guidance record, and
+ * training-side rollout-guided FP4 fake quantisation.
+ *
+ * Sources (page title, section):
+ *   [EN] "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts"
+ *     - "Why Does FP4 Rollout 'Break' RL Training?", worked example after
+ *       Fig. 1: nearly equal train/rollout values that share a global and a
+ *       block scale can round to different E2M1 points (60.24 -> 3,
+ *       59.76 -> 2, gap amplified to 24).
+ *     - "TRACE Core Concept", first design (before Fig. 3): rollout records the
+ *       FP4 results of routed-expert activations and KV states; training-side
+ *       fake quantisation picks, of the two adjacent E2M1 points, the one
+ *       closer to the rollout's actual point instead of plain RTN.
+ *     - "TRACE Core Concept", second design (after Fig. 3): full records are
+ *       costly to move GPU -> CPU -> disk -> GPU; over 99% of mismatches are
+ *       one codebook entry apart, so a little mantissa information plus the
+ *       scale suffices to set the rounding direction.
+ *   Number formats: OCP Microscaling Formats v1.0 (FP4 E2M1, FP8 E4M3);
+ *   NVFP4 two-level scaling (FP32 tensor scale, E4M3 scale per 16 values).
+ *
+ * Common conventions
+ *   - Tensors are row-major [rows, cols] with cols % 32 == 0 and cols > 0;
+ *     rows == 0 is an empty, valid input.  rows * cols / 32 must stay below
+ *     2^31 and rows below 2^31.  A "block" is 16 consecutive elements of a row.
+ *   - bf16 values are passed as raw 16-bit patterns.
+ *   - Packed E2M1 codes: uint8 [rows, cols/2]; element 2i is the low nibble
+ *     of byte i; nibble = (sign << 3) | m, m = 0..7 indexes the magnitudes
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  The sign is always the input's sign.
+ *   - Block scales: uint8 E4M3 codes [rows, cols/16], plain row-major (not
+ *     the tensor-core scale-factor swizzle).
+ *   - Global scales: float [n_seg], gs = amax / (6 * 448) per segment.
+ *   - Compact guide: uint32 [rows, cols/16]; for element j of a block, bit j
+ *     is its sign and bit 16+j the low bit of its E2M1 index (the single
+ *     mantissa bit).
+ *   - STE mask: uint32 [rows, cols/32]; bit j of word w covers element 32w+j
+ *     of the row and is 0 exactly when the element was clipped by the top
+ *     code (S > 0 and |x| > 6*S), else 1.
+ *   - Segments: a host array of n_seg + 1 int64 row offsets with [0] == 0,
+ *     [n_seg] == rows, non-decreasing (empty segments allowed), at most
+ *     TRACE_MAX_SEGMENTS segments.  row_offsets == NULL means one segment
+ *     over all rows.  The table travels in the kernel's parameter block; the
+ *     caller may free it as soon as the call returns.
+ *   - All tensor pointers are caller-owned DEVICE pointers on the handle's
+ *     device, 16-byte aligned.  Calls enqueue work on `stream` and never
+ *     synchronise the host.  Global scales never leave the device.
+ *   - Errors: argument errors return before anything is enqueued.  A failed
+ *     launch returns TRACE_ERR_CUDA and the raw cudaError_t is available from
+ *     trace_last_cuda_error.  Nothing aborts and no exception crosses the ABI.
+ *   - Threading: one host thread at a time per handle.  Calls through one
+ *     handle on different streams are ordered on the handle's scratch with
+ *     an internal event, so they run one after another on the GPU.
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified codes but never
+ *     fault.
+ *
+ * Arithmetic (shared by every entry point; each step is binary32 with round
+ * to nearest even, no fused multiply-add, subnormals kept):
+ *   amax  = max |x| over the segment;  gs = amax / 2688 (0 if amax == 0)
+ *   bs    = E4M3_rne_satfinite(block_amax / (gs * 6))   (0 if gs == 0)
+ *   S     = decode(bs) * gs;  inv = 1 / S, or 0 when S == 0 or 1/S overflows
+ *   t     = |x| * inv;  RTN index = nearest E2M1 magnitude, ties to the even
+ *           index, t > 6 -> 7;  bracket {lo, hi} = the adjacent points of t
+ */
+#ifndef TRACE_FP4_H
+#define TRACE_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct trace_ctx* trace_handle_t;
+typedef struct CUstream_st* trace_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  TRACE_OK = 0,
+  TRACE_ERR_INVALID_ARG = 1,        /* null pointer, bad shape or segment table */
+  TRACE_ERR_ALIGNMENT = 2,          /* a tensor pointer is not 16-byte aligned   */
+  TRACE_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or not compute capability 10.3 */
+  TRACE_ERR_CUDA = 4,               /* a CUDA call failed; see trace_last_cuda_error */
+  TRACE_ERR_OOM = 5,                /* device scratch could not be allocated     */
+  TRACE_ERR_TIMEOUT = 6             /* reserved: a bounded device wait gave up   */
+} trace_status_t;
+
+typedef enum {
+  TRACE_GUIDE_NONE = 0,    /* plain RTN fake quantisation                    */
+  TRACE_GUIDE_FULL = 1,    /* guide = rollout codes uint8 [rows, cols/2]     */
+  TRACE_GUIDE_COMPACT = 2  /* guide = compact words uint32 [rows, cols/16]   */
+} trace_guide_kind_t;
+
+#define TRACE_MAX_SEGMENTS 4000
+
+typedef struct {
+  const int64_t* row_offsets; /* host array [n_seg + 1], or NULL for one segment */
+  int32_t n_seg;              /* ignored when row_offsets == NULL                */
+} trace_segments_t;
+
+/* Train/rollout code agreement counters, accumulated (never cleared) by
+ * trace_train_fakequant.  Signed index k = sign ? -m : m (so +0 == -0); a
+ * mismatch is k_train != k_rollout.  hist_* count |dk| = 0, 1, 2, >= 3.
+ * With TRACE_GUIDE_NONE only n_elems advances. */
+typedef struct {
+  uint64_t n_elems;
+  uint64_t mismatch_rtn;
+  uint64_t mismatch_guided;
+  uint64_t hist_rtn[4];
+  uint64_t hist_guided[4];
+} trace_stats_t;
+
+/* Kernel identifiers for the built-in profiler. */
+typedef enum {
+  TRACE_KERNEL_AMAX = 0,
+  TRACE_KERNEL_ROLLOUT_QUANT = 1,
+  TRACE_KERNEL_GUIDE_PACK = 2,
+  TRACE_KERNEL_GUIDE_UNPACK = 3,
+  TRACE_KERNEL_FAKEQUANT = 4,
+  TRACE_KERNEL_COUNT = 5
+} trace_kernel_id_t;
+
+typedef struct {
+  uint64_t launches; /* launches timed since the last collect        */
+  double total_ms;   /* summed CUDA-event time of those launches     */
+} trace_kernel_time_t;
+
+/* Creates a handle on `device`: checks for compute capability 10.3 and
+ * allocates the device scratch (per-segment amax words, a completion ticket,
+ * per-segment training global scales).  *out is NULL on failure. */
+trace_status_t trace_create(trace_handle_t* out, int device);
+
+/* Frees the handle.  The caller must have finished (synchronised) all work
+ * enqueued through it.  NULL is accepted. */
+trace_status_t trace_destroy(trace_handle_t h);
+
+/* Static text for a status code. */
+const char* trace_status_string(trace_status_t s);
+
+/* Raw cudaError_t of the last TRACE_ERR_CUDA on this handle (0 if none). */
+int trace_last_cuda_error(trace_handle_t h);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int trace_version(void);
+
+/* Rollout-side quantisation ([EN] "TRACE Core Concept", first and second
+ * designs): per-segment amax and global scale, per-block E4M3 scale, per-
+ * element RTN E2M1 code, and (if guide_bits != NULL) the compact guide words.
+ *   x_bf16     [rows, cols] bf16
+ *   codes_u8   [rows, cols/2] out
+ *   bs_e4m3    [rows, cols/16] out
+ *   gs_f32     [n_seg] out (device)
+ *   guide_bits [rows, cols/16] out, nullable
+ * Two kernels: a streaming amax pass, then the quantiser. */
+trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                   int64_t cols, trace_segments_t seg, void* codes_u8,
+                                   void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
+                                   trace_stream_t stream);
+
+/* Full codes -> compact guide words ([EN] "TRACE Core Concept", second
+ * design): keeps each element's sign and index low bit.  Integer only.
+ *   codes_u8 [rows, cols/2] in; guide_bits [rows, cols/16] out. */
+trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,
+                                int64_t cols, uint32_t* guide_bits, trace_stream_t stream);
+
+/* Compact guide words + reference values -> full rollout codes ([EN] "TRACE
+ * Core Concept", second design: the reference value narrows the candidates).
+ * For each element t = |x_ref| * inv_r in the rollout's own scale frame
+ * (S_r = decode(bs_r) * gs_r[segment]); of the two adjacent E2M1 points the
+ * one whose index low bit equals the stored bit is decoded; a point bracket
+ * needs no bit.  The sign comes from the guide.
+ *   x_ref_bf16 [rows, cols]; guide_bits [rows, cols/16]; bs_r [rows, cols/16];
+ *   gs_r [n_seg_r] (device); codes_u8 [rows, cols/2] out. */
+trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
+                                  const uint32_t* guide_bits, const void* bs_r,
+                                  const float* gs_r, trace_segments_t seg_r, int64_t rows,
+                                  int64_t cols, void* codes_u8, trace_stream_t stream);
+
+/* Training-side rollout-guided fake quantisation ([EN] "TRACE Core Concept",
+ * first design).  The training tensor uses its own scales (segments seg_t).
+ * Each element is restricted to its bracket {lo, hi}; the candidate whose
+ * dequantised value (with the training scale) is closer to the rollout's
+ * reconstructed value (rollout code with the rollout scale; decoded from the
+ * compact word against x itself when kind == COMPACT) is chosen; equal
+ * distances, a point bracket or kind == NONE give RTN.
+ *   x_bf16 [rows, cols]
+ *   guide: codes uint8 [rows, cols/2] (FULL) or words uint32 [rows, cols/16]
+ *          (COMPACT); ignored for NONE
+ *   bs_r [rows, cols/16], gs_r [n_seg_r] (device), seg_r: the rollout's
+ *          scales; ignored for NONE
+ *   y_bf16 [rows, cols] out: +-G[m] * S_t rounded to bf16
+ *   ste_mask [rows, cols/32] out, nullable
+ *   codes_t_u8 [rows, cols/2] out, nullable: the chosen training codes
+ *   stats_dev: device trace_stats_t, nullable, accumulated atomically
+ * Two kernels: the amax pass over x, then the fused fake quantiser. */
+trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                     int64_t cols, trace_segments_t seg_t,
+                                     trace_guide_kind_t kind, const void* guide,
+                                     const void* bs_r, const float* gs_r,
+                                     trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
+                                     void* codes_t_u8, trace_stats_t* stats_dev,
+                                     trace_stream_t stream);
+
+/* Built-in profiler.  While enabled, every kernel launch through the handle
+ * is bracketed by CUDA events on its own stream.  trace_profile_collect
+ * waits for the recorded events, writes per-kernel launch counts and summed
+ * milliseconds into out[TRACE_KERNEL_COUNT] and clears the record.  At most
+ * 4096 launches are kept between collects; later ones are not timed. */
+trace_status_t trace_profile_enable(trace_handle_t h, int enable);
+trace_status_t trace_profile_collect(trace_handle_t h, trace_kernel_time_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRACE_FP4_H */
