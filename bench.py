@@ -1,0 +1,468 @@
+#!/usr/bin/env python3
+"""Benchmark of the guided-NVFP4 hot path of TRACE on GB300.
+
+One step = one pass of the whole path over one batch of the workload:
+  rollout side:  segment amax + NVFP4 quantisation with the compact record
+  record:        guide pack (codes -> compact words), guide unpack (round trip)
+  training side: segment amax + rollout-guided fake quantisation (bf16 out,
+                 STE mask)
+The default workload is the long-rollout KV stream (48 layers x K/V x 131072
+tokens x 4 heads x 128, 6.44 G elements per tensor, guide in 4096-token
+chunks).  Inputs are synthetic (seeded generators), resident in HBM, and far
+larger than L2, so no flush is needed between steps.
+
+Metric: algorithmic bytes in + out of every kernel of the step per second
+(GB/s = 1e9 B/s); per-kernel GB/s and the HBM-roofline fraction of the
+dominant kernel come from CUDA events recorded by the library around each
+launch on its own stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+                  [--guide compact|full] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain single-threaded
+definition) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "guided NVFP4 fake-quant GB/s (bytes in+out) and % of GB300 HBM peak"
+# algorithmic bytes per element of each kernel (reads + writes)
+KERNEL_BYTES = {"amax": 2.0, "rollout_quant": 2.8125, "guide_pack": 0.75,
+                "guide_unpack": 2.8125, "fakequant_compact": 4.4375, "fakequant_full": 4.6875}
+
+
+def step_bytes_per_elem(guide: str) -> float:
+    fq = KERNEL_BYTES["fakequant_" + guide]
+    return (KERNEL_BYTES["amax"] * 2 + KERNEL_BYTES["rollout_quant"] + KERNEL_BYTES["guide_pack"]
+            + KERNEL_BYTES["guide_unpack"] + fq)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.0)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.3 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "samples": len(sm), "power_w_max": max(power), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, rows):
+    """First `rows` rows of training segment 0 with the rollout segments that
+    fall inside them (drawn on the host by the same generator)."""
+    from fp4_rollout_guided_gb300 import synth
+    x, r = synth.segment_inputs(w, 0, "cpu")
+    rows = min(rows, x.shape[0])
+    cuts = w.seg_r[(w.seg_r > 0) & (w.seg_r < rows)]
+    seg_r = np.concatenate([[0], cuts, [rows]]).astype(np.int64)
+    return synth.to_u16(x[:rows]), synth.to_u16(r[:rows]), seg_r
+
+
+def oracle_step(xu, ru, seg_r, guide_kind):
+    import oracle
+    codes, bs, gs, guide = oracle.rollout_quant(ru, seg_r)
+    oracle.guide_pack(codes)
+    oracle.guide_unpack(ru, guide, bs, gs, seg_r)
+    kind = oracle.GUIDE_COMPACT if guide_kind == "compact" else oracle.GUIDE_FULL
+    oracle.train_fakequant(xu, None, kind, guide if guide_kind == "compact" else codes, bs, gs,
+                           seg_r, want_codes=False, want_stats=False)
+
+
+def oracle_rows_for(w, seconds, guide_kind):
+    """Rows of a sample that takes about `seconds` of oracle time."""
+    probe = max(w.seg_r[1] - w.seg_r[0], 1) if w.n_seg_r > 1 else 256
+    probe = int(min(probe, 4096 if w.cols <= 256 else 256))
+    xu, ru, sr = oracle_sample(w, probe)
+    t = time.perf_counter()
+    oracle_step(xu, ru, sr, guide_kind)
+    dt = max(time.perf_counter() - t, 1e-3)
+    rows = int(probe * seconds / dt)
+    quantum = int(w.seg_r[1] - w.seg_r[0]) if w.n_seg_r > 1 else 1
+    quantum = max(1, min(quantum, 4096))
+    rows = max(quantum, rows // quantum * quantum)
+    return rows
+
+
+def cpu_baseline(w, guide_kind, seconds=12.0):
+    import oracle
+    oracle.build()
+    rows = oracle_rows_for(w, seconds, guide_kind)
+    xu, ru, sr = oracle_sample(w, rows)
+    t = time.perf_counter()
+    oracle_step(xu, ru, sr, guide_kind)
+    dt = time.perf_counter() - t
+    elems = xu.size
+    gbs = step_bytes_per_elem(guide_kind) * elems / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows} of training segment 0 ({elems} elements, "
+                      f"{len(sr) - 1} rollout segments), one full step, {dt:.2f} s"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    rows = oracle_rows_for(w, 1.5, args.guide)
+    xu, ru, sr = oracle_sample(w, rows)
+    for _ in range(args.warmup):
+        oracle_step(xu, ru, sr, args.guide)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(xu, ru, sr, args.guide)
+    dt = (time.perf_counter() - t) / max(args.steps, 1)
+    value = step_bytes_per_elem(args.guide) * xu.size / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "sample_rows": rows, "sample_elements": int(xu.size)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: rows 0..{rows} of training segment 0 "
+                                       f"({xu.size} elements)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU path
+# ---------------------------------------------------------------------------
+
+def mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_ours(args, w0):
+    from fp4_rollout_guided_gb300 import build, shard, synth, trace
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, True)
+    build.build()
+    plan = shard.weak_plan(world, rank, args.seed)
+    w = synth.workload(w0.cfg, seed=plan.seed)
+    elems = w.elems
+    h = trace.Handle(local)
+
+    t_gen = time.perf_counter()
+    x, r = synth.make_inputs(w, dev)
+    rows, cols = w.rows, w.cols
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    bs = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+    gs = torch.empty((w.n_seg_r,), dtype=torch.float32, device=dev)
+    guide = torch.empty((rows, cols // 16), dtype=torch.int32, device=dev)
+    packed = torch.empty_like(guide)
+    unpacked = torch.empty_like(codes)
+    y = torch.empty_like(x)
+    mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
+    kind = args.guide
+
+    def step(xd, rd, stats=None):
+        h.rollout_quant(rd, w.seg_r, out=(codes, bs, gs, guide))
+        h.guide_pack(codes, out=packed)
+        h.guide_unpack(rd, guide, bs, gs, w.seg_r, out=unpacked)
+        h.train_fakequant(xd, w.seg_t, kind, guide if kind == "compact" else codes, bs, gs,
+                          w.seg_r, out=(y, mask, None), stats=stats)
+
+    # correctness guard: the round trip of the record and stats of one step
+    st = trace.new_stats(dev)
+    step(x, r, st)
+    torch.cuda.synchronize()
+    stats = trace.stats_dict(st)
+    record_ok = bool(torch.equal(packed, guide) and torch.equal(unpacked, codes))
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        step(x, r)
+    torch.cuda.synchronize()
+    barrier(dist)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(x, r)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = ev0.elapsed_time(ev1) / max(args.steps, 1)
+    ms = max_over_ranks(dist, ms, dev)
+
+    # per-kernel times from the library's own events, same steps again
+    h.profile(True)
+    for _ in range(args.steps):
+        step(x, r)
+    times = h.collect()
+    h.profile(False)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+
+    launches = sum(n for n, _ in times.values())
+    bpe = step_bytes_per_elem(kind)
+    value = bpe * elems * world / (ms * 1e-3) / 1e9
+    peak, peak_src = load_peaks()
+    kernels = {}
+    for name, (n, tot) in times.items():
+        if n == 0:
+            continue
+        b = KERNEL_BYTES["fakequant_" + kind] if name == "fakequant" else KERNEL_BYTES[name]
+        avg = tot / n
+        gbs = b * elems / (avg * 1e-3) / 1e9
+        kernels[name] = {"launches": n, "avg_ms": round(avg, 4), "bytes_per_elem": b,
+                         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+    dom = max(kernels, key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
+    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+            "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / peak, 4),
+            "traffic": None, "peak_source": peak_src}
+
+    e2e = measure_e2e(args, h, w, x, r, step, dev, bpe, (y, mask, guide, bs, gs)) \
+        if not args.no_e2e else None
+    e2e_v = None if e2e is None else max_over_ranks(dist, e2e["ms"], dev)
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(w, kind)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "elements_per_gpu": elems,
+                       "segments_train": w.n_seg_t, "segments_rollout": w.n_seg_r,
+                       "guide": kind, "step": "amax+rollout_quant, guide_pack, guide_unpack, "
+                                              "amax+guided_fakequant",
+                       "step_bytes_per_elem": bpe,
+                       "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": f"replica-per-gpu x{world}"},
+            "percent_of_hbm_peak": round(100 * value / world / peak, 2),
+            "kernels": kernels, "roofline": roof, "gpu_launches": launches,
+            "clocks": clk, "cpu_baseline": base,
+            "e2e": None if e2e is None else {
+                "value": round(bpe * e2e["elems"] * world / (e2e_v * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_v, 3), "scope": e2e["scope"]},
+            "mismatch": {"rtn_rate": stats["mismatch_rtn"] / max(stats["n_elems"], 1),
+                         "guided_rate": stats["mismatch_guided"] / max(stats["n_elems"], 1),
+                         "hist_rtn": stats["hist_rtn"], "hist_guided": stats["hist_guided"]},
+            "record_round_trip_ok": record_ok,
+            "generation_s": round(t_gen, 2),
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(args, h, w, x, r, step, dev, bpe, outs):
+    """Same step through the public API with the inputs in pinned host memory:
+    H2D of x and r, the step, D2H of y, the STE mask and the compact record
+    (words, block scales, global scales), all inside the timed region."""
+    y, mask, guide, bs, gs = outs
+    in_bytes = x.numel() * 2 * 2
+    out_bytes = sum(t.numel() * t.element_size() for t in (y, mask, guide, bs, gs))
+    need = in_bytes + out_bytes
+    avail = mem_available_bytes()
+    scope = "whole workload"
+    rows = w.rows
+    if avail and need * 1.6 > avail:
+        # keep pinned memory within the host's means: a leading row range of
+        # whole training segments (same kernels, fewer rows)
+        frac = avail / (need * 1.6)
+        k = max(1, int(w.n_seg_t * frac))
+        rows = int(w.seg_t[k])
+        scope = f"first {k} of {w.n_seg_t} training segments (host memory)"
+    if rows != w.rows:
+        return None if rows == 0 else _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope)
+    return _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope, step=step, outs=outs)
+
+
+def _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope, step=None, outs=None):
+    xs, rs = x[:rows], r[:rows]
+    x_h = torch.empty(xs.shape, dtype=xs.dtype, pin_memory=True)
+    r_h = torch.empty(rs.shape, dtype=rs.dtype, pin_memory=True)
+    x_h.copy_(xs)
+    r_h.copy_(rs)
+    if step is None:
+        from fp4_rollout_guided_gb300 import synth
+        sub = synth.Workload(w.name, w.cfg, rows, w.cols, w.seg_t[w.seg_t <= rows],
+                             w.seg_r[w.seg_r <= rows], w.sigma, w.seed, w.kind)
+        cols = w.cols
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        bs = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+        gs = torch.empty((sub.n_seg_r,), dtype=torch.float32, device=dev)
+        guide = torch.empty((rows, cols // 16), dtype=torch.int32, device=dev)
+        packed = torch.empty_like(guide)
+        unpacked = torch.empty_like(codes)
+        y = torch.empty_like(xs)
+        mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
+
+        def step(xd, rd, stats=None):
+            h.rollout_quant(rd, sub.seg_r, out=(codes, bs, gs, guide))
+            h.guide_pack(codes, out=packed)
+            h.guide_unpack(rd, guide, bs, gs, sub.seg_r, out=unpacked)
+            h.train_fakequant(xd, sub.seg_t, args.guide,
+                              guide if args.guide == "compact" else codes, bs, gs, sub.seg_r,
+                              out=(y, mask, None))
+        outs = (y, mask, guide, bs, gs)
+    y, mask, guide, bs, gs = outs
+    host_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    xd, rd = xs, rs
+
+    def e2e_step():
+        xd.copy_(x_h, non_blocking=True)
+        rd.copy_(r_h, non_blocking=True)
+        step(xd, rd)
+        for hst, dv in zip(host_outs, outs):
+            hst.copy_(dv, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    h2d = x_h.numel() * 2 + r_h.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in host_outs)
+    return {"ms": ms, "elems": rows * w.cols, "h2d": h2d, "d2h": d2h, "scope": scope}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--guide", default="compact", choices=["compact", "full"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    from fp4_rollout_guided_gb300 import synth
+    w = synth.workload(args.workload, seed=args.seed)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

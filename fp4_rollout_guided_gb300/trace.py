@@ -1,0 +1,270 @@
+"""Thin ctypes binding over ``libtrace_fp4.so`` (include/trace_fp4.h).
+
+Argument marshalling only: every step of the path runs in the library's
+sm_103a kernels.  PyTorch supplies device memory and the current CUDA stream.
+If the library has not been built, or no compute capability 10.3 GPU is
+present, calls raise :class:`TraceError`; there is no fallback path.
+
+Tensor dtypes: bf16 inputs are ``torch.bfloat16``; codes and block scales
+are ``torch.uint8``; compact words and STE masks are ``torch.int32`` holding
+the unsigned 32-bit patterns; global scales are ``torch.float32``; the
+statistics block is ``torch.int64[11]`` (the layout of ``trace_stats_t``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
+_KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
+KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant")
+MAX_SEGMENTS = 4000
+STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
+          4: "CUDA error", 5: "out of memory", 6: "timeout"}
+
+
+class TraceError(RuntimeError):
+    def __init__(self, where: str, status: int, cuda_error: int = 0):
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if cuda_error:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+        self.status = status
+        self.cuda_error = cuda_error
+
+
+class Segments(ctypes.Structure):
+    _fields_ = [("row_offsets", ctypes.c_void_p), ("n_seg", ctypes.c_int32)]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_uint64), ("total_ms", ctypes.c_double)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+# name -> (restype, argtypes); every symbol the header declares
+P, I64, I32, INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+SIGNATURES = {
+    "trace_create": (INT, [ctypes.POINTER(ctypes.c_void_p), INT]),
+    "trace_destroy": (INT, [P]),
+    "trace_status_string": (ctypes.c_char_p, [INT]),
+    "trace_last_cuda_error": (INT, [P]),
+    "trace_version": (INT, []),
+    "trace_rollout_quant": (INT, [P, P, I64, I64, Segments, P, P, P, P, P]),
+    "trace_guide_pack": (INT, [P, P, I64, I64, P, P]),
+    "trace_guide_unpack": (INT, [P, P, P, P, P, Segments, I64, I64, P, P]),
+    "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
+                                    P, P, P]),
+    "trace_profile_enable": (INT, [P, INT]),
+    "trace_profile_collect": (INT, [P, ctypes.POINTER(KernelTime)]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library; raises TraceError if it was never built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise TraceError(f"libtrace_fp4.so missing at {path}; build it with "
+                                 "__graft_entry__.build()", 3)
+            so = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(so, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = so
+        return _lib
+
+
+def _segments(seg, rows, keep: list) -> Segments:
+    if seg is None:
+        return Segments(None, 1)
+    arr = np.ascontiguousarray(np.asarray(seg, dtype=np.int64))
+    keep.append(arr)
+    return Segments(arr.ctypes.data, len(arr) - 1)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, shape, name, device):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got "
+                         f"{t.dtype} {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got {t.device}")
+
+
+class Handle:
+    """One library handle on one CUDA device (owns a small device scratch)."""
+
+    def __init__(self, device: Optional[int] = None):
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device_index = int(device)
+        self.device = torch.device("cuda", self.device_index)
+        h = ctypes.c_void_p()
+        st = lib().trace_create(ctypes.byref(h), self.device_index)
+        if st != 0:
+            raise TraceError("trace_create", st)
+        self._h = h
+
+    # -- life cycle ----------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            torch.cuda.synchronize(self.device)
+            lib().trace_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            if getattr(self, "_h", None):
+                lib().trace_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+    def _check(self, where, st):
+        if st != 0:
+            raise TraceError(where, st, lib().trace_last_cuda_error(self._h))
+
+    # -- a1 + a2 ---------------------------------------------------------------
+    def rollout_quant(self, x: torch.Tensor, seg=None, *, guide: bool = True, out=None):
+        """-> (codes uint8[rows, cols/2], bs uint8[rows, cols/16],
+        gs float32[n_seg], guide int32[rows, cols/16] or None)."""
+        rows, cols = x.shape
+        n_seg = 1 if seg is None else len(seg) - 1
+        if out is None:
+            out = (torch.empty((rows, cols // 2), dtype=torch.uint8, device=self.device),
+                   torch.empty((rows, cols // 16), dtype=torch.uint8, device=self.device),
+                   torch.empty((n_seg,), dtype=torch.float32, device=self.device),
+                   torch.empty((rows, cols // 16), dtype=torch.int32, device=self.device)
+                   if guide else None)
+        codes, bs, gs, gd = out
+        _need(x, torch.bfloat16, (rows, cols), "x", self.device)
+        _need(codes, torch.uint8, (rows, cols // 2), "codes", self.device)
+        _need(bs, torch.uint8, (rows, cols // 16), "bs", self.device)
+        _need(gs, torch.float32, (n_seg,), "gs", self.device)
+        if gd is not None:
+            _need(gd, torch.int32, (rows, cols // 16), "guide", self.device)
+        keep = []
+        st = lib().trace_rollout_quant(self._h, _ptr(x), rows, cols, _segments(seg, rows, keep),
+                                       _ptr(codes), _ptr(bs), _ptr(gs), _ptr(gd), _stream())
+        self._check("trace_rollout_quant", st)
+        return codes, bs, gs, gd
+
+    # -- a3 ----------------------------------------------------------------------
+    def guide_pack(self, codes: torch.Tensor, out: Optional[torch.Tensor] = None):
+        rows, half = codes.shape
+        cols = half * 2
+        if out is None:
+            out = torch.empty((rows, cols // 16), dtype=torch.int32, device=self.device)
+        _need(codes, torch.uint8, (rows, half), "codes", self.device)
+        _need(out, torch.int32, (rows, cols // 16), "guide", self.device)
+        st = lib().trace_guide_pack(self._h, _ptr(codes), rows, cols, _ptr(out), _stream())
+        self._check("trace_guide_pack", st)
+        return out
+
+    # -- a4 ----------------------------------------------------------------------
+    def guide_unpack(self, x_ref, guide, bs_r, gs_r, seg_r=None, out=None):
+        rows, cols = x_ref.shape
+        if out is None:
+            out = torch.empty((rows, cols // 2), dtype=torch.uint8, device=self.device)
+        _need(x_ref, torch.bfloat16, (rows, cols), "x_ref", self.device)
+        _need(guide, torch.int32, (rows, cols // 16), "guide", self.device)
+        _need(bs_r, torch.uint8, (rows, cols // 16), "bs_r", self.device)
+        _need(out, torch.uint8, (rows, cols // 2), "codes", self.device)
+        keep = []
+        st = lib().trace_guide_unpack(self._h, _ptr(x_ref), _ptr(guide), _ptr(bs_r), _ptr(gs_r),
+                                      _segments(seg_r, rows, keep), rows, cols, _ptr(out),
+                                      _stream())
+        self._check("trace_guide_unpack", st)
+        return out
+
+    # -- a5 + a6 -----------------------------------------------------------------
+    def train_fakequant(self, x, seg_t=None, kind="none", guide=None, bs_r=None, gs_r=None,
+                        seg_r=None, *, mask: bool = True, codes: bool = False,
+                        stats: Optional[torch.Tensor] = None, out=None):
+        """-> (y bf16[rows, cols], mask int32[rows, cols/32] or None,
+        codes uint8[rows, cols/2] or None, stats)."""
+        k = _KINDS[kind] if isinstance(kind, str) else int(kind)
+        rows, cols = x.shape
+        if out is None:
+            out = (torch.empty((rows, cols), dtype=torch.bfloat16, device=self.device),
+                   torch.empty((rows, cols // 32), dtype=torch.int32, device=self.device)
+                   if mask else None,
+                   torch.empty((rows, cols // 2), dtype=torch.uint8, device=self.device)
+                   if codes else None)
+        y, m, c = out
+        _need(x, torch.bfloat16, (rows, cols), "x", self.device)
+        _need(y, torch.bfloat16, (rows, cols), "y", self.device)
+        if m is not None:
+            _need(m, torch.int32, (rows, cols // 32), "mask", self.device)
+        if c is not None:
+            _need(c, torch.uint8, (rows, cols // 2), "codes_t", self.device)
+        if stats is not None:
+            _need(stats, torch.int64, (11,), "stats", self.device)
+        if k != GUIDE_NONE:
+            if k == GUIDE_FULL:
+                _need(guide, torch.uint8, (rows, cols // 2), "guide", self.device)
+            else:
+                _need(guide, torch.int32, (rows, cols // 16), "guide", self.device)
+            _need(bs_r, torch.uint8, (rows, cols // 16), "bs_r", self.device)
+        keep = []
+        st = lib().trace_train_fakequant(
+            self._h, _ptr(x), rows, cols, _segments(seg_t, rows, keep), k, _ptr(guide),
+            _ptr(bs_r), _ptr(gs_r), _segments(seg_r, rows, keep), _ptr(y), _ptr(m), _ptr(c),
+            _ptr(stats), _stream())
+        self._check("trace_train_fakequant", st)
+        return y, m, c, stats
+
+    # -- profiler ---------------------------------------------------------------
+    def profile(self, enable: bool = True):
+        self._check("trace_profile_enable", lib().trace_profile_enable(self._h, int(enable)))
+
+    def collect(self) -> dict:
+        arr = (KernelTime * len(KERNELS))()
+        self._check("trace_profile_collect", lib().trace_profile_collect(self._h, arr))
+        return {name: (int(arr[i].launches), float(arr[i].total_ms))
+                for i, name in enumerate(KERNELS)}
+
+
+def new_stats(device) -> torch.Tensor:
+    return torch.zeros(11, dtype=torch.int64, device=device)
+
+
+def stats_dict(stats: torch.Tensor) -> dict:
+    v = stats.cpu().numpy().astype(np.uint64)
+    return {"n_elems": int(v[0]), "mismatch_rtn": int(v[1]), "mismatch_guided": int(v[2]),
+            "hist_rtn": [int(a) for a in v[3:7]], "hist_guided": [int(a) for a in v[7:11]]}
+
+
+__all__: Sequence[str] = ["Handle", "TraceError", "lib", "library_path", "new_stats",
+                          "stats_dict", "GUIDE_NONE", "GUIDE_FULL", "GUIDE_COMPACT",
+                          "KERNELS", "SIGNATURES", "MAX_SEGMENTS"]

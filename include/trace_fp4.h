@@ -68,6 +68,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define TRACE_API __attribute__((visibility("default")))
+#else
+#define TRACE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -128,20 +134,20 @@ typedef struct {
 /* Creates a handle on `device`: checks for compute capability 10.3 and
  * allocates the device scratch (per-segment amax words, a completion ticket,
  * per-segment training global scales).  *out is NULL on failure. */
-trace_status_t trace_create(trace_handle_t* out, int device);
+TRACE_API trace_status_t trace_create(trace_handle_t* out, int device);
 
 /* Frees the handle.  The caller must have finished (synchronised) all work
  * enqueued through it.  NULL is accepted. */
-trace_status_t trace_destroy(trace_handle_t h);
+TRACE_API trace_status_t trace_destroy(trace_handle_t h);
 
 /* Static text for a status code. */
-const char* trace_status_string(trace_status_t s);
+TRACE_API const char* trace_status_string(trace_status_t s);
 
 /* Raw cudaError_t of the last TRACE_ERR_CUDA on this handle (0 if none). */
-int trace_last_cuda_error(trace_handle_t h);
+TRACE_API int trace_last_cuda_error(trace_handle_t h);
 
 /* Library version as major*10000 + minor*100 + patch. */
-int trace_version(void);
+TRACE_API int trace_version(void);
 
 /* Rollout-side quantisation ([EN] "TRACE Core Concept", first and second
  * designs): per-segment amax and global scale, per-block E4M3 scale, per-
@@ -152,7 +158,7 @@ int trace_version(void);
  *   gs_f32     [n_seg] out (device)
  *   guide_bits [rows, cols/16] out, nullable
  * Two kernels: a streaming amax pass, then the quantiser. */
-trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
+TRACE_API trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
                                    int64_t cols, trace_segments_t seg, void* codes_u8,
                                    void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
                                    trace_stream_t stream);
@@ -160,7 +166,7 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
 /* Full codes -> compact guide words ([EN] "TRACE Core Concept", second
  * design): keeps each element's sign and index low bit.  Integer only.
  *   codes_u8 [rows, cols/2] in; guide_bits [rows, cols/16] out. */
-trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,
+TRACE_API trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,
                                 int64_t cols, uint32_t* guide_bits, trace_stream_t stream);
 
 /* Compact guide words + reference values -> full rollout codes ([EN] "TRACE
@@ -171,7 +177,7 @@ trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t 
  * needs no bit.  The sign comes from the guide.
  *   x_ref_bf16 [rows, cols]; guide_bits [rows, cols/16]; bs_r [rows, cols/16];
  *   gs_r [n_seg_r] (device); codes_u8 [rows, cols/2] out. */
-trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
+TRACE_API trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
                                   const uint32_t* guide_bits, const void* bs_r,
                                   const float* gs_r, trace_segments_t seg_r, int64_t rows,
                                   int64_t cols, void* codes_u8, trace_stream_t stream);
@@ -193,7 +199,7 @@ trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
  *   codes_t_u8 [rows, cols/2] out, nullable: the chosen training codes
  *   stats_dev: device trace_stats_t, nullable, accumulated atomically
  * Two kernels: the amax pass over x, then the fused fake quantiser. */
-trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
+TRACE_API trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
                                      int64_t cols, trace_segments_t seg_t,
                                      trace_guide_kind_t kind, const void* guide,
                                      const void* bs_r, const float* gs_r,
@@ -206,8 +212,8 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
  * waits for the recorded events, writes per-kernel launch counts and summed
  * milliseconds into out[TRACE_KERNEL_COUNT] and clears the record.  At most
  * 4096 launches are kept between collects; later ones are not timed. */
-trace_status_t trace_profile_enable(trace_handle_t h, int enable);
-trace_status_t trace_profile_collect(trace_handle_t h, trace_kernel_time_t* out);
+TRACE_API trace_status_t trace_profile_enable(trace_handle_t h, int enable);
+TRACE_API trace_status_t trace_profile_collect(trace_handle_t h, trace_kernel_time_t* out);
 
 #ifdef __cplusplus
 }

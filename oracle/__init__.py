@@ -75,6 +75,9 @@ def _load():
             "orc_f32_to_bf16_array": (None, [P, I64, P]),
             "orc_segment_amax": (INT, [P, I64, I64, P, I32, P]),
             "orc_rollout_quant": (INT, [P, I64, I64, P, I32, P, P, P, P]),
+            "orc_rollout_quant_given": (INT, [P, I64, I64, P, I32, P, P, P, P, P]),
+            "orc_train_fakequant_given": (INT, [P, I64, I64, P, I32, P, INT, P, P, P, P,
+                                                I32, P, P, P, P]),
             "orc_guide_pack": (INT, [P, I64, I64, P]),
             "orc_guide_unpack": (INT, [P, P, P, P, P, I32, I64, I64, P]),
             "orc_train_fakequant": (INT, [P, I64, I64, P, I32, INT, P, P, P, P,
@@ -192,9 +195,10 @@ def segment_amax(x, seg=None):
     return out
 
 
-def rollout_quant(x, seg=None, want_guide=True):
+def rollout_quant(x, seg=None, want_guide=True, amax=None):
     """-> codes uint8[rows, cols/2], bs uint8[rows, cols/16], gs float32[n_seg],
-    guide uint32[rows, cols/16] (or None)."""
+    guide uint32[rows, cols/16] (or None).  ``amax`` (float32[n_seg]) replaces
+    the segment maxima of the rows given (for sampled checks)."""
     x = _u16(x)
     rows, cols = x.shape
     s, n = _seg(seg, rows)
@@ -202,8 +206,10 @@ def rollout_quant(x, seg=None, want_guide=True):
     bs = np.zeros((rows, cols // 16), dtype=np.uint8)
     gs = np.zeros(n, dtype=np.float32)
     guide = np.zeros((rows, cols // 16), dtype=np.uint32) if want_guide else None
-    _check(_load().orc_rollout_quant(_ptr(x), rows, cols, _ptr(s), n, _ptr(codes),
-                                     _ptr(bs), _ptr(gs), _ptr(guide)), "rollout_quant")
+    am = None if amax is None else np.ascontiguousarray(amax, dtype=np.float32)
+    _check(_load().orc_rollout_quant_given(_ptr(x), rows, cols, _ptr(s), n, _ptr(am),
+                                           _ptr(codes), _ptr(bs), _ptr(gs), _ptr(guide)),
+           "rollout_quant")
     return codes, bs, gs, guide
 
 
@@ -231,7 +237,7 @@ def guide_unpack(x_ref, guide, bs_r, gs_r, seg_r=None):
 
 def train_fakequant(x, seg_t=None, kind=GUIDE_NONE, guide=None, bs_r=None,
                     gs_r=None, seg_r=None, want_codes=True, want_stats=True,
-                    want_mask=True):
+                    want_mask=True, amax_t=None):
     """-> y uint16[rows, cols] (bf16 bits), mask uint32[rows, cols/32],
     codes_t uint8[rows, cols/2] (or None), stats uint64[11] (or None)."""
     x = _u16(x)
@@ -248,8 +254,10 @@ def train_fakequant(x, seg_t=None, kind=GUIDE_NONE, guide=None, bs_r=None,
     mask = np.zeros((rows, cols // 32), dtype=np.uint32) if want_mask else None
     codes_t = np.zeros((rows, cols // 2), dtype=np.uint8) if want_codes else None
     stats = np.zeros(STAT_COUNT, dtype=np.uint64) if want_stats else None
-    rc = _load().orc_train_fakequant(_ptr(x), rows, cols, _ptr(st), nt, int(kind),
-                                     _ptr(guide), _ptr(bs_r), _ptr(gs_r), _ptr(sr), nr,
-                                     _ptr(y), _ptr(mask), _ptr(codes_t), _ptr(stats))
+    am = None if amax_t is None else np.ascontiguousarray(amax_t, dtype=np.float32)
+    rc = _load().orc_train_fakequant_given(_ptr(x), rows, cols, _ptr(st), nt, _ptr(am),
+                                           int(kind), _ptr(guide), _ptr(bs_r), _ptr(gs_r),
+                                           _ptr(sr), nr, _ptr(y), _ptr(mask), _ptr(codes_t),
+                                           _ptr(stats))
     _check(rc, "train_fakequant")
     return y, mask, codes_t, stats

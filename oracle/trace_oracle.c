@@ -307,6 +307,12 @@ static float block_amax(const uint16_t* xb) {
 int orc_rollout_quant(const uint16_t* x, int64_t rows, int64_t cols,
                       const int64_t* seg, int32_t n_seg, uint8_t* codes,
                       uint8_t* bs, float* gs, uint32_t* guide) {
+  return orc_rollout_quant_given(x, rows, cols, seg, n_seg, NULL, codes, bs, gs, guide);
+}
+
+int orc_rollout_quant_given(const uint16_t* x, int64_t rows, int64_t cols,
+                            const int64_t* seg, int32_t n_seg, const float* amax_in,
+                            uint8_t* codes, uint8_t* bs, float* gs, uint32_t* guide) {
   if (check_shape(rows, cols) || check_segments(seg, n_seg, rows)) return -1;
   int32_t ns = seg_count(seg, n_seg);
   int64_t nb = cols / 16;
@@ -314,7 +320,10 @@ int orc_rollout_quant(const uint16_t* x, int64_t rows, int64_t cols,
     int64_t r0 = seg_begin(seg, s), r1 = seg_end(seg, s, rows);
     float amax;
     int64_t one[2] = {0, r1 - r0};
-    orc_segment_amax(x + r0 * cols, r1 - r0, cols, one, 1, &amax);
+    if (amax_in)
+      amax = amax_in[s];
+    else
+      orc_segment_amax(x + r0 * cols, r1 - r0, cols, one, 1, &amax);
     float g = orc_global_scale(amax);
     gs[s] = g;
     for (int64_t r = r0; r < r1; ++r) {
@@ -427,6 +436,16 @@ int orc_train_fakequant(const uint16_t* x, int64_t rows, int64_t cols,
                         const float* gs_r, const int64_t* seg_r,
                         int32_t n_seg_r, uint16_t* y, uint32_t* mask,
                         uint8_t* codes_t, uint64_t* stats) {
+  return orc_train_fakequant_given(x, rows, cols, seg_t, n_seg_t, NULL, kind, guide, bs_r,
+                                   gs_r, seg_r, n_seg_r, y, mask, codes_t, stats);
+}
+
+int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,
+                              const int64_t* seg_t, int32_t n_seg_t,
+                              const float* amax_t_in, int kind, const void* guide,
+                              const uint8_t* bs_r, const float* gs_r,
+                              const int64_t* seg_r, int32_t n_seg_r, uint16_t* y,
+                              uint32_t* mask, uint8_t* codes_t, uint64_t* stats) {
   if (check_shape(rows, cols) || check_segments(seg_t, n_seg_t, rows)) return -1;
   if (kind != ORC_GUIDE_NONE) {
     if (!guide || !bs_r || !gs_r) return -1;
@@ -438,7 +457,10 @@ int orc_train_fakequant(const uint16_t* x, int64_t rows, int64_t cols,
     int64_t r0 = seg_begin(seg_t, s), r1 = seg_end(seg_t, s, rows);
     float amax;
     int64_t one[2] = {0, r1 - r0};
-    orc_segment_amax(x + r0 * cols, r1 - r0, cols, one, 1, &amax);
+    if (amax_t_in)
+      amax = amax_t_in[s];
+    else
+      orc_segment_amax(x + r0 * cols, r1 - r0, cols, one, 1, &amax);
     float g_t = orc_global_scale(amax);
     for (int64_t r = r0; r < r1; ++r) {
       float g_r = 0.0f;

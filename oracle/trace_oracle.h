@@ -89,6 +89,13 @@ int orc_rollout_quant(const uint16_t* x, int64_t rows, int64_t cols,
                       const int64_t* seg, int32_t n_seg, uint8_t* codes,
                       uint8_t* bs, float* gs, uint32_t* guide);
 
+/* Same as orc_rollout_quant, but the per-segment maxima come from amax_in
+ * [n_seg] instead of the rows themselves.  This lets a test check a sample
+ * of rows of a large segment whose maximum was taken separately. */
+int orc_rollout_quant_given(const uint16_t* x, int64_t rows, int64_t cols,
+                            const int64_t* seg, int32_t n_seg, const float* amax_in,
+                            uint8_t* codes, uint8_t* bs, float* gs, uint32_t* guide);
+
 int orc_guide_pack(const uint8_t* codes, int64_t rows, int64_t cols,
                    uint32_t* guide);
 
@@ -103,6 +110,15 @@ int orc_train_fakequant(const uint16_t* x, int64_t rows, int64_t cols,
                         const float* gs_r, const int64_t* seg_r,
                         int32_t n_seg_r, uint16_t* y, uint32_t* mask,
                         uint8_t* codes_t, uint64_t* stats);
+
+/* Same as orc_train_fakequant with the training maxima taken from
+ * amax_t_in [n_seg_t] (see orc_rollout_quant_given). */
+int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,
+                              const int64_t* seg_t, int32_t n_seg_t,
+                              const float* amax_t_in, int kind, const void* guide,
+                              const uint8_t* bs_r, const float* gs_r,
+                              const int64_t* seg_r, int32_t n_seg_r, uint16_t* y,
+                              uint32_t* mask, uint8_t* codes_t, uint64_t* stats);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,293 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+element by element and bit for bit, on the same seeded inputs.
+
+Inputs come from the seeded generators or from hand-built edge cases; every
+expected value comes from the oracle run on the host copy of those inputs.
+Small workloads are checked on every element; the full-size workloads are
+checked on sampled row windows (the oracle is given the segment maxima taken
+from the whole segment on the host) plus whole-tensor invariants.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_rollout_guided_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from fp4_rollout_guided_gb300 import build, trace
+    build.build()
+    oracle.build()
+    hd = trace.Handle(0)
+    yield hd
+    hd.close()
+
+
+def u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def u16(t):
+    return synth.to_u16(t)
+
+
+def bf16_from_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def assert_same(name, got, want):
+    got = np.asarray(got)
+    want = np.asarray(want)
+    assert got.shape == want.shape, (name, got.shape, want.shape)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{name}: {len(bad)} mismatches, first at {i}: "
+                             f"gpu={got[i]!r} oracle={want[i]!r}")
+
+
+def run_everything(h, x_cpu, r_cpu, seg_t, seg_r, stats=True):
+    """All entry points on the GPU; returns numpy outputs."""
+    from fp4_rollout_guided_gb300 import trace
+    xg, rg = x_cpu.to(DEV), r_cpu.to(DEV)
+    codes, bs, gs, guide = h.rollout_quant(rg, seg_r)
+    packed = h.guide_pack(codes)
+    unpack_r = h.guide_unpack(rg, guide, bs, gs, seg_r)
+    unpack_x = h.guide_unpack(xg, guide, bs, gs, seg_r)
+    out = {}
+    for kind, g in (("none", None), ("full", codes), ("compact", guide)):
+        st = trace.new_stats(DEV) if stats else None
+        if kind == "none":
+            y, m, c, _ = h.train_fakequant(xg, seg_t, "none", codes=True, stats=st)
+        else:
+            y, m, c, _ = h.train_fakequant(xg, seg_t, kind, g, bs, gs, seg_r, codes=True, stats=st)
+        out[kind] = (u16(y), u32(m), c.cpu().numpy(),
+                     None if st is None else st.cpu().numpy().astype(np.uint64))
+    torch.cuda.synchronize()
+    return dict(codes=codes.cpu().numpy(), bs=bs.cpu().numpy(), gs=gs.cpu().numpy(),
+                guide=u32(guide), packed=u32(packed), unpack_r=unpack_r.cpu().numpy(),
+                unpack_x=unpack_x.cpu().numpy(), fq=out)
+
+
+def oracle_everything(xu, ru, seg_t, seg_r):
+    codes, bs, gs, guide = oracle.rollout_quant(ru, seg_r)
+    fq = {"none": oracle.train_fakequant(xu, seg_t),
+          "full": oracle.train_fakequant(xu, seg_t, oracle.GUIDE_FULL, codes, bs, gs, seg_r),
+          "compact": oracle.train_fakequant(xu, seg_t, oracle.GUIDE_COMPACT, guide, bs, gs, seg_r)}
+    return dict(codes=codes, bs=bs, gs=gs, guide=guide,
+                unpack_x=oracle.guide_unpack(xu, guide, bs, gs, seg_r), fq=fq)
+
+
+def check_all(h, x_cpu, r_cpu, seg_t, seg_r, label):
+    g = run_everything(h, x_cpu, r_cpu, seg_t, seg_r)
+    o = oracle_everything(u16(x_cpu), u16(r_cpu), seg_t, seg_r)
+    assert_same(f"{label} codes", g["codes"], o["codes"])
+    assert_same(f"{label} bs", g["bs"], o["bs"])
+    assert_same(f"{label} gs", g["gs"].view(np.uint32), o["gs"].view(np.uint32))
+    assert_same(f"{label} guide", g["guide"], o["guide"])
+    assert_same(f"{label} pack", g["packed"], o["guide"])
+    assert_same(f"{label} unpack(r)", g["unpack_r"], o["codes"])
+    assert_same(f"{label} unpack(x)", g["unpack_x"], o["unpack_x"])
+    for kind in ("none", "full", "compact"):
+        gy, gm, gc, gst = g["fq"][kind]
+        oy, om, oc, ost = o["fq"][kind]
+        assert_same(f"{label} {kind} y", gy, oy)
+        assert_same(f"{label} {kind} mask", gm, om)
+        assert_same(f"{label} {kind} codes_t", gc, oc)
+        if kind == "none":
+            assert gst[0] == ost[0]
+        else:
+            assert_same(f"{label} {kind} stats", gst, ost)
+    return g, o
+
+
+# ---------------------------------------------------------------------------
+# the five workloads, shrunk so the oracle checks every element
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_small_workloads_bit_exact(h, cfg):
+    w = synth.workload(cfg, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    check_all(h, x, r, w.seg_t, w.seg_r, f"cfg{cfg}")
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def rand_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def drift(x, seed, sigma):
+    g = torch.Generator().manual_seed(seed + 1)
+    return (x.float() * (1 + sigma * torch.randn(x.shape, generator=g))).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (3, 96), (7, 160), (1000, 64), (517, 224),
+                                        (2049, 32), (5, 4096)])
+def test_ragged_shapes(h, rows, cols):
+    x = rand_bf16((rows, cols), rows * 7 + cols)
+    r = drift(x, rows, 2.0 ** -6)
+    check_all(h, x, r, None, None, f"{rows}x{cols}")
+
+
+def test_many_uneven_segments(h):
+    rng = np.random.default_rng(5)
+    counts = rng.integers(0, 9, 700)
+    counts[::37] = 0                      # empty segments
+    counts[5] = 300                       # one long segment spanning several steps
+    rows = int(counts.sum())
+    seg_t = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    # the rollout table cuts differently: finer, misaligned with training
+    cuts = np.unique(np.concatenate([seg_t, rng.integers(0, rows, 500)]))
+    seg_r = np.concatenate([cuts[cuts < rows], [rows]]).astype(np.int64)
+    seg_r = np.unique(seg_r)
+    x = rand_bf16((rows, 64), 11, scale=3.0)
+    # per-row scale so segments differ widely
+    x = (x.float() * torch.from_numpy(np.exp(rng.normal(0, 2, (rows, 1))).astype(np.float32))).to(torch.bfloat16)
+    r = drift(x, 12, 2.0 ** -5)
+    check_all(h, x, r, seg_t, seg_r, "segments")
+
+
+def test_max_segments(h):
+    from fp4_rollout_guided_gb300 import trace
+    n = trace.MAX_SEGMENTS
+    rows = n * 2 + 17
+    counts = np.full(n, 2)
+    counts[-1] += 17
+    seg = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    x = rand_bf16((rows, 32), 21)
+    r = drift(x, 22, 2.0 ** -7)
+    check_all(h, x, r, seg, seg, "4000 segments")
+
+
+def test_special_values(h):
+    """Zeros, negative zeros, a block flushed by an overflowing reciprocal,
+    values on E2M1 points and rounding ties (S = 1 exactly), values at the
+    top of the bf16 range, and a zero segment."""
+    rows, cols = 8, 64
+    a = np.zeros((rows, cols), np.float32)
+    a[0, 0] = 2688.0                                   # gs = 1 for segment 0
+    a[0, 16:32] = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0,
+                   -0.25, -5.0]                        # S = 1: exact ties and grid points
+    a[0, 32:48] = -0.0
+    a[0, 48] = 147.0                                   # clipped element
+    a[1, :16] = 2.0 ** -118                            # tiny segment values
+    a[1, 16] = 2.0 ** -118 / 1000.0                    # flushed block (1/S overflows)
+    a[1, 17] = -(2.0 ** -118) / 3000.0
+    a[2, :] = 3.0e38                                   # near the top of bf16
+    a[2, 1::2] = -1.0e38
+    a[3, :] = 1.0                                      # constant rows
+    # rows 4..7: segment of zeros
+    x = torch.from_numpy(a).to(torch.bfloat16)
+    r = drift(x, 31, 2.0 ** -4)
+    seg = np.array([0, 1, 2, 3, 4, 8], np.int64)
+    check_all(h, x, r, seg, seg, "specials")
+    # opposite-sign rollout record
+    check_all(h, x, (-r.float()).to(torch.bfloat16), seg, seg, "specials negated")
+
+
+def test_unrelated_rollout(h):
+    """Independent rollout values: opposite signs and multi-entry mismatches
+    exercise every branch of the guided choice and every histogram bucket."""
+    x = rand_bf16((300, 256), 41)
+    r = rand_bf16((300, 256), 42, scale=1.7)
+    seg_t = np.array([0, 100, 300], np.int64)
+    seg_r = np.array([0, 50, 51, 299, 300], np.int64)
+    g, o = check_all(h, x, r, seg_t, seg_r, "unrelated")
+    assert np.all(o["fq"]["full"][3][3:7] > 0)
+
+
+def test_empty_input(h):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    codes, bs, gs, guide = h.rollout_quant(x, np.array([0, 0, 0], np.int64))
+    torch.cuda.synchronize()
+    assert gs.shape == (2,) and torch.all(gs == 0)
+    y, m, c, _ = h.train_fakequant(x, None, "compact", guide, bs, gs.new_zeros(1), None)
+    assert y.numel() == 0
+
+
+def test_repeated_calls_and_streams(h):
+    """Scratch is reused call after call and across streams: results stay
+    identical (the amax scratch re-zeroes itself)."""
+    w = synth.workload(2, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    first = run_everything(h, x, r, w.seg_t, w.seg_r, stats=False)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        second = run_everything(h, x, r, w.seg_t, w.seg_r, stats=False)
+    s.synchronize()
+    for k in ("codes", "bs", "gs", "guide", "unpack_x"):
+        assert np.array_equal(first[k], second[k]), k
+    for kind in ("none", "full", "compact"):
+        for a, b in zip(first["fq"][kind][:3], second["fq"][kind][:3]):
+            assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+
+def sampled_check(h, cfg, windows_per_seg=2, window_rows=1536, seg_picks=3):
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(cfg)
+    x, r = synth.make_inputs(w, DEV)
+    codes, bs, gs, guide = h.rollout_quant(r, w.seg_r)
+    packed = h.guide_pack(codes)
+    unpacked = h.guide_unpack(r, guide, bs, gs, w.seg_r)
+    st = trace.new_stats(DEV)
+    y, m, _, _ = h.train_fakequant(x, w.seg_t, "compact", guide, bs, gs, w.seg_r, stats=st)
+    torch.cuda.synchronize()
+    # whole-tensor invariants that hold at any size
+    assert torch.equal(packed, guide), "pack(codes) != rollout guide"
+    assert torch.equal(unpacked, codes), "unpack(pack(codes), r) != codes"
+    stats = st.cpu().numpy().astype(np.uint64)
+    assert stats[0] == w.elems
+    assert stats[2] <= stats[1]
+
+    segs = np.unique(np.linspace(0, w.n_seg_t - 1, seg_picks).astype(int))
+    for s in segs:
+        t0, t1 = int(w.seg_t[s]), int(w.seg_t[s + 1])
+        xs = u16(x[t0:t1])
+        amax_t = np.abs(oracle.bf16_to_f32(xs)).max()
+        # sample windows each inside one rollout segment
+        inner, first = synth.rollout_segments_within(w, s)
+        picks = np.unique(np.linspace(0, len(inner) - 2, windows_per_seg).astype(int))
+        for k in picks:
+            ra, rb = t0 + int(inner[k]), t0 + int(inner[k + 1])
+            rs = u16(r[ra:rb])
+            amax_r = np.abs(oracle.bf16_to_f32(rs)).max()
+            a = ra + max(0, (rb - ra - window_rows) // 2)
+            b = min(rb, a + window_rows)
+            ru = u16(r[a:b])
+            xu = u16(x[a:b])
+            o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(ru, None, amax=[amax_r])
+            lbl = f"cfg{cfg} seg{s} rows {a}:{b}"
+            assert_same(lbl + " gs", gs[first + k:first + k + 1].cpu().numpy().view(np.uint32),
+                        o_gs.view(np.uint32))
+            assert_same(lbl + " codes", codes[a:b].cpu().numpy(), o_codes)
+            assert_same(lbl + " bs", bs[a:b].cpu().numpy(), o_bs)
+            assert_same(lbl + " guide", u32(guide[a:b]), o_guide)
+            o_y, o_m, _, _ = oracle.train_fakequant(xu, None, oracle.GUIDE_COMPACT, o_guide, o_bs,
+                                                    o_gs, None, amax_t=[amax_t],
+                                                    want_codes=False, want_stats=False)
+            assert_same(lbl + " y", u16(y[a:b]), o_y)
+            assert_same(lbl + " mask", u32(m[a:b]), o_m)
+    del x, r, codes, bs, gs, guide, packed, unpacked, y, m
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_sampled(h, cfg):
+    sampled_check(h, cfg)
