@@ -73,8 +73,10 @@ trace_status_t check_shape(int64_t rows, int64_t cols) {
   return TRACE_OK;
 }
 
-trace_status_t check_tensor(const void* p) {
-  if (!p) return TRACE_ERR_INVALID_ARG;
+// A tensor pointer must be non-null and 16-byte aligned, except that an
+// empty input (rows == 0) may pass null pointers for its empty tensors.
+trace_status_t check_tensor(const void* p, bool empty = false) {
+  if (!p) return empty ? TRACE_OK : TRACE_ERR_INVALID_ARG;
   if (!aligned(p, 16)) return TRACE_ERR_ALIGNMENT;
   return TRACE_OK;
 }
@@ -217,8 +219,9 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
+  const bool empty = rows == 0;
   for (const void* p : {x_bf16, (const void*)codes_u8, (const void*)bs_e4m3})
-    if ((s = check_tensor(p)) != TRACE_OK) return s;
+    if ((s = check_tensor(p, empty)) != TRACE_OK) return s;
   if (guide_bits && (s = check_tensor(guide_bits)) != TRACE_OK) return s;
   if (!gs_f32) return TRACE_ERR_INVALID_ARG;
   if (!aligned(gs_f32, 4)) return TRACE_ERR_ALIGNMENT;
@@ -254,8 +257,9 @@ trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t 
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
-  if ((s = check_tensor(codes_u8)) != TRACE_OK) return s;
-  if ((s = check_tensor(guide_bits)) != TRACE_OK) return s;
+  const bool empty = rows == 0;
+  if ((s = check_tensor(codes_u8, empty)) != TRACE_OK) return s;
+  if ((s = check_tensor(guide_bits, empty)) != TRACE_OK) return s;
   const int64_t nchunks = rows * (cols / 32);
   if (nchunks == 0) return TRACE_OK;
   DeviceGuard g(h->device);
@@ -274,8 +278,9 @@ trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
+  const bool empty = rows == 0;
   for (const void* p : {x_ref_bf16, (const void*)guide_bits, bs_r, (const void*)codes_u8})
-    if ((s = check_tensor(p)) != TRACE_OK) return s;
+    if ((s = check_tensor(p, empty)) != TRACE_OK) return s;
   if (!gs_r) return TRACE_ERR_INVALID_ARG;
   if (!aligned(gs_r, 4)) return TRACE_ERR_ALIGNMENT;
   static thread_local tfp4::SegParam sp;
@@ -304,16 +309,17 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
   if (s != TRACE_OK) return s;
   if (kind != TRACE_GUIDE_NONE && kind != TRACE_GUIDE_FULL && kind != TRACE_GUIDE_COMPACT)
     return TRACE_ERR_INVALID_ARG;
-  if ((s = check_tensor(x_bf16)) != TRACE_OK) return s;
-  if ((s = check_tensor(y_bf16)) != TRACE_OK) return s;
+  const bool empty = rows == 0;
+  if ((s = check_tensor(x_bf16, empty)) != TRACE_OK) return s;
+  if ((s = check_tensor(y_bf16, empty)) != TRACE_OK) return s;
   if (ste_mask && (s = check_tensor(ste_mask)) != TRACE_OK) return s;
   if (codes_t_u8 && (s = check_tensor(codes_t_u8)) != TRACE_OK) return s;
   if (stats_dev && !aligned(stats_dev, 8)) return TRACE_ERR_ALIGNMENT;
   static thread_local tfp4::SegParam spt, spr;
   if ((s = make_segments(seg_t, rows, &spt)) != TRACE_OK) return s;
   if (kind != TRACE_GUIDE_NONE) {
-    if ((s = check_tensor(guide)) != TRACE_OK) return s;
-    if ((s = check_tensor(bs_r)) != TRACE_OK) return s;
+    if ((s = check_tensor(guide, empty)) != TRACE_OK) return s;
+    if ((s = check_tensor(bs_r, empty)) != TRACE_OK) return s;
     if (!gs_r) return TRACE_ERR_INVALID_ARG;
     if (!aligned(gs_r, 4)) return TRACE_ERR_ALIGNMENT;
     if ((s = make_segments(seg_r, rows, &spr)) != TRACE_OK) return s;

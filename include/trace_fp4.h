@@ -22,7 +22,9 @@
  *
  * Common conventions
  *   - Tensors are row-major [rows, cols] with cols % 32 == 0 and cols > 0;
- *     rows == 0 is an empty, valid input.  rows * cols / 32 must stay below
+ *     rows == 0 is an empty, valid input whose tensor pointers may be NULL
+ *     (trace_rollout_quant still writes gs = 0 for every segment).
+ *     rows * cols / 32 must stay below
  *     2^31 and rows below 2^31.  A "block" is 16 consecutive elements of a row.
  *   - bf16 values are passed as raw 16-bit patterns.
  *   - Packed E2M1 codes: uint8 [rows, cols/2]; element 2i is the low nibble
