@@ -1,6 +1,6 @@
 """Builds libtrace_fp4.so in-tree with nvcc for sm_103a.
 
-Two translation units compile in parallel, then link into one shared library
+The translation units compile in parallel, then link into one shared library
 under ``fp4_rollout_guided_gb300/_build``.  Flags: -O3, no fused multiply-add
 contraction (-fmad=false), IEEE division/square root and no flush-to-zero
 (nvcc's defaults, stated explicitly), line info for the profiler.
@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtrace_fp4.so")
-SOURCES = ["trace_kernels.cu", "trace_api.cu"]
+SOURCES = ["trace_kernels.cu", "trace_api.cu", "trace_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC",

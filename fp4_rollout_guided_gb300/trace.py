@@ -64,6 +64,7 @@ SIGNATURES = {
     "trace_guide_unpack": (INT, [P, P, P, P, P, Segments, I64, I64, P, P]),
     "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
                                     P, P, P]),
+    "trace_rollout_quant_noalloc": (INT, [P, I64, I64, Segments, P, P, P, P, P]),
     "trace_profile_enable": (INT, [P, INT]),
     "trace_profile_collect": (INT, [P, ctypes.POINTER(KernelTime)]),
 }

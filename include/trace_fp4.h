@@ -209,6 +209,32 @@ TRACE_API trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_b
                                      void* codes_t_u8, trace_stats_t* stats_dev,
                                      trace_stream_t stream);
 
+/* Rollout-side quantisation without a handle and without any device
+ * allocation.  The paper has no counterpart: this is a deployment variant of
+ * trace_rollout_quant with the same arguments, layouts and results.
+ *
+ * It is for callers that must not call cudaMalloc (code running inside a
+ * device allocator or memory pool, runtimes that pre-reserve all device
+ * memory for their own arena, allocation-free real-time loops); such callers
+ * cannot create a handle either, since trace_create allocates scratch.  The
+ * scratch this call needs (per-segment maxima and a completion ticket) is a
+ * fixed array in the library's device image, held by every GPU that loads
+ * the library until the process exits, sized for at most
+ * TRACE_NOALLOC_MAX_SEGMENTS segments; more segments return
+ * TRACE_ERR_INVALID_ARG before anything is enqueued.
+ *
+ * It works on the current device.  Its first call on a device resolves the
+ * array's device address (cudaGetSymbolAddress) and caches it, so make that
+ * first call before any stream capture.  Every call clears the part of the
+ * array it uses on `stream`; all calls on one device share the array, so
+ * calls that overlap on the GPU (e.g. on two streams at once) race. */
+#define TRACE_NOALLOC_MAX_SEGMENTS 1024
+TRACE_API trace_status_t trace_rollout_quant_noalloc(const void* x_bf16, int64_t rows,
+                                                     int64_t cols, trace_segments_t seg,
+                                                     void* codes_u8, void* bs_e4m3,
+                                                     float* gs_f32, uint32_t* guide_bits,
+                                                     trace_stream_t stream);
+
 /* Built-in profiler.  While enabled, every kernel launch through the handle
  * is bracketed by CUDA events on its own stream.  trace_profile_collect
  * waits for the recorded events, writes per-kernel launch counts and summed
