@@ -180,20 +180,41 @@ __device__ __forceinline__ void real_scale(uint32_t code, float gs, float& S, fl
   inv = r;
 }
 
+// Two binary32 values -> two E4M3 codes (RNE, satfinite): byte 0 = lo.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  unsigned short c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
 // Both blocks' E4M3 scales from their maxima and the segment scale.
+//
+// The method divides: q = bamax / (gs * 6), rounded once.  An IEEE division
+// costs about twenty integer-pipe instructions, so the quotient is first
+// formed as q' = bamax * fl(1 / (gs * 6)), which lies within 2.5 ulp of q.
+// E4M3 encoding is monotone, so when q' * (1 - 2^-21) and q' * (1 + 2^-21)
+// (a bracket around q) encode to the same code, that code is the code of q.
+// Otherwise -- q within a few ulps of an E4M3 rounding boundary, or a
+// reciprocal that overflows -- the correctly rounded division decides.
 __device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, float gs) {
-  float q0 = 0.0f, q1 = 0.0f;
+  uint32_t codes = 0;
   if (gs > 0.0f) {
     const float den = __fmul_rn(gs, 6.0f);
-    q0 = __fdiv_rn(bamax0, den);
-    q1 = __fdiv_rn(bamax1, den);
+    const float rden = __frcp_rn(den);
+    bool exact = !(rden < __int_as_float(0x7F800000));
+    if (!exact) {
+      const float q0 = __fmul_rn(bamax0, rden), q1 = __fmul_rn(bamax1, rden);
+      const uint32_t lo = e4m3x2(__fmul_rn(q0, 1.0f - 0x1p-21f), __fmul_rn(q1, 1.0f - 0x1p-21f));
+      const uint32_t hi = e4m3x2(__fmul_rn(q0, 1.0f + 0x1p-21f), __fmul_rn(q1, 1.0f + 0x1p-21f));
+      codes = lo;
+      exact = lo != hi;
+    }
+    if (exact) codes = e4m3x2(__fdiv_rn(bamax0, den), __fdiv_rn(bamax1, den));
   }
-  unsigned short c;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(q1), "f"(q0));
   PairScale p;
-  p.codes = c;
-  real_scale(c & 0xFFu, gs, p.S[0], p.inv[0]);
-  real_scale((uint32_t)c >> 8, gs, p.S[1], p.inv[1]);
+  p.codes = codes;
+  real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
+  real_scale(codes >> 8, gs, p.S[1], p.inv[1]);
   return p;
 }
 
@@ -204,6 +225,47 @@ __device__ __forceinline__ PairScale pair_scale_stored(uint32_t codes, float gs)
   real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
   real_scale((codes >> 8) & 0xFFu, gs, p.S[1], p.inv[1]);
   return p;
+}
+
+// ---------------------------------------------------------------------------
+// packed binary32 pairs (f32x2 instructions: one issue slot for two lanes)
+// ---------------------------------------------------------------------------
+
+struct F2 {
+  float x, y;
+};
+
+#define TFP4_F2_OP(name, inst)                                                      \
+  __device__ __forceinline__ F2 name(F2 a, F2 b) {                                   \
+    F2 d;                                                                           \
+    asm("{ .reg .b64 A, B, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; " inst       \
+        " D, A, B; mov.b64 {%0, %1}, D; }"                                          \
+        : "=f"(d.x), "=f"(d.y)                                                      \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                  \
+    return d;                                                                       \
+  }
+TFP4_F2_OP(add2_rn, "add.rn.f32x2")
+TFP4_F2_OP(add2_rz, "add.rz.f32x2")
+TFP4_F2_OP(add2_rp, "add.rp.f32x2")
+TFP4_F2_OP(sub2_rn, "sub.rn.f32x2")
+TFP4_F2_OP(mul2_rn, "mul.rn.f32x2")
+#undef TFP4_F2_OP
+
+__device__ __forceinline__ F2 fma2_rn(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("{ .reg .b64 A, B, C, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; "
+      "mov.b64 C, {%6, %7}; fma.rn.f32x2 D, A, B, C; mov.b64 {%0, %1}, D; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
+
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------------------
@@ -228,16 +290,26 @@ __device__ __forceinline__ float magic_of(float tc) {
   return __uint_as_float(e + 0x0B400000u);
 }
 
-// Rollout-frame decode of one element from the compact record: the bracket
-// member of t_r whose index parity equals bit 0 of `lsb_word` (a point
-// bracket ignores the bit).  Returns the E2M1 magnitude.
-__device__ __forceinline__ float decode_compact(float tr, uint32_t lsb_word) {
-  const float tc = fminf(tr, 6.0f);
-  const float C = magic_of(tc);
-  const uint32_t uz = __float_as_uint(__fadd_rz(tc, C));
-  const uint32_t up = __float_as_uint(__fadd_ru(tc, C));
-  const uint32_t us = uz + ((uz ^ lsb_word) & (up - uz));
-  return __fsub_rn(__uint_as_float(us), C);
+// The same constant for a pair of clamped values.  Two exact formulations:
+// TFP4_MAGIC_FMA = 1 builds it on the FMA pipe from two saturating
+// indicators, b1 = [tc > 2] and b2 = [tc > 4] (sat(tc * 2^30 - 2^31) is 0 for
+// tc <= 2 and 1 otherwise: the next binary32 above 2 is 2 + 2^-22), then
+// C = K * (1 + b1) * (1 + b2), K = 1.5 * 2^22; otherwise it takes the
+// exponent field with integer operations.  At tc = 2 or 4 both constants put
+// the (on-grid) value on the grid, so the boundary side does not matter.
+#ifndef TFP4_MAGIC_FMA
+#define TFP4_MAGIC_FMA 1
+#endif
+__device__ __forceinline__ F2 magic_pair(F2 tc) {
+#if TFP4_MAGIC_FMA
+  const float k = 0x1.8p22f;
+  const F2 b1 = {fma_sat(tc.x, 0x1p30f, -0x1p31f), fma_sat(tc.y, 0x1p30f, -0x1p31f)};
+  const F2 b2 = {fma_sat(tc.x, 0x1p30f, -0x1p32f), fma_sat(tc.y, 0x1p30f, -0x1p32f)};
+  const F2 m1 = fma2_rn(b1, splat(k), splat(k));
+  return fma2_rn(b2, m1, m1);
+#else
+  return F2{magic_of(tc.x), magic_of(tc.y)};
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -449,16 +521,29 @@ __global__ void __launch_bounds__(kThreads)
 // a4: guide unpack
 // ---------------------------------------------------------------------------
 
+// Rollout-frame decode of a pair from the compact record: for each element
+// the bracket member of t_r whose index parity equals its stored bit (a
+// point bracket ignores the bit).  `lsb0` / `lsb1` carry the bits in bit 0.
+// Returns the two E2M1 magnitudes.
+__device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t lsb0, uint32_t lsb1) {
+  const F2 tc = {fminf(tr.x, 6.0f), fminf(tr.y, 6.0f)};
+  const F2 C = magic_pair(tc);
+  const F2 uz = add2_rz(tc, C), up = add2_rp(tc, C);
+  const uint32_t z0 = __float_as_uint(uz.x), z1 = __float_as_uint(uz.y);
+  const F2 us = {((z0 ^ lsb0) & 1u) ? up.x : uz.x, ((z1 ^ lsb1) & 1u) ? up.y : uz.y};
+  return sub2_rn(us, C);
+}
+
 // Two elements of one bf16x2 word -> one byte of rollout codes.  j0 is the
 // index of the word's low element inside its 16-element block.
 __device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t gw, int j0) {
-  const float a0 = __uint_as_float((w << 16) & 0x7FFF0000u);
-  const float a1 = __uint_as_float(w & 0x7FFF0000u);
-  float g0 = decode_compact(__fmul_rn(a0, inv), gw >> (16 + j0));
-  float g1 = decode_compact(__fmul_rn(a1, inv), gw >> (17 + j0));
-  g0 = __uint_as_float(__float_as_uint(g0) | ((gw << (31 - j0)) & 0x80000000u));
-  g1 = __uint_as_float(__float_as_uint(g1) | ((gw << (30 - j0)) & 0x80000000u));
-  return e2m1x2(g0, g1);  // exact grid points: the conversion yields the index
+  const uint32_t a = w & kAbs2;
+  const F2 ax = {__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)};
+  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw >> (16 + j0), gw >> (17 + j0));
+  // signs from the record; E2M1 conversion of exact grid points gives indices
+  const float g0 = __uint_as_float(__float_as_uint(g.x) | ((gw << (31 - j0)) & 0x80000000u));
+  const float g1 = __uint_as_float(__float_as_uint(g.y) | ((gw << (30 - j0)) & 0x80000000u));
+  return e2m1x2(g0, g1);
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -566,41 +651,77 @@ __device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) 
   k.h_g[3] += d1 >= 3;
 }
 
-// One training element.  ax = |x|, sx = x's sign bit (0 or 0x80000000);
-// vr_rel is the rollout's reconstructed value with its sign taken relative
-// to x (negated when the signs differ), so the candidate distances are formed
-// on magnitudes: |(+-v_c) - v_r| = |v_c - vr_rel| exactly (round-to-nearest
-// is symmetric).  Returns the signed output; g_out / g_rtn receive the chosen
-// and the RTN magnitudes.
-template <bool GUIDED>
-__device__ __forceinline__ float train_element(float ax, uint32_t sx, float inv_t, float S_t,
-                                               float vr_rel, float& g_out, float& g_rtn) {
-  const float t = __fmul_rn(ax, inv_t);
-  const float tc = fminf(t, 6.0f);
-  const float C = magic_of(tc);
-  const float s_rn = __fadd_rn(tc, C);
-  float y;
+__device__ __forceinline__ float fmul_sat(float a, float b) {
+  float d;
+  asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Training side of one pair of elements.  ax holds |x|; vr holds the rollout's
+// reconstructed values with their signs taken relative to x (negated where
+// the signs differ), so candidate distances can be formed on magnitudes:
+// |(+-v_c) - v_r| = |v_c - vr| exactly, round-to-nearest being symmetric.
+// ym receives the chosen magnitudes (G[m] * S_t); with WANT_G, gsel / grtn
+// receive the chosen and the RTN E2M1 magnitudes.
+//
+// The choice: hi wins when |d_hi| < |d_lo|, or on equality when RTN is hi.
+// diff = |d_lo| - |d_hi| is exact in sign (and +0 only on equality), and
+// RTN-is-hi is bits(s_rn) - bits(s_rz), 0 or 1, so hi <=> bits(diff) +
+// rtn_hi - 1 >= 0 as a signed integer.  TFP4_CHOICE_FMA = 1 forms the same
+// decision on the FMA pipe: with a = s_rn - s_rz (0 or one ulp) and
+// D = diff * 2^127 (at least 2^-22 in magnitude when diff != 0),
+// h = sat((D * 2^127 + a) * 2^127) is exactly 1 for hi and 0 for lo, and the
+// output is v_lo + h * (v_hi - v_lo) (the difference is exact: the two
+// candidates are within a factor of two, or v_lo is 0).
+#ifndef TFP4_CHOICE_FMA
+#define TFP4_CHOICE_FMA 0
+#endif
+template <bool GUIDED, bool WANT_G>
+__device__ __forceinline__ void train_pair(F2 ax, float inv_t, float S_t, F2 vr, F2& ym, F2& gsel,
+                                           F2& grtn) {
+  const F2 t = mul2_rn(ax, splat(inv_t));
+  const F2 tc = {fminf(t.x, 6.0f), fminf(t.y, 6.0f)};
+  const F2 C = magic_pair(tc);
+  const F2 sn = add2_rn(tc, C);
   if (!GUIDED) {
-    const float g = __fsub_rn(s_rn, C);
-    g_out = g;
-    g_rtn = g;
-    y = __fmul_rn(g, S_t);
-  } else {
-    const float s_rz = __fadd_rz(tc, C);
-    const float s_rp = __fadd_ru(tc, C);
-    const float g_lo = __fsub_rn(s_rz, C);
-    const float g_hi = __fsub_rn(s_rp, C);
-    const float v_lo = __fmul_rn(g_lo, S_t);
-    const float v_hi = __fmul_rn(g_hi, S_t);
-    const float d_lo = fabsf(__fsub_rn(v_lo, vr_rel));
-    const float d_hi = fabsf(__fsub_rn(v_hi, vr_rel));
-    const bool rtn_hi = s_rn != s_rz;
-    const bool hi = (d_hi < d_lo) || (!(d_lo < d_hi) && rtn_hi);
-    y = hi ? v_hi : v_lo;
-    g_out = hi ? g_hi : g_lo;
-    g_rtn = rtn_hi ? g_hi : g_lo;
+    const F2 g = sub2_rn(sn, C);
+    ym = mul2_rn(g, splat(S_t));
+    gsel = g;
+    grtn = g;
+    return;
   }
-  return __uint_as_float(__float_as_uint(y) | sx);
+  const F2 sz = add2_rz(tc, C), sp = add2_rp(tc, C);
+  const F2 glo = sub2_rn(sz, C), ghi = sub2_rn(sp, C);
+  const F2 vlo = mul2_rn(glo, splat(S_t)), vhi = mul2_rn(ghi, splat(S_t));
+  const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
+  const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
+  const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
+#if TFP4_CHOICE_FMA
+  const F2 a = sub2_rn(sn, sz);
+  const F2 D = mul2_rn(F2{diff0, diff1}, splat(0x1p127f));
+  const F2 D2 = fma2_rn(D, splat(0x1p127f), a);
+  const F2 h = {fmul_sat(D2.x, 0x1p127f), fmul_sat(D2.y, 0x1p127f)};
+  ym = fma2_rn(h, sub2_rn(vhi, vlo), vlo);
+  const bool hi0 = h.x != 0.0f, hi1 = h.y != 0.0f;
+#else
+  const int k0 = (int)(__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x));
+  const int k1 = (int)(__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y));
+  const bool hi0 = k0 >= 0, hi1 = k1 >= 0;
+  ym = F2{hi0 ? vhi.x : vlo.x, hi1 ? vhi.y : vlo.y};
+#endif
+  if (WANT_G) {
+    gsel = F2{hi0 ? ghi.x : glo.x, hi1 ? ghi.y : glo.y};
+    grtn = F2{sn.x != sz.x ? ghi.x : glo.x, sn.y != sz.y ? ghi.y : glo.y};
+  }
+}
+
+// Spreads the 16 low bits of v to the even bit positions.
+__device__ __forceinline__ uint32_t spread16(uint32_t v) {
+  v = (v | (v << 8)) & 0x00FF00FFu;
+  v = (v | (v << 4)) & 0x0F0F0F0Fu;
+  v = (v | (v << 2)) & 0x33333333u;
+  v = (v | (v << 1)) & 0x55555555u;
+  return v;
 }
 
 template <int KIND, bool MASK, bool CODES, bool STATS>
@@ -677,10 +798,17 @@ __global__ void __launch_bounds__(kThreads)
       const PairScale pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
       PairScale pr = {};
       if (GUIDED) pr = pair_scale_stored(bcur, gs_r[s_r]);
-      float six[2];
+      // STE threshold per block in bf16 magnitude bits: |x| > 6 * S exactly
+      // when the bf16 |x| exceeds 6 * S rounded down to bf16 (truncation), so
+      // two elements compare at once in 16-bit lanes: bit 15 of each lane of
+      // (0x8000 + thr) - |x| is set exactly when the element is kept.
+      uint32_t thr2[2];
 #pragma unroll
-      for (int b = 0; b < 2; ++b)
-        six[b] = pt.S[b] > 0.0f ? __fmul_rn(6.0f, pt.S[b]) : __int_as_float(0x7F800000);
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t thr =
+            pt.S[b] > 0.0f ? (__float_as_uint(__fmul_rn(6.0f, pt.S[b])) >> 16) : 0x7FFFu;
+        thr2[b] = (thr | 0x8000u) * 0x00010001u;
+      }
 
       uint32_t ybits[16];
       uint32_t cbytes[16];
@@ -690,49 +818,46 @@ __global__ void __launch_bounds__(kThreads)
         const int b = i >> 3;        // block of this word
         const int j0 = (i & 7) * 2;  // index of its low element in the block
         const uint32_t w = cur.w[i];
-        float gfull[2] = {0.0f, 0.0f};
-        if (KIND == TRACE_GUIDE_FULL) {
+        const F2 ax = {__uint_as_float(a[i] << 16), __uint_as_float(a[i] & 0xFFFF0000u)};
+        const uint32_t sx0 = (w << 16) & 0x80000000u, sx1 = w & 0x80000000u;
+        F2 vr = {0.0f, 0.0f};
+        F2 grs = {0.0f, 0.0f};  // signed rollout magnitudes (statistics)
+        if (KIND == TRACE_GUIDE_COMPACT) {
+          const uint32_t gw = b ? gcur.y : gcur.x;
+          const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw >> (16 + j0),
+                                    gw >> (17 + j0));
+          const uint32_t sr0 = (gw << (31 - j0)) & 0x80000000u;
+          const uint32_t sr1 = (gw << (30 - j0)) & 0x80000000u;
+          const uint32_t Sb = __float_as_uint(pr.S[b]);
+          vr = mul2_rn(gr, F2{__uint_as_float(Sb | (sx0 ^ sr0)), __uint_as_float(Sb | (sx1 ^ sr1))});
+          if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
+                              __uint_as_float(__float_as_uint(gr.y) | sr1)};
+        } else if (KIND == TRACE_GUIDE_FULL) {
           const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
-          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, gfull[0], gfull[1]);
+          float g0, g1;
+          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
+          const uint32_t Sb = __float_as_uint(pr.S[b]);
+          vr = mul2_rn(F2{g0, g1}, F2{__uint_as_float(Sb | sx0), __uint_as_float(Sb | sx1)});
+          if (STATS) grs = F2{g0, g1};
         }
-        float outv[2], gsel[2], grtn[2], gr_signed[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t xb = h ? (w & 0xFFFF0000u) : (w << 16);
-          const float ax = __uint_as_float(xb & 0x7FFFFFFFu);
-          const uint32_t sx = xb & 0x80000000u;
-          float vr_rel = 0.0f;
-          gr_signed[h] = 0.0f;
-          if (KIND == TRACE_GUIDE_COMPACT) {
-            const int j = j0 + h;
-            const uint32_t gw = b ? gcur.y : gcur.x;
-            const float g_r = decode_compact(__fmul_rn(ax, pr.inv[b]), gw >> (16 + j));
-            const float v_r = __fmul_rn(g_r, pr.S[b]);
-            const uint32_t sr_bit = (gw << (31 - j)) & 0x80000000u;
-            vr_rel = __uint_as_float(__float_as_uint(v_r) | (sx ^ sr_bit));
-            gr_signed[h] = __uint_as_float(__float_as_uint(g_r) | sr_bit);
-          } else if (KIND == TRACE_GUIDE_FULL) {
-            const float v_r = __fmul_rn(gfull[h], pr.S[b]);
-            vr_rel = __uint_as_float(__float_as_uint(v_r) ^ sx);
-            gr_signed[h] = gfull[h];
-          }
-          outv[h] = train_element<GUIDED>(ax, sx, pt.inv[b], pt.S[b], vr_rel, gsel[h], grtn[h]);
-          if (MASK) kept |= (ax > six[b] ? 0u : 1u) << (2 * i + h);
-        }
-        ybits[i] = bf16x2_rn(outv[0], outv[1]);
+        F2 ym, gsel, grtn;
+        train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], pt.S[b], vr, ym, gsel, grtn);
+        ybits[i] = bf16x2_rn(ym.x, ym.y) | (w & 0x80008000u);
+        if (MASK) kept = (kept >> 1) | ((thr2[b] - a[i]) & 0x80008000u);
         if (CODES || STATS) {
-          const uint32_t s0 = (w << 16) & 0x80000000u, s1 = w & 0x80000000u;
-          const float g0 = __uint_as_float(__float_as_uint(gsel[0]) | s0);
-          const float g1 = __uint_as_float(__float_as_uint(gsel[1]) | s1);
+          const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
+          const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
           if (CODES) cbytes[i] = e2m1x2(g0, g1);
           if (STATS && GUIDED) {
-            count(cnt, signed_index(gr_signed[0]),
-                  signed_index(__uint_as_float(__float_as_uint(grtn[0]) | s0)), signed_index(g0));
-            count(cnt, signed_index(gr_signed[1]),
-                  signed_index(__uint_as_float(__float_as_uint(grtn[1]) | s1)), signed_index(g1));
+            count(cnt, signed_index(grs.x),
+                  signed_index(__uint_as_float(__float_as_uint(grtn.x) | sx0)), signed_index(g0));
+            count(cnt, signed_index(grs.y),
+                  signed_index(__uint_as_float(__float_as_uint(grtn.y) | sx1)), signed_index(g1));
           }
         }
       }
+      // word i left its two bits at positions i and 16 + i: interleave
+      if (MASK) kept = spread16(kept & 0xFFFFu) | (spread16(kept >> 16) << 1);
       uint8_t* yp = y + (uint64_t)c * 64u;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
