@@ -262,6 +262,13 @@ __device__ __forceinline__ F2 fma2_rn(F2 a, F2 b, F2 c) {
 
 __device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
 
+// Multiply-add on the FMA pipe (IMAD): a * b + c, wrapping.
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float d;
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -523,14 +530,18 @@ __global__ void __launch_bounds__(kThreads)
 
 // Rollout-frame decode of a pair from the compact record: for each element
 // the bracket member of t_r whose index parity equals its stored bit (a
-// point bracket ignores the bit).  `lsb0` / `lsb1` carry the bits in bit 0.
-// Returns the two E2M1 magnitudes.
-__device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t lsb0, uint32_t lsb1) {
+// point bracket ignores the bit).  gw is the block's compact word and j0 the
+// first element's index: the parity of the lower member (bit 0 of the
+// rz-sum) is moved up to the stored bit's position (16 + j) by a multiply
+// and compared there.  Returns the two E2M1 magnitudes.
+__device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t gw, int j0) {
   const F2 tc = {fminf(tr.x, 6.0f), fminf(tr.y, 6.0f)};
   const F2 C = magic_pair(tc);
   const F2 uz = add2_rz(tc, C), up = add2_rp(tc, C);
-  const uint32_t z0 = __float_as_uint(uz.x), z1 = __float_as_uint(uz.y);
-  const F2 us = {((z0 ^ lsb0) & 1u) ? up.x : uz.x, ((z1 ^ lsb1) & 1u) ? up.y : uz.y};
+  const uint32_t b0 = 1u << (16 + j0), b1 = 1u << (17 + j0);
+  const uint32_t m0 = (imad(__float_as_uint(uz.x), b0, 0u) ^ gw) & b0;
+  const uint32_t m1 = (imad(__float_as_uint(uz.y), b1, 0u) ^ gw) & b1;
+  const F2 us = {m0 ? up.x : uz.x, m1 ? up.y : uz.y};
   return sub2_rn(us, C);
 }
 
@@ -539,7 +550,7 @@ __device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t lsb0, uint32_t lsb1) {
 __device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t gw, int j0) {
   const uint32_t a = w & kAbs2;
   const F2 ax = {__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)};
-  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw >> (16 + j0), gw >> (17 + j0));
+  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw, j0);
   // signs from the record; E2M1 conversion of exact grid points gives indices
   const float g0 = __uint_as_float(__float_as_uint(g.x) | ((gw << (31 - j0)) & 0x80000000u));
   const float g1 = __uint_as_float(__float_as_uint(g.y) | ((gw << (30 - j0)) & 0x80000000u));
@@ -657,27 +668,20 @@ __device__ __forceinline__ float fmul_sat(float a, float b) {
   return d;
 }
 
-// Training side of one pair of elements.  ax holds |x|; vr holds the rollout's
-// reconstructed values with their signs taken relative to x (negated where
-// the signs differ), so candidate distances can be formed on magnitudes:
-// |(+-v_c) - v_r| = |v_c - vr| exactly, round-to-nearest being symmetric.
-// ym receives the chosen magnitudes (G[m] * S_t); with WANT_G, gsel / grtn
-// receive the chosen and the RTN E2M1 magnitudes.
+// Training side of one pair of elements.  ax holds |x|; St holds the
+// training scale carrying each element's sign, vr the rollout's
+// reconstructed values with the rollout's signs, so the candidates
+// v_c = G[c] * St are the signed values the method compares and the chosen
+// one is the signed output.  ym receives the chosen signed values; with
+// WANT_G, gsel / grtn receive the chosen and the RTN E2M1 magnitudes.
 //
 // The choice: hi wins when |d_hi| < |d_lo|, or on equality when RTN is hi.
 // diff = |d_lo| - |d_hi| is exact in sign (and +0 only on equality), and
 // RTN-is-hi is bits(s_rn) - bits(s_rz), 0 or 1, so hi <=> bits(diff) +
-// rtn_hi - 1 >= 0 as a signed integer.  TFP4_CHOICE_FMA = 1 forms the same
-// decision on the FMA pipe: with a = s_rn - s_rz (0 or one ulp) and
-// D = diff * 2^127 (at least 2^-22 in magnitude when diff != 0),
-// h = sat((D * 2^127 + a) * 2^127) is exactly 1 for hi and 0 for lo, and the
-// output is v_lo + h * (v_hi - v_lo) (the difference is exact: the two
-// candidates are within a factor of two, or v_lo is 0).
-#ifndef TFP4_CHOICE_FMA
-#define TFP4_CHOICE_FMA 0
-#endif
+// rtn_hi - 1 >= 0 as a signed integer; the select is done on the bit
+// patterns: y = v_hi - lo * (v_hi - v_lo) with lo = 0 or 1.
 template <bool GUIDED, bool WANT_G>
-__device__ __forceinline__ void train_pair(F2 ax, float inv_t, float S_t, F2 vr, F2& ym, F2& gsel,
+__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2& ym, F2& gsel,
                                            F2& grtn) {
   const F2 t = mul2_rn(ax, splat(inv_t));
   const F2 tc = {fminf(t.x, 6.0f), fminf(t.y, 6.0f)};
@@ -685,32 +689,24 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, float S_t, F2 vr,
   const F2 sn = add2_rn(tc, C);
   if (!GUIDED) {
     const F2 g = sub2_rn(sn, C);
-    ym = mul2_rn(g, splat(S_t));
+    ym = mul2_rn(g, St);
     gsel = g;
     grtn = g;
     return;
   }
   const F2 sz = add2_rz(tc, C), sp = add2_rp(tc, C);
   const F2 glo = sub2_rn(sz, C), ghi = sub2_rn(sp, C);
-  const F2 vlo = mul2_rn(glo, splat(S_t)), vhi = mul2_rn(ghi, splat(S_t));
+  const F2 vlo = mul2_rn(glo, St), vhi = mul2_rn(ghi, St);
   const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
   const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
   const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
-#if TFP4_CHOICE_FMA
-  const F2 a = sub2_rn(sn, sz);
-  const F2 D = mul2_rn(F2{diff0, diff1}, splat(0x1p127f));
-  const F2 D2 = fma2_rn(D, splat(0x1p127f), a);
-  const F2 h = {fmul_sat(D2.x, 0x1p127f), fmul_sat(D2.y, 0x1p127f)};
-  ym = fma2_rn(h, sub2_rn(vhi, vlo), vlo);
-  const bool hi0 = h.x != 0.0f, hi1 = h.y != 0.0f;
-#else
-  const int k0 = (int)(__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x));
-  const int k1 = (int)(__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y));
-  const bool hi0 = k0 >= 0, hi1 = k1 >= 0;
-  ym = F2{hi0 ? vhi.x : vlo.x, hi1 ? vhi.y : vlo.y};
-#endif
+  const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
+  const uint32_t lo1 = (__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y)) >> 31;
+  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
+  ym = F2{__uint_as_float(imad(lo0, __float_as_uint(vlo.x) - h0, h0)),
+          __uint_as_float(imad(lo1, __float_as_uint(vlo.y) - h1, h1))};
   if (WANT_G) {
-    gsel = F2{hi0 ? ghi.x : glo.x, hi1 ? ghi.y : glo.y};
+    gsel = F2{lo0 ? glo.x : ghi.x, lo1 ? glo.y : ghi.y};
     grtn = F2{sn.x != sz.x ? ghi.x : glo.x, sn.y != sz.y ? ghi.y : glo.y};
   }
 }
@@ -724,8 +720,11 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
+#ifndef TFP4_FQ_MIN_CTAS
+#define TFP4_FQ_MIN_CTAS 1
+#endif
 template <int KIND, bool MASK, bool CODES, bool STATS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     k_fakequant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
                 uint32_t steps_per_cta, const __grid_constant__ SegParam seg_t,
                 const float* __restrict__ gs_t, const __grid_constant__ SegParam seg_r,
@@ -819,31 +818,31 @@ __global__ void __launch_bounds__(kThreads)
         const int j0 = (i & 7) * 2;  // index of its low element in the block
         const uint32_t w = cur.w[i];
         const F2 ax = {__uint_as_float(a[i] << 16), __uint_as_float(a[i] & 0xFFFF0000u)};
-        const uint32_t sx0 = (w << 16) & 0x80000000u, sx1 = w & 0x80000000u;
+        const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
+        const uint32_t Stb = __float_as_uint(pt.S[b]);
+        const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
         F2 vr = {0.0f, 0.0f};
         F2 grs = {0.0f, 0.0f};  // signed rollout magnitudes (statistics)
         if (KIND == TRACE_GUIDE_COMPACT) {
           const uint32_t gw = b ? gcur.y : gcur.x;
-          const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw >> (16 + j0),
-                                    gw >> (17 + j0));
-          const uint32_t sr0 = (gw << (31 - j0)) & 0x80000000u;
-          const uint32_t sr1 = (gw << (30 - j0)) & 0x80000000u;
+          const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw, j0);
+          const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
+          const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
           const uint32_t Sb = __float_as_uint(pr.S[b]);
-          vr = mul2_rn(gr, F2{__uint_as_float(Sb | (sx0 ^ sr0)), __uint_as_float(Sb | (sx1 ^ sr1))});
+          vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
           if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
                               __uint_as_float(__float_as_uint(gr.y) | sr1)};
         } else if (KIND == TRACE_GUIDE_FULL) {
           const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
           float g0, g1;
           e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
-          const uint32_t Sb = __float_as_uint(pr.S[b]);
-          vr = mul2_rn(F2{g0, g1}, F2{__uint_as_float(Sb | sx0), __uint_as_float(Sb | sx1)});
+          vr = mul2_rn(F2{g0, g1}, splat(pr.S[b]));
           if (STATS) grs = F2{g0, g1};
         }
         F2 ym, gsel, grtn;
-        train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], pt.S[b], vr, ym, gsel, grtn);
-        ybits[i] = bf16x2_rn(ym.x, ym.y) | (w & 0x80008000u);
-        if (MASK) kept = (kept >> 1) | ((thr2[b] - a[i]) & 0x80008000u);
+        train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, ym, gsel, grtn);
+        ybits[i] = bf16x2_rn(ym.x, ym.y);
+        if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
         if (CODES || STATS) {
           const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
           const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
