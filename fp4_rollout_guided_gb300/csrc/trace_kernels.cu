@@ -720,8 +720,11 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
+#ifndef TFP4_FQ_PREFETCH
+#define TFP4_FQ_PREFETCH 0
+#endif
 #ifndef TFP4_FQ_MIN_CTAS
-#define TFP4_FQ_MIN_CTAS 1
+#define TFP4_FQ_MIN_CTAS 5
 #endif
 template <int KIND, bool MASK, bool CODES, bool STATS>
 __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
@@ -767,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   for (; step < step_end; ++step) {
     const uint32_t c0 = step * kThreads;
     const uint32_t c = c0 + threadIdx.x;
-    if (step + 1 < step_end) {
+    if (TFP4_FQ_PREFETCH && step + 1 < step_end) {
       const uint32_t cn = c + kThreads;
       if (cn < nchunks) {
         load_chunk(nxt, x, cn);
@@ -809,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         thr2[b] = (thr | 0x8000u) * 0x00010001u;
       }
 
-      uint32_t ybits[16];
+      uint32_t ybits[4];
       uint32_t cbytes[16];
       uint32_t kept = 0;
 #pragma unroll
@@ -841,7 +844,9 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         }
         F2 ym, gsel, grtn;
         train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, ym, gsel, grtn);
-        ybits[i] = bf16x2_rn(ym.x, ym.y);
+        ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
+        if ((i & 3) == 3)
+          st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
         if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
         if (CODES || STATS) {
           const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
@@ -857,10 +862,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       // word i left its two bits at positions i and 16 + i: interleave
       if (MASK) kept = spread16(kept & 0xFFFFu) | (spread16(kept >> 16) << 1);
-      uint8_t* yp = y + (uint64_t)c * 64u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_stream(yp + 16 * q, ybits[4 * q], ybits[4 * q + 1], ybits[4 * q + 2], ybits[4 * q + 3]);
       if (MASK) st_stream1(mask + (uint64_t)c * 4u, kept);
       if (CODES) {
         uint32_t o[4];
@@ -872,9 +873,24 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       if (STATS) n_done += 32;
     }
-    cur = nxt;
-    gcur = gnxt;
-    bcur = bnxt;
+    if (TFP4_FQ_PREFETCH) {
+      cur = nxt;
+      gcur = gnxt;
+      bcur = bnxt;
+    } else if (step + 1 < step_end) {
+      const uint32_t cn = c + kThreads;
+      if (cn < nchunks) {
+        load_chunk(cur, x, cn);
+        if (KIND == TRACE_GUIDE_COMPACT) {
+          const uint2 v = ld_stream2(guide + (uint64_t)cn * 8u);
+          gcur.x = v.x;
+          gcur.y = v.y;
+        } else if (KIND == TRACE_GUIDE_FULL) {
+          gcur = ld_stream(guide + (uint64_t)cn * 16u);
+        }
+        if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
+      }
+    }
   }
   if (STATS) {
     const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
