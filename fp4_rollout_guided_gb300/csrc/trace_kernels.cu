@@ -196,11 +196,11 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // (a bracket around q) encode to the same code, that code is the code of q.
 // Otherwise -- q within a few ulps of an E4M3 rounding boundary, or a
 // reciprocal that overflows -- the correctly rounded division decides.
-__device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, float gs) {
+// E4M3 codes of both blocks given den = gs * 6 and rden = fl(1 / den).
+__device__ __forceinline__ uint32_t pair_codes(float bamax0, float bamax1, float gs, float den,
+                                               float rden) {
   uint32_t codes = 0;
   if (gs > 0.0f) {
-    const float den = __fmul_rn(gs, 6.0f);
-    const float rden = __frcp_rn(den);
     bool exact = !(rden < __int_as_float(0x7F800000));
     if (!exact) {
       const float q0 = __fmul_rn(bamax0, rden), q1 = __fmul_rn(bamax1, rden);
@@ -211,6 +211,12 @@ __device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, floa
     }
     if (exact) codes = e4m3x2(__fdiv_rn(bamax0, den), __fdiv_rn(bamax1, den));
   }
+  return codes;
+}
+
+__device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, float gs) {
+  const float den = __fmul_rn(gs, 6.0f);
+  const uint32_t codes = pair_codes(bamax0, bamax1, gs, den, gs > 0.0f ? __frcp_rn(den) : 0.0f);
   PairScale p;
   p.codes = codes;
   real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
@@ -218,12 +224,41 @@ __device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, floa
   return p;
 }
 
+// STE threshold of a block in bf16 magnitude bits, doubled into two 16-bit
+// lanes with the lane top bits set: |x| > 6 * S exactly when the bf16 |x|
+// exceeds 6 * S rounded down to bf16 (truncation), so for a word of two
+// magnitudes, bit 15 / 31 of thr2 - |x| is set exactly when the element is
+// kept (no borrow crosses the lanes).
+__device__ __forceinline__ uint32_t ste_threshold2(float S) {
+  const uint32_t thr = S > 0.0f ? (__float_as_uint(__fmul_rn(6.0f, S)) >> 16) : 0x7FFFu;
+  return (thr | 0x8000u) * 0x00010001u;
+}
+
+// Per-segment table in shared memory, indexed by E4M3 code: the block's real
+// scale, its reciprocal (flush rule applied) and STE threshold.  A segment's
+// blocks take one of at most 127 scales, so the reciprocals are formed once
+// per segment instead of once per block.  Codes above 0x7E never come out of
+// the quantiser; a stored code is masked to 7 bits before the lookup.
+struct ScaleTab {
+  float2 sinv[128];
+  uint32_t thr2[128];
+};
+
+__device__ __forceinline__ void build_tab(ScaleTab& t, float gs) {
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+    float S, inv;
+    real_scale((uint32_t)c, gs, S, inv);
+    t.sinv[c] = make_float2(S, inv);
+    t.thr2[c] = ste_threshold2(S);
+  }
+}
+
 // Real scales of two stored E4M3 codes (the rollout side's record).
 __device__ __forceinline__ PairScale pair_scale_stored(uint32_t codes, float gs) {
   PairScale p;
   p.codes = codes;
-  real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
-  real_scale((codes >> 8) & 0xFFu, gs, p.S[1], p.inv[1]);
+  real_scale(codes & 0x7Fu, gs, p.S[0], p.inv[0]);
+  real_scale((codes >> 8) & 0x7Fu, gs, p.S[1], p.inv[1]);
   return p;
 }
 
@@ -749,6 +784,9 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   }
   Counters cnt = {};
   uint32_t n_done = 0;
+  __shared__ ScaleTab tab_t, tab_r;
+  int tseg = -1, rseg = -1;                 // segments the tables hold
+  float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
 
   Chunk cur, nxt;
   uint4 gcur = make_uint4(0, 0, 0, 0), gnxt = make_uint4(0, 0, 0, 0);
@@ -787,6 +825,24 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kThreads, nchunks) - 1);
     const bool uni_t = st.update(seg_t, r0, r1);
     const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
+    // refresh the scale tables when the (uniform) segment changes
+    const bool new_t = uni_t && st.cur != tseg;
+    const bool new_r = GUIDED && uni_r && sr.cur != rseg;
+    if (new_t || new_r) {
+      __syncthreads();
+      if (new_t) {
+        tseg = st.cur;
+        seg_gs = gs_t[tseg];
+        seg_den = __fmul_rn(seg_gs, 6.0f);
+        seg_rden = seg_gs > 0.0f ? __frcp_rn(seg_den) : 0.0f;
+        build_tab(tab_t, seg_gs);
+      }
+      if (new_r) {
+        rseg = sr.cur;
+        build_tab(tab_r, gs_r[rseg]);
+      }
+      __syncthreads();
+    }
     if (c < nchunks) {
       int s_t = st.cur, s_r = sr.cur;
       if (!uni_t || !uni_r) {
@@ -797,19 +853,34 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       uint32_t a[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-      const PairScale pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
-      PairScale pr = {};
-      if (GUIDED) pr = pair_scale_stored(bcur, gs_r[s_r]);
-      // STE threshold per block in bf16 magnitude bits: |x| > 6 * S exactly
-      // when the bf16 |x| exceeds 6 * S rounded down to bf16 (truncation), so
-      // two elements compare at once in 16-bit lanes: bit 15 of each lane of
-      // (0x8000 + thr) - |x| is set exactly when the element is kept.
+      PairScale pt, pr = {};
       uint32_t thr2[2];
+      if (uni_t) {
+        pt.codes = pair_codes(block_amax8(a), block_amax8(a + 8), seg_gs, seg_den, seg_rden);
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const uint32_t thr =
-            pt.S[b] > 0.0f ? (__float_as_uint(__fmul_rn(6.0f, pt.S[b])) >> 16) : 0x7FFFu;
-        thr2[b] = (thr | 0x8000u) * 0x00010001u;
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t code = (pt.codes >> (8 * b)) & 0xFFu;
+          const float2 e = tab_t.sinv[code];
+          pt.S[b] = e.x;
+          pt.inv[b] = e.y;
+          thr2[b] = tab_t.thr2[code];
+        }
+      } else {
+        pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
+        thr2[0] = ste_threshold2(pt.S[0]);
+        thr2[1] = ste_threshold2(pt.S[1]);
+      }
+      if (GUIDED) {
+        if (uni_r) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const float2 e = tab_r.sinv[(bcur >> (8 * b)) & 0x7Fu];
+            pr.S[b] = e.x;
+            pr.inv[b] = e.y;
+          }
+        } else {
+          pr = pair_scale_stored(bcur, gs_r[s_r]);
+        }
       }
 
       uint32_t ybits[4];
