@@ -735,11 +735,21 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2&
   const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
   const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
   const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
+#if TFP4_SELECT_IMAD
+  // lo = key >> 31 as the high word of key * 2; v_lo - v_hi on bit patterns
+  const uint32_t k0 = __float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x);
+  const uint32_t k1 = __float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y);
+  const uint32_t lo0 = __umulhi(k0, 2u), lo1 = __umulhi(k1, 2u);
+  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
+  ym = F2{__uint_as_float(imad(lo0, imad(h0, 0xFFFFFFFFu, __float_as_uint(vlo.x)), h0)),
+          __uint_as_float(imad(lo1, imad(h1, 0xFFFFFFFFu, __float_as_uint(vlo.y)), h1))};
+#else
   const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
   const uint32_t lo1 = (__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y)) >> 31;
   const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
   ym = F2{__uint_as_float(imad(lo0, __float_as_uint(vlo.x) - h0, h0)),
           __uint_as_float(imad(lo1, __float_as_uint(vlo.y) - h1, h1))};
+#endif
   if (WANT_G) {
     gsel = F2{lo0 ? glo.x : ghi.x, lo1 ? glo.y : ghi.y};
     grtn = F2{sn.x != sz.x ? ghi.x : glo.x, sn.y != sz.y ? ghi.y : glo.y};
@@ -759,7 +769,7 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
 #define TFP4_FQ_PREFETCH 0
 #endif
 #ifndef TFP4_FQ_MIN_CTAS
-#define TFP4_FQ_MIN_CTAS 5
+#define TFP4_FQ_MIN_CTAS 4
 #endif
 template <int KIND, bool MASK, bool CODES, bool STATS>
 __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
@@ -891,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         const int b = i >> 3;        // block of this word
         const int j0 = (i & 7) * 2;  // index of its low element in the block
         const uint32_t w = cur.w[i];
-        const F2 ax = {__uint_as_float(a[i] << 16), __uint_as_float(a[i] & 0xFFFF0000u)};
+        const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)), __uint_as_float(a[i] & 0xFFFF0000u)};
         const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
         const uint32_t Stb = __float_as_uint(pt.S[b]);
         const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
