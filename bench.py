@@ -51,6 +51,28 @@ def step_bytes_per_elem(guide: str) -> float:
             + KERNEL_BYTES["guide_unpack"] + fq)
 
 
+# DRAM bytes per element (read + write) of the dominant kernel from one ncu
+# capture (profiles/kernels_kv_rows_32x2x8192x8x128.md), valid only for the
+# kernel source it was taken on; a changed source reports traffic as null.
+MEASURED_TRAFFIC = {
+    "fakequant_compact": {"bytes_per_elem": 4.457, "kernels_sha1": "a383b27ee778"},
+}
+
+
+def kernels_sha1() -> str:
+    import hashlib
+    path = os.path.join(ROOT, "fp4_rollout_guided_gb300", "csrc", "trace_kernels.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def measured_traffic(kind: str, elems: int):
+    m = MEASURED_TRAFFIC.get("fakequant_" + kind)
+    if not m or m["kernels_sha1"] != kernels_sha1():
+        return None
+    return round(m["bytes_per_elem"] * elems / 1e9, 3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -325,7 +347,8 @@ def run_ours(args, w0):
     dom = max(kernels, key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
     roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
             "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / peak, 4),
-            "traffic": None, "peak_source": peak_src}
+            "traffic": measured_traffic(kind, elems) if dom == "fakequant" else None,
+            "traffic_unit": "GB per launch", "peak_source": peak_src}
 
     e2e = measure_e2e(args, h, w, x, r, step, dev, bpe, (y, mask, guide, bs, gs)) \
         if not args.no_e2e else None
