@@ -765,12 +765,6 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
-#ifndef TFP4_FQB_MIN_CTAS
-#define TFP4_FQB_MIN_CTAS 5
-#endif
-#ifndef TFP4_FQ_BLOCK_PER_THREAD
-#define TFP4_FQ_BLOCK_PER_THREAD 1
-#endif
 #ifndef TFP4_FQ_PREFETCH
 #define TFP4_FQ_PREFETCH 0
 #endif
@@ -993,197 +987,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   }
 }
 
-// Same computation with one 16-element block per thread (two threads per
-// 32-element chunk): half the per-thread state, so more warps fit per SM.
-// A step covers 128 chunks = 256 blocks.
-__device__ __forceinline__ uint32_t spread8(uint32_t v) {
-  v = (v | (v << 4)) & 0x0F0Fu;
-  v = (v | (v << 2)) & 0x3333u;
-  v = (v | (v << 1)) & 0x5555u;
-  return v;
-}
-
-template <int KIND, bool MASK, bool CODES, bool STATS>
-__global__ void __launch_bounds__(kThreads, TFP4_FQB_MIN_CTAS)
-    k_fakequant_b(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
-                  uint32_t steps_per_cta, const __grid_constant__ SegParam seg_t,
-                  const float* __restrict__ gs_t, const __grid_constant__ SegParam seg_r,
-                  const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
-                  const float* __restrict__ gs_r, uint8_t* __restrict__ y,
-                  uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
-                  trace_stats_t* __restrict__ stats) {
-  constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
-  constexpr uint32_t kChunksPerStep = kThreads / 2;
-  const uint32_t nblocks = nchunks * 2u;
-  const uint32_t nsteps = (nchunks + kChunksPerStep - 1) / kChunksPerStep;
-  uint32_t step = blockIdx.x * steps_per_cta;
-  const uint32_t step_end = min(step + steps_per_cta, nsteps);
-  StepSeg st, sr;
-  st.cur = 0;
-  sr.cur = 0;
-  if (step < step_end) {
-    const uint32_t r0 = cpr.div(step * kChunksPerStep);
-    st.cur = seg_search(seg_t, r0);
-    if (GUIDED) sr.cur = seg_search(seg_r, r0);
-  }
-  Counters cnt = {};
-  uint32_t n_done = 0;
-  __shared__ ScaleTab tab_t, tab_r;
-  int tseg = -1, rseg = -1;
-  float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
-
-  for (; step < step_end; ++step) {
-    const uint32_t c0 = step * kChunksPerStep;
-    const uint32_t blk = step * kThreads + threadIdx.x;
-    // issue this block's loads first; the segment bookkeeping below overlaps them
-    uint32_t w[8];
-    uint2 gv = make_uint2(0, 0);
-    uint32_t bcode = 0;
-    if (blk < nblocks) {
-      const uint8_t* p = x + (uint64_t)blk * 32u;
-      const uint4 v0 = ld_stream(p), v1 = ld_stream(p + 16);
-      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-      if (KIND == TRACE_GUIDE_COMPACT) {
-        unsigned int g;
-        asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(g) : "l"(guide + (uint64_t)blk * 4u));
-        gv.x = g;
-      } else if (KIND == TRACE_GUIDE_FULL) {
-        gv = ld_stream2(guide + (uint64_t)blk * 8u);
-      }
-      if (GUIDED) {
-        unsigned short b;
-        asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(b) : "l"(bs_r + blk));
-        bcode = b;
-      }
-    }
-    const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kChunksPerStep, nchunks) - 1);
-    const bool uni_t = st.update(seg_t, r0, r1);
-    const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
-    const bool new_t = uni_t && st.cur != tseg;
-    const bool new_r = GUIDED && uni_r && sr.cur != rseg;
-    if (new_t || new_r) {
-      __syncthreads();
-      if (new_t) {
-        tseg = st.cur;
-        seg_gs = gs_t[tseg];
-        seg_den = __fmul_rn(seg_gs, 6.0f);
-        seg_rden = seg_gs > 0.0f ? __frcp_rn(seg_den) : 0.0f;
-        build_tab(tab_t, seg_gs);
-      }
-      if (new_r) {
-        rseg = sr.cur;
-        build_tab(tab_r, gs_r[rseg]);
-      }
-      __syncthreads();
-    }
-    if (blk < nblocks) {
-      int s_t = st.cur, s_r = sr.cur;
-      if (!uni_t || !uni_r) {
-        const uint32_t row = cpr.div(blk >> 1);
-        if (!uni_t) s_t = seg_advance(seg_t, st.cur, row);
-        if (GUIDED && !uni_r) s_r = seg_advance(seg_r, sr.cur, row);
-      }
-      uint32_t a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = w[i] & kAbs2;
-      const float bamax = block_amax8(a);
-      float S_t, inv_t, S_r = 0.0f, inv_r = 0.0f;
-      uint32_t thr2;
-      if (uni_t) {
-        const uint32_t code = pair_codes(bamax, bamax, seg_gs, seg_den, seg_rden) & 0xFFu;
-        const float2 e = tab_t.sinv[code];
-        S_t = e.x;
-        inv_t = e.y;
-        thr2 = tab_t.thr2[code];
-      } else {
-        const PairScale ps = pair_scale(bamax, bamax, gs_t[s_t]);
-        S_t = ps.S[0];
-        inv_t = ps.inv[0];
-        thr2 = ste_threshold2(S_t);
-      }
-      if (GUIDED) {
-        if (uni_r) {
-          const float2 e = tab_r.sinv[bcode & 0x7Fu];
-          S_r = e.x;
-          inv_r = e.y;
-        } else {
-          real_scale(bcode & 0x7Fu, gs_r[s_r], S_r, inv_r);
-        }
-      }
-      uint32_t ybits[4];
-      uint32_t cbytes[8];
-      uint32_t kept = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j0 = 2 * i;
-        const uint32_t wi = w[i];
-        const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)), __uint_as_float(a[i] & 0xFFFF0000u)};
-        const uint32_t sx0 = imad(wi, 0x10000u, 0u) & 0x80000000u, sx1 = wi & 0x80000000u;
-        const uint32_t Stb = __float_as_uint(S_t);
-        const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
-        F2 vr = {0.0f, 0.0f};
-        F2 grs = {0.0f, 0.0f};
-        if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint32_t gw = gv.x;
-          const F2 gr = decode_pair(mul2_rn(ax, splat(inv_r)), gw, j0);
-          const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
-          const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
-          const uint32_t Sb = __float_as_uint(S_r);
-          vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
-          if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
-                              __uint_as_float(__float_as_uint(gr.y) | sr1)};
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          const uint32_t gword = i < 4 ? gv.x : gv.y;
-          float g0, g1;
-          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
-          vr = mul2_rn(F2{g0, g1}, splat(S_r));
-          if (STATS) grs = F2{g0, g1};
-        }
-        F2 ym, gsel, grtn;
-        train_pair<GUIDED, CODES || STATS>(ax, inv_t, St, vr, ym, gsel, grtn);
-        ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
-        if ((i & 3) == 3)
-          st_stream(y + (uint64_t)blk * 32u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-        if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2) & 0x80008000u);
-        if (CODES || STATS) {
-          const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
-          const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
-          if (CODES) cbytes[i] = e2m1x2(g0, g1);
-          if (STATS && GUIDED) {
-            count(cnt, signed_index(grs.x),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.x) | sx0)), signed_index(g0));
-            count(cnt, signed_index(grs.y),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.y) | sx1)), signed_index(g1));
-          }
-        }
-      }
-      if (MASK) {
-        // word i left its bits at 8 + i (even element) and 24 + i (odd)
-        const uint32_t m16 = spread8((kept >> 8) & 0xFFu) | (spread8(kept >> 24) << 1);
-        st_stream_u16(mask + (uint64_t)blk * 2u, m16);
-      }
-      if (CODES)
-        st_stream2(codes_t + (uint64_t)blk * 8u,
-                   cbytes[0] | (cbytes[1] << 8) | (cbytes[2] << 16) | (cbytes[3] << 24),
-                   cbytes[4] | (cbytes[5] << 8) | (cbytes[6] << 16) | (cbytes[7] << 24));
-      if (STATS) n_done += 16;
-    }
-  }
-  if (STATS) {
-    const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
-                            cnt.h_rtn[1], cnt.h_rtn[2], cnt.h_rtn[3], cnt.h_g[0],
-                            cnt.h_g[1],   cnt.h_g[2],   cnt.h_g[3]};
-    unsigned long long* dst = reinterpret_cast<unsigned long long*>(stats);
-#pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      if (!GUIDED && k > 0) break;
-      const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, v[k]);
-      if ((threadIdx.x & 31) == 0 && tot) atomicAdd(dst + k, (unsigned long long)tot);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // launch planning: persistent grids of (occupancy x SM count) CTAs, each
 // owning a contiguous range of steps
@@ -1225,13 +1028,8 @@ int64_t steps_of(int64_t nchunks, int64_t per_step) { return (nchunks + per_step
 template <int KIND, bool MASK, bool CODES, bool STATS>
 cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegParam& seg_r,
                       int sm_count, cudaStream_t st) {
-#if TFP4_FQ_BLOCK_PER_THREAD
-  auto kern = k_fakequant_b<KIND, MASK, CODES, STATS>;
-  const Plan p = plan_for((const void*)kern, steps_of(a.nchunks, kThreads / 2), sm_count);
-#else
   auto kern = k_fakequant<KIND, MASK, CODES, STATS>;
   const Plan p = plan_for((const void*)kern, steps_of(a.nchunks, kThreads), sm_count);
-#endif
   kern<<<p.grid, kThreads, 0, st>>>((const uint8_t*)a.x, (uint32_t)a.nchunks,
                                     FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
                                     seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
