@@ -1027,11 +1027,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       if (STATS) n_done += 32;
     }
-#if TFP4_FQ_CPASYNC
-    bcur = bnxt;
-    stg ^= 1;
-#else
-    if (TFP4_FQ_PREFETCH) {
+    if (TFP4_FQ_CPASYNC) {
+      bcur = bnxt;
+      stg ^= 1;
+    } else if (TFP4_FQ_PREFETCH) {
       cur = nxt;
       gcur = gnxt;
       bcur = bnxt;
@@ -1049,11 +1048,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
       }
     }
-#endif
   }
-#if TFP4_FQ_CPASYNC
-  cp_async_wait<0>();
-#endif
   if (STATS) {
     const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
                             cnt.h_rtn[1], cnt.h_rtn[2], cnt.h_rtn[3], cnt.h_g[0],
