@@ -83,29 +83,6 @@ __device__ __forceinline__ void st_stream_u16(void* p, uint32_t a) {
   asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)a) : "memory");
 }
 
-// Asynchronous global -> shared copies (LDGSTS): the data lands in shared
-// memory without passing through registers; a thread waits for its own
-// committed groups with cp.async.wait_group.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(smem)),
-               "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(smem)),
-               "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 struct Chunk {
   uint32_t w[16];  // 32 bf16: element 2i in the low half of w[i]
 };
@@ -788,9 +765,6 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
-#ifndef TFP4_FQ_CPASYNC
-#define TFP4_FQ_CPASYNC 1
-#endif
 #ifndef TFP4_FQ_PREFETCH
 #define TFP4_FQ_PREFETCH 0
 #endif
@@ -827,30 +801,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   Chunk cur, nxt;
   uint4 gcur = make_uint4(0, 0, 0, 0), gnxt = make_uint4(0, 0, 0, 0);
   uint32_t bcur = 0, bnxt = 0;
-#if TFP4_FQ_CPASYNC
-  // Double-buffered staging: while a thread computes its chunk of step k, its
-  // chunk of step k + 1 is already on its way into shared memory, so HBM keeps
-  // streaming through the compute phase.  Each thread copies and reads only
-  // its own slots, so no barrier is needed.
-  __shared__ __align__(16) uint4 sx[2][kThreads][4];
-  __shared__ __align__(16) uint4 sg[2][kThreads];
-  auto stage_copy = [&](int stg, uint32_t cc) {
-    if (cc < nchunks) {
-      const uint8_t* px = x + (uint64_t)cc * 64u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) cp_async16(&sx[stg][threadIdx.x][q], px + 16 * q);
-      if (KIND == TRACE_GUIDE_COMPACT) cp_async8(&sg[stg][threadIdx.x], guide + (uint64_t)cc * 8u);
-      if (KIND == TRACE_GUIDE_FULL) cp_async16(&sg[stg][threadIdx.x], guide + (uint64_t)cc * 16u);
-    }
-    cp_async_commit();
-  };
-  if (step < step_end) {
-    const uint32_t c = step * kThreads + threadIdx.x;
-    stage_copy(0, c);
-    if (GUIDED && c < nchunks) bcur = ld_stream_u16(bs_r + (uint64_t)c * 2u);
-  }
-  int stg = 0;
-#else
   if (step < step_end) {
     const uint32_t c = step * kThreads + threadIdx.x;
     if (c < nchunks) {
@@ -865,19 +815,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)c * 2u);
     }
   }
-#endif
   for (; step < step_end; ++step) {
     const uint32_t c0 = step * kThreads;
     const uint32_t c = c0 + threadIdx.x;
-#if TFP4_FQ_CPASYNC
-    if (step + 1 < step_end) {
-      stage_copy(stg ^ 1, c + kThreads);
-      if (GUIDED && c + kThreads < nchunks) bnxt = ld_stream_u16(bs_r + (uint64_t)(c + kThreads) * 2u);
-    } else {
-      cp_async_commit();
-    }
-#endif
-    if (!TFP4_FQ_CPASYNC && TFP4_FQ_PREFETCH && step + 1 < step_end) {
+    if (TFP4_FQ_PREFETCH && step + 1 < step_end) {
       const uint32_t cn = c + kThreads;
       if (cn < nchunks) {
         load_chunk(nxt, x, cn);
@@ -912,20 +853,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       __syncthreads();
     }
-#if TFP4_FQ_CPASYNC
-    cp_async_wait<1>();  // this step's copies have landed
-    if (c < nchunks) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = sx[stg][threadIdx.x][q];
-        cur.w[4 * q + 0] = v.x;
-        cur.w[4 * q + 1] = v.y;
-        cur.w[4 * q + 2] = v.z;
-        cur.w[4 * q + 3] = v.w;
-      }
-      if (GUIDED) gcur = sg[stg][threadIdx.x];
-    }
-#endif
     if (c < nchunks) {
       int s_t = st.cur, s_r = sr.cur;
       if (!uni_t || !uni_r) {
@@ -1027,10 +954,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       if (STATS) n_done += 32;
     }
-    if (TFP4_FQ_CPASYNC) {
-      bcur = bnxt;
-      stg ^= 1;
-    } else if (TFP4_FQ_PREFETCH) {
+    if (TFP4_FQ_PREFETCH) {
       cur = nxt;
       gcur = gnxt;
       bcur = bnxt;
