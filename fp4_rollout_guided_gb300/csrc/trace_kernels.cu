@@ -304,18 +304,6 @@ __device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-// High word of a * b on the FMA pipe (IMAD.HI); with b a power of two this
-// is a right shift that leaves the integer pipe free.
-__device__ __forceinline__ uint32_t imad_hi(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0u));
-  return d;
-}
-
-#ifndef TFP4_ALU_DIET
-#define TFP4_ALU_DIET 1
-#endif
-
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float d;
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -588,16 +576,7 @@ __device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t gw, int j0) {
   const uint32_t b0 = 1u << (16 + j0), b1 = 1u << (17 + j0);
   const uint32_t m0 = (imad(__float_as_uint(uz.x), b0, 0u) ^ gw) & b0;
   const uint32_t m1 = (imad(__float_as_uint(uz.y), b1, 0u) ^ gw) & b1;
-#if TFP4_ALU_DIET
-  // mismatch bit -> 0/1 through the high product word, then a multiply-add
-  // selects between the two sums' bit patterns
-  const uint32_t z0 = __float_as_uint(uz.x), z1 = __float_as_uint(uz.y);
-  const uint32_t k0 = imad_hi(m0, 1u << (16 - j0)), k1 = imad_hi(m1, 1u << (15 - j0));
-  const F2 us = {__uint_as_float(imad(k0, imad(z0, 0xFFFFFFFFu, __float_as_uint(up.x)), z0)),
-                 __uint_as_float(imad(k1, imad(z1, 0xFFFFFFFFu, __float_as_uint(up.y)), z1))};
-#else
   const F2 us = {m0 ? up.x : uz.x, m1 ? up.y : uz.y};
-#endif
   return sub2_rn(us, C);
 }
 
@@ -764,13 +743,6 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2&
   const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
   ym = F2{__uint_as_float(imad(lo0, imad(h0, 0xFFFFFFFFu, __float_as_uint(vlo.x)), h0)),
           __uint_as_float(imad(lo1, imad(h1, 0xFFFFFFFFu, __float_as_uint(vlo.y)), h1))};
-#elif TFP4_ALU_DIET
-  const uint32_t k0 = __float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x);
-  const uint32_t k1 = __float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y);
-  const uint32_t lo0 = imad_hi(k0, 2u), lo1 = imad_hi(k1, 2u);
-  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
-  ym = F2{__uint_as_float(imad(lo0, imad(h0, 0xFFFFFFFFu, __float_as_uint(vlo.x)), h0)),
-          __uint_as_float(imad(lo1, imad(h1, 0xFFFFFFFFu, __float_as_uint(vlo.y)), h1))};
 #else
   const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
   const uint32_t lo1 = (__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y)) >> 31;
@@ -929,12 +901,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         const int b = i >> 3;        // block of this word
         const int j0 = (i & 7) * 2;  // index of its low element in the block
         const uint32_t w = cur.w[i];
-#if TFP4_ALU_DIET
-        const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)),
-                       __uint_as_float(imad(imad_hi(a[i], 0x10000u), 0x10000u, 0u))};
-#else
         const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)), __uint_as_float(a[i] & 0xFFFF0000u)};
-#endif
         const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
         const uint32_t Stb = __float_as_uint(pt.S[b]);
         const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
@@ -961,11 +928,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
         if ((i & 3) == 3)
           st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-#if TFP4_ALU_DIET
-        if (MASK) kept = imad_hi(kept, 0x80000000u) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
-#else
         if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
-#endif
         if (CODES || STATS) {
           const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
           const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
