@@ -79,6 +79,7 @@ def _load():
             "orc_train_fakequant_given": (INT, [P, I64, I64, P, I32, P, INT, P, P, P, P,
                                                 I32, P, P, P, P]),
             "orc_guide_pack": (INT, [P, I64, I64, P]),
+            "orc_ste_backward": (INT, [P, P, I64, I64, P]),
             "orc_guide_unpack": (INT, [P, P, P, P, P, I32, I64, I64, P]),
             "orc_train_fakequant": (INT, [P, I64, I64, P, I32, INT, P, P, P, P,
                                           I32, P, P, P, P]),
@@ -261,3 +262,13 @@ def train_fakequant(x, seg_t=None, kind=GUIDE_NONE, guide=None, bs_r=None,
                                            _ptr(stats))
     _check(rc, "train_fakequant")
     return y, mask, codes_t, stats
+
+
+def ste_backward(g, mask):
+    """-> uint16[rows, cols]: g where the mask bit is 1, +0 elsewhere."""
+    g = _u16(g)
+    rows, cols = g.shape
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    out = np.zeros((rows, cols), dtype=np.uint16)
+    _check(_load().orc_ste_backward(_ptr(g), _ptr(mask), rows, cols, _ptr(out)), "ste_backward")
+    return out

@@ -523,3 +523,18 @@ int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,
   }
   return 0;
 }
+
+/* Straight-through estimator ("QAT" in the article's title implies a
+ * fake quantiser trained through; READING: the gradient passes unchanged for
+ * kept elements and is cut to +0 for elements clipped by the top code). */
+int orc_ste_backward(const uint16_t* g, const uint32_t* mask, int64_t rows, int64_t cols,
+                     uint16_t* out) {
+  if (check_shape(rows, cols)) return -1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      int64_t e = r * cols + c;
+      int kept = (int)((mask[e / 32] >> (e % 32)) & 1u);
+      out[e] = kept ? g[e] : (uint16_t)0;
+    }
+  return 0;
+}

@@ -111,6 +111,12 @@ int orc_train_fakequant(const uint16_t* x, int64_t rows, int64_t cols,
                         int32_t n_seg_r, uint16_t* y, uint32_t* mask,
                         uint8_t* codes_t, uint64_t* stats);
 
+/* Straight-through backward of the fake quantiser: the incoming gradient
+ * passes where the element's mask bit is 1 and becomes +0 where it is 0.
+ *   g, out  uint16 [rows, cols] bf16 patterns;  mask uint32 [rows, cols/32] */
+int orc_ste_backward(const uint16_t* g, const uint32_t* mask, int64_t rows, int64_t cols,
+                     uint16_t* out);
+
 /* Same as orc_train_fakequant with the training maxima taken from
  * amax_t_in [n_seg_t] (see orc_rollout_quant_given). */
 int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,

@@ -703,3 +703,23 @@ def test_unrelated_rollout_statistics(orc):
     assert np.count_nonzero(np.signbit(xf) != (n_r >> 3).astype(bool)) > 1000
     np.testing.assert_array_equal(nibbles(c_f)[inside], nibbles(c_c)[inside])
     np.testing.assert_array_equal(nibbles(dec)[inside], n_r[inside])
+
+
+def test_ste_backward_against_numpy_unpackbits(orc):
+    """The backward passes the gradient where numpy's little-endian unpacking
+    of the mask words has a 1 and gives +0 elsewhere; with the fake
+    quantiser's own mask, clipped elements (|x| > 6 S) get no gradient."""
+    rng = np.random.default_rng(3)
+    rows, cols = 37, 96
+    g = rng.integers(0, 2 ** 16, (rows, cols), dtype=np.uint64).astype(np.uint16)
+    m = rng.integers(0, 2 ** 32, (rows, cols // 32), dtype=np.uint64).astype(np.uint32)
+    out = orc.ste_backward(g, m)
+    bits = np.unpackbits(m.view(np.uint8), bitorder="little").reshape(rows, cols).astype(bool)
+    np.testing.assert_array_equal(out, np.where(bits, g, 0))
+    row = np.zeros(64, np.float32)
+    row[0], row[35] = 2688.0, 147.0                      # element 35 is clipped (see above)
+    x = bf16_bits(row).reshape(1, 64)
+    _, mask, _, _ = orc.train_fakequant(x)
+    grad = np.full((1, 64), 0x3F80, np.uint16)             # all ones
+    gi = orc.ste_backward(grad, mask)
+    assert gi[0, 35] == 0 and np.all(np.delete(gi[0], 35) == 0x3F80)
