@@ -363,6 +363,27 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
   return TRACE_OK;
 }
 
+trace_status_t trace_ste_backward(trace_handle_t h, const void* grad_out_bf16,
+                                  const uint32_t* ste_mask, int64_t rows, int64_t cols,
+                                  void* grad_in_bf16, trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  const bool empty = rows == 0;
+  for (const void* p : {grad_out_bf16, (const void*)ste_mask, (const void*)grad_in_bf16})
+    if ((s = check_tensor(p, empty)) != TRACE_OK) return s;
+  const int64_t nchunks = rows * (cols / 32);
+  if (nchunks == 0) return TRACE_OK;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = timed(h, TRACE_KERNEL_STE_BACKWARD, st, [&] {
+    return tfp4::launch_ste_backward(grad_out_bf16, ste_mask, nchunks, grad_in_bf16, h->sm_count,
+                                     st);
+  });
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
 trace_status_t trace_profile_enable(trace_handle_t h, int enable) {
   if (!h) return TRACE_ERR_INVALID_ARG;
   h->profiling = enable != 0;

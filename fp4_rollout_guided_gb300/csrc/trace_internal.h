@@ -67,6 +67,10 @@ cudaError_t launch_guide_unpack(const void* x_ref, const uint32_t* guide, const 
                                 const SegParam& seg_r, void* codes, int sm_count,
                                 cudaStream_t st);
 
+// backward: straight-through gradient through the fake quantiser.
+cudaError_t launch_ste_backward(const void* g, const uint32_t* mask, int64_t nchunks, void* out,
+                                int sm_count, cudaStream_t st);
+
 // a5 + a6: training-side guided fake quantisation.
 struct FakequantArgs {
   const void* x;

@@ -988,6 +988,54 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
 }
 
 // ---------------------------------------------------------------------------
+// straight-through backward: grad_in = grad_out where the mask bit is 1, +0
+// elsewhere.  One chunk (32 elements, one mask word) per thread per step;
+// each mask bit pair becomes a 0xFFFF / 0x0000 lane mask for a bf16x2 word.
+// ---------------------------------------------------------------------------
+
+constexpr int kSteChunks = 2;  // chunks per thread per step (bytes in flight)
+
+__global__ void __launch_bounds__(kThreads)
+    k_ste_backward(const uint8_t* __restrict__ g, const uint8_t* __restrict__ mask,
+                   uint32_t nchunks, uint32_t steps_per_cta, uint8_t* __restrict__ out) {
+  constexpr uint32_t kStep = kThreads * kSteChunks;
+  const uint32_t nsteps = (nchunks + kStep - 1) / kStep;
+  uint32_t step = blockIdx.x * steps_per_cta;
+  const uint32_t step_end = min(step + steps_per_cta, nsteps);
+  for (; step < step_end; ++step) {
+    Chunk v[kSteChunks];
+    uint32_t m[kSteChunks];
+#pragma unroll
+    for (int k = 0; k < kSteChunks; ++k) {
+      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
+      if (c < nchunks) {
+        load_chunk(v[k], g, c);
+        unsigned int mw;
+        asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(mw) : "l"(mask + (uint64_t)c * 4u));
+        m[k] = mw;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kSteChunks; ++k) {
+      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
+      if (c < nchunks) {
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          // bits 2i, 2i+1 -> lane masks (0 - bit keeps all 16 lane bits)
+          const uint32_t lo = (0u - ((m[k] >> (2 * i)) & 1u)) & 0x0000FFFFu;
+          const uint32_t hi = (0u - ((m[k] >> (2 * i + 1)) & 1u)) & 0xFFFF0000u;
+          o[i] = v[k].w[i] & (lo | hi);
+        }
+        uint8_t* p = out + (uint64_t)c * 64u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_stream(p + 16 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launch planning: persistent grids of (occupancy x SM count) CTAs, each
 // owning a contiguous range of steps
 // ---------------------------------------------------------------------------
@@ -1096,6 +1144,15 @@ cudaError_t launch_guide_unpack(const void* x_ref, const uint32_t* guide, const 
   k_guide_unpack<<<p.grid, kThreads, 0, st>>>(
       (const uint8_t*)x_ref, (const uint8_t*)guide, (const uint8_t*)bs_r, gs_r,
       (uint32_t)nchunks, FastDivU((uint32_t)cpr), p.steps_per_cta, seg_r, (uint8_t*)codes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ste_backward(const void* g, const uint32_t* mask, int64_t nchunks, void* out,
+                                int sm_count, cudaStream_t st) {
+  const Plan p = plan_for((const void*)k_ste_backward,
+                          steps_of(nchunks, (int64_t)kThreads * kSteChunks), sm_count);
+  k_ste_backward<<<p.grid, kThreads, 0, st>>>((const uint8_t*)g, (const uint8_t*)mask,
+                                              (uint32_t)nchunks, p.steps_per_cta, (uint8_t*)out);
   return cudaGetLastError();
 }
 

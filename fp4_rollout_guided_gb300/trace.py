@@ -24,7 +24,7 @@ from . import build as _build
 
 GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
-KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant")
+KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward")
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
           4: "CUDA error", 5: "out of memory", 6: "timeout"}
@@ -64,6 +64,7 @@ SIGNATURES = {
     "trace_guide_unpack": (INT, [P, P, P, P, P, Segments, I64, I64, P, P]),
     "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
                                     P, P, P]),
+    "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
     "trace_rollout_quant_noalloc": (INT, [P, I64, I64, Segments, P, P, P, P, P]),
     "trace_profile_enable": (INT, [P, INT]),
     "trace_profile_collect": (INT, [P, ctypes.POINTER(KernelTime)]),
@@ -245,6 +246,20 @@ class Handle:
         self._check("trace_train_fakequant", st)
         return y, m, c, stats
 
+    # -- backward ---------------------------------------------------------------
+    def ste_backward(self, grad_out: torch.Tensor, mask: torch.Tensor, out=None):
+        """grad_in = grad_out where the STE mask bit is 1, +0 elsewhere."""
+        rows, cols = grad_out.shape
+        if out is None:
+            out = torch.empty_like(grad_out)
+        _need(grad_out, torch.bfloat16, (rows, cols), "grad_out", self.device)
+        _need(mask, torch.int32, (rows, cols // 32), "mask", self.device)
+        _need(out, torch.bfloat16, (rows, cols), "grad_in", self.device)
+        st = lib().trace_ste_backward(self._h, _ptr(grad_out), _ptr(mask), rows, cols, _ptr(out),
+                                      _stream())
+        self._check("trace_ste_backward", st)
+        return out
+
     # -- profiler ---------------------------------------------------------------
     def profile(self, enable: bool = True):
         self._check("trace_profile_enable", lib().trace_profile_enable(self._h, int(enable)))
@@ -269,3 +284,28 @@ def stats_dict(stats: torch.Tensor) -> dict:
 __all__: Sequence[str] = ["Handle", "TraceError", "lib", "library_path", "new_stats",
                           "stats_dict", "GUIDE_NONE", "GUIDE_FULL", "GUIDE_COMPACT",
                           "KERNELS", "SIGNATURES", "MAX_SEGMENTS"]
+
+
+class GuidedFakeQuant(torch.autograd.Function):
+    """Rollout-guided FP4 fake quantisation as an autograd function: the
+    forward is trace_train_fakequant, the backward the straight-through
+    estimator (trace_ste_backward) with the forward's mask."""
+
+    @staticmethod
+    def forward(ctx, x, handle, seg_t, kind, guide, bs_r, gs_r, seg_r):
+        y, mask, _, _ = handle.train_fakequant(x.contiguous(), seg_t, kind, guide, bs_r, gs_r,
+                                               seg_r, mask=True)
+        ctx.handle = handle
+        ctx.save_for_backward(mask)
+        return y
+
+    @staticmethod
+    def backward(ctx, grad_y):
+        (mask,) = ctx.saved_tensors
+        g = grad_y.contiguous().to(torch.bfloat16)
+        return ctx.handle.ste_backward(g, mask), None, None, None, None, None, None, None
+
+
+def guided_fake_quant(x, handle, seg_t=None, kind="none", guide=None, bs_r=None, gs_r=None,
+                      seg_r=None):
+    return GuidedFakeQuant.apply(x, handle, seg_t, kind, guide, bs_r, gs_r, seg_r)

@@ -125,7 +125,8 @@ typedef enum {
   TRACE_KERNEL_GUIDE_PACK = 2,
   TRACE_KERNEL_GUIDE_UNPACK = 3,
   TRACE_KERNEL_FAKEQUANT = 4,
-  TRACE_KERNEL_COUNT = 5
+  TRACE_KERNEL_STE_BACKWARD = 5,
+  TRACE_KERNEL_COUNT = 6
 } trace_kernel_id_t;
 
 typedef struct {
@@ -208,6 +209,17 @@ TRACE_API trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_b
                                      trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
                                      void* codes_t_u8, trace_stats_t* stats_dev,
                                      trace_stream_t stream);
+
+/* Backward of the fake quantiser through the straight-through estimator
+ * (the article's title names quantization-aware training, which trains
+ * through the fake quantiser): grad_in = grad_out where the element's mask
+ * bit (from trace_train_fakequant) is 1, +0 where it is 0.
+ *   grad_out_bf16 [rows, cols]; ste_mask [rows, cols/32];
+ *   grad_in_bf16 [rows, cols] out (may alias grad_out_bf16). */
+TRACE_API trace_status_t trace_ste_backward(trace_handle_t h, const void* grad_out_bf16,
+                                            const uint32_t* ste_mask, int64_t rows,
+                                            int64_t cols, void* grad_in_bf16,
+                                            trace_stream_t stream);
 
 /* Rollout-side quantisation without a handle and without any device
  * allocation.  The paper has no counterpart: this is a deployment variant of

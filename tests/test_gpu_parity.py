@@ -293,3 +293,43 @@ def sampled_check(h, cfg, windows_per_seg=2, window_rows=1536, seg_picks=3):
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_full_size_sampled(h, cfg):
     sampled_check(h, cfg)
+
+
+# ---------------------------------------------------------------------------
+# straight-through backward and the autograd wrapper
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [1, 3, 5])
+def test_ste_backward_bit_exact(h, cfg):
+    w = synth.workload(cfg, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    xg = x.to(DEV)
+    _, m, _, _ = h.train_fakequant(xg, w.seg_t, "none")
+    g = rand_bf16(tuple(x.shape), 99 + cfg, scale=0.3)
+    gi = h.ste_backward(g.to(DEV), m)
+    # in place: the output may alias the incoming gradient
+    gg = g.to(DEV)
+    h.ste_backward(gg, m, out=gg)
+    torch.cuda.synchronize()
+    _, om, _, _ = oracle.train_fakequant(u16(x), w.seg_t)
+    want = oracle.ste_backward(u16(g), om)
+    assert_same(f"cfg{cfg} ste", u16(gi), want)
+    assert_same(f"cfg{cfg} ste in place", u16(gg), want)
+
+
+def test_autograd_guided_fake_quant(h):
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(2, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    xg, rg = x.to(DEV), r.to(DEV)
+    codes, bs, gs, guide = h.rollout_quant(rg, w.seg_r)
+    xr = xg.clone().requires_grad_(True)
+    y = trace.guided_fake_quant(xr, h, w.seg_t, "compact", guide, bs, gs, w.seg_r)
+    y.float().sum().backward()
+    torch.cuda.synchronize()
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(u16(r), w.seg_r)
+    o_y, o_m, _, _ = oracle.train_fakequant(u16(x), w.seg_t, oracle.GUIDE_COMPACT, o_guide, o_bs,
+                                            o_gs, w.seg_r)
+    assert_same("autograd y", u16(y.detach()), o_y)
+    ones = np.full(u16(x).shape, 0x3F80, np.uint16)          # bf16 1.0
+    assert_same("autograd grad", u16(xr.grad), oracle.ste_backward(ones, o_m))
