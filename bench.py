@@ -467,6 +467,79 @@ def _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope, step=None, outs=None):
     return {"ms": ms, "elems": rows * w.cols, "h2d": h2d, "d2h": d2h, "scope": scope}
 
 
+def run_transport(args, w):
+    """Guide-record transport on one GPU: device -> pinned host (export),
+    host -> file (write + fsync), file -> pinned host (read), pinned host ->
+    device (import), for the full record (4-bit codes) and the compact one
+    (2 bits per element), on the same rollout output.  Prints one JSON line."""
+    import tempfile
+    from fp4_rollout_guided_gb300 import build, synth, trace
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    h = trace.Handle(0)
+    x, r = synth.make_inputs(w, dev)
+    del x
+    codes, bs, gs, guide = h.rollout_quant(r, w.seg_r)
+    del r
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    res = {}
+    tmp = tempfile.mkdtemp(prefix="trace_record_")
+    try:
+        for kind, g in (("full", codes), ("compact", guide)):
+            size = trace.record_size(kind, w.rows, w.cols, w.n_seg_r)
+            host = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+            out = (torch.empty_like(g), torch.empty_like(bs), torch.empty_like(gs))
+            for _ in range(args.warmup):
+                h.record_export(g, bs, gs, w.seg_r, out=host)
+                h.record_import(host, out=out)
+            torch.cuda.synchronize()
+            d2h, h2d = [], []
+            for _ in range(args.steps):
+                a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                a.record(stream)
+                h.record_export(g, bs, gs, w.seg_r, out=host, wait=False)
+                b.record(stream)
+                h.record_import(host, out=out)
+                c.record(stream)
+                c.synchronize()
+                d2h.append(a.elapsed_time(b))
+                h2d.append(b.elapsed_time(c))
+            assert torch.equal(out[0], g) and torch.equal(out[1], bs)
+            path = os.path.join(tmp, f"{kind}.trg")
+            t0 = time.perf_counter()
+            trace.save_record(host, path)
+            with open(path, "rb+") as f:
+                os.fsync(f.fileno())
+            t_write = time.perf_counter() - t0
+            t0 = time.perf_counter()
+            back = trace.load_record(path)
+            t_read = time.perf_counter() - t0
+            assert torch.equal(back, host)
+            os.remove(path)
+            del back
+            ms_d2h, ms_h2d = statistics.median(d2h), statistics.median(h2d)
+            res[kind] = {"record_bytes": size, "guide_bytes": g.numel() * g.element_size(),
+                         "d2h_ms": round(ms_d2h, 4), "d2h_gbs": round(size / ms_d2h / 1e6, 2),
+                         "h2d_ms": round(ms_h2d, 4), "h2d_gbs": round(size / ms_h2d / 1e6, 2),
+                         "disk_write_ms": round(t_write * 1e3, 2),
+                         "disk_read_ms": round(t_read * 1e3, 2)}
+    finally:
+        os.rmdir(tmp)
+    line = {"metric": "guide record transport (device->host->disk->host->device)",
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "config": {"workload": w.name, "rows": w.rows, "cols": w.cols,
+                       "rollout_segments": w.n_seg_r},
+            "full": res["full"], "compact": res["compact"],
+            "compact_over_full_bytes": round(res["compact"]["record_bytes"]
+                                             / res["full"]["record_bytes"], 4),
+            "disk_note": "write includes fsync; read is from the page cache"}
+    print(json.dumps(line), flush=True)
+    h.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,12 +551,16 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--transport", action="store_true",
+                    help="time the guide record's device/host/disk round trip instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     from fp4_rollout_guided_gb300 import synth
     w = synth.workload(args.workload, seed=args.seed)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.transport:
+        return run_transport(args, w)
     return run_ours(args, w)
 
 

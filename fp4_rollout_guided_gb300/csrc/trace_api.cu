@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string.h>
+
 #include <mutex>
 #include <new>
 #include <vector>
@@ -380,6 +382,135 @@ trace_status_t trace_ste_backward(trace_handle_t h, const void* grad_out_bf16,
     return tfp4::launch_ste_backward(grad_out_bf16, ste_mask, nchunks, grad_in_bf16, h->sm_count,
                                      st);
   });
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+// ---- guide transport -------------------------------------------------------
+
+static_assert(sizeof(trace_record_header_t) == 64, "record header is 64 bytes");
+
+static uint64_t align256(uint64_t v) { return (v + 255u) & ~uint64_t(255); }
+
+// Full record: one 4-bit code per element; compact: one 32-bit word (16 sign
+// bits, 16 index-parity bits) per 16 elements.
+static uint64_t record_guide_bytes(const trace_record_header_t& hd) {
+  return hd.kind == TRACE_GUIDE_FULL ? (uint64_t)hd.rows * (uint64_t)(hd.cols / 2)
+                                     : (uint64_t)hd.rows * (uint64_t)(hd.cols / 16) * 4;
+}
+
+static uint64_t record_bs_bytes(const trace_record_header_t& hd) {
+  return (uint64_t)hd.rows * (uint64_t)(hd.cols / 16);
+}
+
+static bool record_layout(trace_guide_kind_t kind, int64_t rows, int64_t cols, int32_t n_seg,
+                          trace_record_header_t* hd) {
+  if (kind != TRACE_GUIDE_FULL && kind != TRACE_GUIDE_COMPACT) return false;
+  if (check_shape(rows, cols) != TRACE_OK) return false;
+  if (n_seg < 1 || n_seg > TRACE_MAX_SEGMENTS) return false;
+  memset(hd, 0, sizeof(*hd));
+  hd->kind = (uint32_t)kind;
+  hd->rows = rows;
+  hd->cols = cols;
+  const uint64_t guide_bytes = record_guide_bytes(*hd), bs_bytes = record_bs_bytes(*hd);
+  hd->magic = TRACE_RECORD_MAGIC;
+  hd->version = 1;
+  hd->n_seg = n_seg;
+  hd->guide_offset = 256;
+  hd->bs_offset = align256(hd->guide_offset + guide_bytes);
+  hd->gs_offset = align256(hd->bs_offset + bs_bytes);
+  hd->seg_offset = align256(hd->gs_offset + sizeof(float) * (uint64_t)n_seg);
+  return true;
+}
+
+static uint64_t record_end(const trace_record_header_t& hd) {
+  return hd.seg_offset + sizeof(int64_t) * ((uint64_t)hd.n_seg + 1);
+}
+
+extern "C" size_t trace_record_size(trace_guide_kind_t kind, int64_t rows, int64_t cols,
+                                    int32_t n_seg) {
+  trace_record_header_t hd;
+  if (!record_layout(kind, rows, cols, n_seg, &hd)) return 0;
+  return (size_t)record_end(hd);
+}
+
+extern "C" trace_status_t trace_record_export(trace_handle_t h, trace_guide_kind_t kind,
+                                              const void* guide, const void* bs,
+                                              const float* gs, int64_t rows, int64_t cols,
+                                              trace_segments_t seg, void* host_dst,
+                                              size_t dst_bytes, trace_stream_t stream) {
+  if (!h || !host_dst) return TRACE_ERR_INVALID_ARG;
+  const int32_t n_seg = seg.row_offsets ? seg.n_seg : 1;
+  trace_record_header_t hd;
+  if (!record_layout(kind, rows, cols, n_seg, &hd)) return TRACE_ERR_INVALID_ARG;
+  if (dst_bytes < record_end(hd)) return TRACE_ERR_INVALID_ARG;
+  static thread_local tfp4::SegParam sp;
+  trace_status_t s = make_segments(seg, rows, &sp);
+  if (s != TRACE_OK) return s;
+  const bool empty = rows == 0;
+  if ((s = check_tensor(guide, empty)) != TRACE_OK) return s;
+  if ((s = check_tensor(bs, empty)) != TRACE_OK) return s;
+  if (!gs) return TRACE_ERR_INVALID_ARG;
+  uint8_t* dst = (uint8_t*)host_dst;
+  memset(dst, 0, 256);
+  memcpy(dst, &hd, sizeof(hd));
+  int64_t* offs = (int64_t*)(dst + hd.seg_offset);
+  for (int32_t i = 0; i <= n_seg; ++i) offs[i] = sp.off[i];
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const uint64_t guide_bytes = record_guide_bytes(hd), bs_bytes = record_bs_bytes(hd);
+  cudaError_t e = cudaSuccess;
+  if (guide_bytes) e = cudaMemcpyAsync(dst + hd.guide_offset, guide, guide_bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && bs_bytes)
+    e = cudaMemcpyAsync(dst + hd.bs_offset, bs, bs_bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dst + hd.gs_offset, gs, sizeof(float) * n_seg, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+extern "C" trace_status_t trace_record_info(const void* host_src, size_t src_bytes,
+                                            trace_record_header_t* out) {
+  if (!host_src || !out || src_bytes < sizeof(trace_record_header_t)) return TRACE_ERR_INVALID_ARG;
+  trace_record_header_t hd;
+  memcpy(&hd, host_src, sizeof(hd));
+  trace_record_header_t ref;
+  if (hd.magic != TRACE_RECORD_MAGIC || hd.version != 1) return TRACE_ERR_INVALID_ARG;
+  if (!record_layout((trace_guide_kind_t)hd.kind, hd.rows, hd.cols, hd.n_seg, &ref))
+    return TRACE_ERR_INVALID_ARG;
+  if (ref.guide_offset != hd.guide_offset || ref.bs_offset != hd.bs_offset ||
+      ref.gs_offset != hd.gs_offset || ref.seg_offset != hd.seg_offset)
+    return TRACE_ERR_INVALID_ARG;
+  if (src_bytes < record_end(hd)) return TRACE_ERR_INVALID_ARG;
+  const int64_t* offs = (const int64_t*)((const uint8_t*)host_src + hd.seg_offset);
+  if (offs[0] != 0 || offs[hd.n_seg] != hd.rows) return TRACE_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < hd.n_seg; ++i)
+    if (offs[i + 1] < offs[i]) return TRACE_ERR_INVALID_ARG;
+  *out = hd;
+  return TRACE_OK;
+}
+
+extern "C" trace_status_t trace_record_import(trace_handle_t h, const void* host_src,
+                                              size_t src_bytes, void* guide, void* bs, float* gs,
+                                              trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_record_header_t hd;
+  trace_status_t s = trace_record_info(host_src, src_bytes, &hd);
+  if (s != TRACE_OK) return s;
+  const bool empty = hd.rows == 0;
+  if ((s = check_tensor(guide, empty)) != TRACE_OK) return s;
+  if ((s = check_tensor(bs, empty)) != TRACE_OK) return s;
+  if (!gs) return TRACE_ERR_INVALID_ARG;
+  const uint64_t guide_bytes = record_guide_bytes(hd), bs_bytes = record_bs_bytes(hd);
+  const uint8_t* src = (const uint8_t*)host_src;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  if (guide_bytes) e = cudaMemcpyAsync(guide, src + hd.guide_offset, guide_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && bs_bytes)
+    e = cudaMemcpyAsync(bs, src + hd.bs_offset, bs_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(gs, src + hd.gs_offset, sizeof(float) * hd.n_seg, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   return TRACE_OK;
 }

@@ -15,7 +15,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -65,10 +65,26 @@ SIGNATURES = {
     "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
                                     P, P, P]),
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
+    "trace_record_size": (ctypes.c_size_t, [INT, I64, I64, ctypes.c_int32]),
+    "trace_record_export": (INT, [P, INT, P, P, P, I64, I64, Segments, P, ctypes.c_size_t, P]),
+    "trace_record_info": (INT, [P, ctypes.c_size_t, P]),
+    "trace_record_import": (INT, [P, P, ctypes.c_size_t, P, P, P, P]),
     "trace_rollout_quant_noalloc": (INT, [P, I64, I64, Segments, P, P, P, P, P]),
     "trace_profile_enable": (INT, [P, INT]),
     "trace_profile_collect": (INT, [P, ctypes.POINTER(KernelTime)]),
 }
+
+
+RECORD_MAGIC = 0x31475254
+
+
+class RecordHeader(ctypes.Structure):
+    """trace_record_header_t: the 64-byte header of a guide record."""
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32),
+                ("kind", ctypes.c_uint32), ("n_seg", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("guide_offset", ctypes.c_uint64), ("bs_offset", ctypes.c_uint64),
+                ("gs_offset", ctypes.c_uint64), ("seg_offset", ctypes.c_uint64)]
 
 
 def library_path() -> str:
@@ -260,6 +276,54 @@ class Handle:
         self._check("trace_ste_backward", st)
         return out
 
+    # -- guide transport ---------------------------------------------------------
+    def record_export(self, guide: torch.Tensor, bs: torch.Tensor, gs: torch.Tensor, seg=None,
+                      out: Optional[torch.Tensor] = None, wait: bool = True) -> torch.Tensor:
+        """Copies a rollout record (guide, block scales, global scales and the
+        segment table) into one pinned host buffer.  The guide's dtype names
+        the kind: uint8 [rows, cols/2] full codes, int32 [rows, cols/16]
+        compact words.  With wait=False the device-to-host copies are still
+        in flight on the current stream when this returns."""
+        rows = guide.shape[0]
+        if guide.dtype == torch.uint8:
+            k, cols = GUIDE_FULL, guide.shape[1] * 2
+        elif guide.dtype == torch.int32:
+            k, cols = GUIDE_COMPACT, guide.shape[1] * 16
+        else:
+            raise ValueError("guide must be uint8 (full) or int32 (compact)")
+        n_seg = 1 if seg is None else len(seg) - 1
+        _need(guide, guide.dtype, tuple(guide.shape), "guide", self.device)
+        _need(bs, torch.uint8, (rows, cols // 16), "bs", self.device)
+        _need(gs, torch.float32, (n_seg,), "gs", self.device)
+        size = record_size(k, rows, cols, n_seg)
+        if out is None:
+            out = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+        p, n = _host_ptr(out)
+        keep = []
+        st = lib().trace_record_export(self._h, k, _ptr(guide), _ptr(bs), _ptr(gs), rows, cols,
+                                       _segments(seg, rows, keep), p, n, _stream())
+        self._check("trace_record_export", st)
+        if wait:
+            torch.cuda.current_stream(self.device).synchronize()
+        return out
+
+    def record_import(self, buf, out=None):
+        """-> (guide, bs, gs, seg_offsets) on this device from a record in host
+        memory (pinned memory makes the copies asynchronous)."""
+        hd, seg = record_info(buf)
+        rows, cols = hd.rows, hd.cols
+        if out is None:
+            gshape = (rows, cols // 2) if hd.kind == GUIDE_FULL else (rows, cols // 16)
+            gdt = torch.uint8 if hd.kind == GUIDE_FULL else torch.int32
+            out = (torch.empty(gshape, dtype=gdt, device=self.device),
+                   torch.empty((rows, cols // 16), dtype=torch.uint8, device=self.device),
+                   torch.empty((hd.n_seg,), dtype=torch.float32, device=self.device))
+        g, bs, gs = out
+        p, n = _host_ptr(buf)
+        st = lib().trace_record_import(self._h, p, n, _ptr(g), _ptr(bs), _ptr(gs), _stream())
+        self._check("trace_record_import", st)
+        return g, bs, gs, seg
+
     # -- profiler ---------------------------------------------------------------
     def profile(self, enable: bool = True):
         self._check("trace_profile_enable", lib().trace_profile_enable(self._h, int(enable)))
@@ -281,9 +345,61 @@ def stats_dict(stats: torch.Tensor) -> dict:
             "hist_rtn": [int(a) for a in v[3:7]], "hist_guided": [int(a) for a in v[7:11]]}
 
 
+def record_size(kind, rows: int, cols: int, n_seg: int = 1) -> int:
+    """Bytes of a guide record of this shape (host-only call)."""
+    k = _KINDS[kind] if isinstance(kind, str) else int(kind)
+    n = lib().trace_record_size(k, rows, cols, n_seg)
+    if n == 0:
+        raise TraceError("trace_record_size", 1)
+    return int(n)
+
+
+def _host_ptr(buf) -> Tuple[ctypes.c_void_p, int]:
+    if isinstance(buf, torch.Tensor):
+        if buf.device.type != "cpu" or buf.dtype != torch.uint8 or not buf.is_contiguous():
+            raise ValueError("a record is a contiguous uint8 CPU tensor")
+        return ctypes.c_void_p(buf.data_ptr()), buf.numel()
+    arr = np.ascontiguousarray(buf, dtype=np.uint8)
+    return ctypes.c_void_p(arr.ctypes.data), arr.size
+
+
+def record_info(buf) -> Tuple[RecordHeader, np.ndarray]:
+    """Validates a record and returns its header and row offsets (host-only)."""
+    keep = buf if isinstance(buf, torch.Tensor) else np.ascontiguousarray(buf, dtype=np.uint8)
+    p, n = _host_ptr(keep)
+    hd = RecordHeader()
+    st = lib().trace_record_info(p, n, ctypes.byref(hd))
+    if st != 0:
+        raise TraceError("trace_record_info", st)
+    raw = keep.numpy() if isinstance(keep, torch.Tensor) else keep
+    seg = raw[hd.seg_offset:hd.seg_offset + 8 * (hd.n_seg + 1)].view(np.int64).copy()
+    return hd, seg
+
+
+def save_record(buf, path: str) -> None:
+    """Writes a record to disk as is (its bytes are the on-disk format)."""
+    raw = buf.numpy() if isinstance(buf, torch.Tensor) else np.asarray(buf, dtype=np.uint8)
+    with open(path, "wb") as f:
+        f.write(memoryview(raw))
+
+
+def load_record(path: str, pin: bool = True) -> torch.Tensor:
+    """Reads a record file into a (pinned) uint8 host tensor and validates it."""
+    size = os.path.getsize(path)
+    buf = torch.empty(size, dtype=torch.uint8, pin_memory=pin)
+    with open(path, "rb") as f:
+        got = f.readinto(memoryview(buf.numpy()))
+    if got != size:
+        raise TraceError("load_record: short read", 1)
+    record_info(buf)
+    return buf
+
+
 __all__: Sequence[str] = ["Handle", "TraceError", "lib", "library_path", "new_stats",
                           "stats_dict", "GUIDE_NONE", "GUIDE_FULL", "GUIDE_COMPACT",
-                          "KERNELS", "SIGNATURES", "MAX_SEGMENTS"]
+                          "KERNELS", "SIGNATURES", "MAX_SEGMENTS", "RecordHeader",
+                          "record_size", "record_info", "save_record", "load_record",
+                          "guided_fake_quant", "GuidedFakeQuant"]
 
 
 class GuidedFakeQuant(torch.autograd.Function):

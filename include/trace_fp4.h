@@ -221,6 +221,50 @@ TRACE_API trace_status_t trace_ste_backward(trace_handle_t h, const void* grad_o
                                             int64_t cols, void* grad_in_bf16,
                                             trace_stream_t stream);
 
+/* Guide transport ([EN] "TRACE Core Concept", second design: rollout
+ * records travel GPU -> CPU -> CPU cache -> disk -> back to the GPU, which is
+ * why the compact record exists).  A record is one byte buffer: a 64-byte
+ * header, then 256-byte-aligned sections: the guide (full codes
+ * [rows, cols/2] or compact words [rows, cols/16]), the block scales
+ * [rows, cols/16], the global scales [n_seg] and the row offsets
+ * [n_seg + 1] (int64).  The buffer can be written to disk as is. */
+#define TRACE_RECORD_MAGIC 0x31475254u /* "TRG1" little-endian */
+typedef struct {
+  uint32_t magic;      /* TRACE_RECORD_MAGIC                              */
+  uint32_t version;    /* 1                                               */
+  uint32_t kind;       /* TRACE_GUIDE_FULL or TRACE_GUIDE_COMPACT          */
+  int32_t n_seg;
+  int64_t rows, cols;
+  uint64_t guide_offset, bs_offset, gs_offset, seg_offset; /* from the start */
+} trace_record_header_t;
+
+/* Bytes of a record for this shape (0 for bad arguments). */
+TRACE_API size_t trace_record_size(trace_guide_kind_t kind, int64_t rows, int64_t cols,
+                                   int32_t n_seg);
+
+/* Writes the header and the row offsets into host_dst at once and enqueues
+ * device -> host copies of the guide, block scales and global scales on
+ * `stream` (pinned host memory makes them asynchronous).  host_dst must hold
+ * trace_record_size(...) bytes and stay valid until the stream passes the
+ * copies.  seg.row_offsets == NULL means one segment. */
+TRACE_API trace_status_t trace_record_export(trace_handle_t h, trace_guide_kind_t kind,
+                                             const void* guide, const void* bs,
+                                             const float* gs, int64_t rows, int64_t cols,
+                                             trace_segments_t seg, void* host_dst,
+                                             size_t dst_bytes, trace_stream_t stream);
+
+/* Validates a record's header (magic, version, kind, sizes against
+ * src_bytes) and copies it out; returns TRACE_ERR_INVALID_ARG for a damaged
+ * or truncated record.  The row offsets are at host_src + header.seg_offset. */
+TRACE_API trace_status_t trace_record_info(const void* host_src, size_t src_bytes,
+                                           trace_record_header_t* out);
+
+/* Enqueues host -> device copies of a validated record's guide, block scales
+ * and global scales into caller-owned device buffers of the record's shape. */
+TRACE_API trace_status_t trace_record_import(trace_handle_t h, const void* host_src,
+                                             size_t src_bytes, void* guide, void* bs,
+                                             float* gs, trace_stream_t stream);
+
 /* Rollout-side quantisation without a handle and without any device
  * allocation.  The paper has no counterpart: this is a deployment variant of
  * trace_rollout_quant with the same arguments, layouts and results.

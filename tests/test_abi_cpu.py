@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -81,3 +82,71 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(trace, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(trace.TraceError):
         trace.lib()
+
+
+def _hand_record(kind, rows, cols, seg):
+    """A guide record built here from its documented layout (64-byte header,
+    256-byte-aligned sections: guide, block scales, global scales, offsets)."""
+    a = lambda v: (v + 255) // 256 * 256
+    n_seg = len(seg) - 1
+    gbytes = rows * cols // 2 if kind == 1 else rows * (cols // 16) * 4
+    goff = 256
+    boff = a(goff + gbytes)
+    soff = a(boff + rows * cols // 16)
+    ooff = a(soff + 4 * n_seg)
+    buf = np.zeros(ooff + 8 * (n_seg + 1), dtype=np.uint8)
+    hdr = np.array([0x31475254, 1, kind, n_seg], dtype=np.uint32).view(np.uint8)
+    buf[:16] = hdr
+    buf[16:32] = np.array([rows, cols], dtype=np.int64).view(np.uint8)
+    buf[32:64] = np.array([goff, boff, soff, ooff], dtype=np.uint64).view(np.uint8)
+    buf[ooff:] = np.asarray(seg, dtype=np.int64).view(np.uint8)
+    return buf
+
+
+@pytest.mark.parametrize("kind,rows,cols,seg", [(1, 5, 64, [0, 2, 5]), (2, 7, 32, [0, 7]),
+                                                (2, 0, 128, [0, 0]), (1, 33, 96, [0, 1, 1, 33])])
+def test_record_layout_and_validation(lib, kind, rows, cols, seg):
+    from fp4_rollout_guided_gb300 import trace
+    buf = _hand_record(kind, rows, cols, seg)
+    assert trace.record_size(kind, rows, cols, len(seg) - 1) == buf.size
+    hd, offs = trace.record_info(buf)
+    assert (hd.kind, hd.rows, hd.cols, hd.n_seg) == (kind, rows, cols, len(seg) - 1)
+    assert offs.tolist() == seg
+    # damaged records are rejected: truncated, bad magic, bad kind, moved
+    # section, non-monotone or wrong-total segment table
+    with pytest.raises(trace.TraceError):
+        trace.record_info(buf[:-1])
+    for byte, flip in ((0, 0x55), (4, 0x02), (8, 0x04), (40, 0x10), (56, 0x08)):
+        bad = buf.copy()
+        bad[byte] ^= flip
+        with pytest.raises(trace.TraceError):
+            trace.record_info(bad)
+    if len(seg) > 2:
+        bad = buf.copy()
+        o = bad[hd.seg_offset:].view(np.int64)
+        o[1] = rows + 1
+        with pytest.raises(trace.TraceError):
+            trace.record_info(bad)
+    bad = buf.copy()
+    bad[hd.seg_offset + 8 * (len(seg) - 1):].view(np.int64)[0] = rows + 1
+    with pytest.raises(trace.TraceError):
+        trace.record_info(bad)
+
+
+def test_record_size_rejects_bad_shapes(lib):
+    assert lib.trace_record_size(0, 4, 32, 1) == 0          # no guide kind
+    assert lib.trace_record_size(1, 4, 48, 1) == 0          # cols % 32
+    assert lib.trace_record_size(2, 4, 32, 0) == 0          # no segments
+    assert lib.trace_record_size(2, 4, 32, 4001) == 0
+    # sizes: header page + 256-aligned sections (compact 4 B per 16 elements)
+    assert lib.trace_record_size(2, 16, 32, 1) == 256 + 256 + 256 + 256 + 16
+
+
+def test_record_calls_without_handle(lib):
+    from fp4_rollout_guided_gb300.trace import Segments
+    p = ctypes.c_void_p(256)
+    buf = ctypes.create_string_buffer(4096)
+    assert lib.trace_record_export(None, 2, p, p, p, 1, 32, Segments(None, 1), buf, 4096,
+                                   None) == 1
+    assert lib.trace_record_import(None, buf, 4096, p, p, p, None) == 1
+    assert lib.trace_record_info(buf, 4096, None) == 1

@@ -333,3 +333,59 @@ def test_autograd_guided_fake_quant(h):
     assert_same("autograd y", u16(y.detach()), o_y)
     ones = np.full(u16(x).shape, 0x3F80, np.uint16)          # bf16 1.0
     assert_same("autograd grad", u16(xr.grad), oracle.ste_backward(ones, o_m))
+
+
+# ---------------------------------------------------------------------------
+# guide transport: device -> pinned host record -> disk -> host -> device
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["full", "compact"])
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_record_round_trip(h, tmp_path, kind, cfg):
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(cfg, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    xg, rg = x.to(DEV), r.to(DEV)
+    codes, bs, gs, guide = h.rollout_quant(rg, w.seg_r)
+    g = codes if kind == "full" else guide
+    rec = h.record_export(g, bs, gs, w.seg_r)
+    assert rec.is_pinned() and rec.numel() == trace.record_size(kind, w.rows, w.cols, w.n_seg_r)
+    path = str(tmp_path / f"guide_{kind}.trg")
+    trace.save_record(rec, path)
+    back = trace.load_record(path)
+    g2, bs2, gs2, seg2 = h.record_import(back)
+    torch.cuda.synchronize()
+    assert seg2.tolist() == [int(v) for v in w.seg_r]
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(u16(r), w.seg_r)
+    want = o_codes if kind == "full" else o_guide
+    got = g2.cpu().numpy() if kind == "full" else u32(g2)
+    assert_same(f"record {kind} guide", got, want)
+    assert_same(f"record {kind} bs", bs2.cpu().numpy(), o_bs)
+    assert_same(f"record {kind} gs", gs2.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    # the imported record drives the training side to the oracle's result
+    y, m, _, _ = h.train_fakequant(xg, w.seg_t, kind, g2, bs2, gs2, seg2)
+    kk = oracle.GUIDE_FULL if kind == "full" else oracle.GUIDE_COMPACT
+    o_y, o_m, _, _ = oracle.train_fakequant(u16(x), w.seg_t, kk, want, o_bs, o_gs, w.seg_r)
+    assert_same(f"record {kind} y", u16(y), o_y)
+    assert_same(f"record {kind} mask", u32(m), o_m)
+
+
+def test_record_async_export_and_sizes(h):
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(3, small=True)
+    _, r = synth.make_inputs(w, "cpu")
+    codes, bs, gs, guide = h.rollout_quant(r.to(DEV), w.seg_r)
+    full = h.record_export(codes, bs, gs, w.seg_r, wait=False)
+    comp = h.record_export(guide, bs, gs, w.seg_r, wait=False)
+    torch.cuda.current_stream().synchronize()
+    hf, _ = trace.record_info(full)
+    hc, _ = trace.record_info(comp)
+    # guide sections: 4 bits per element (full) and 2 bits (compact), each
+    # padded to 256 bytes
+    pad = lambda v: (v + 255) // 256 * 256
+    assert hf.bs_offset - hf.guide_offset == pad(w.rows * w.cols // 2)
+    assert hc.bs_offset - hc.guide_offset == pad(w.rows * w.cols // 4)
+    # a record that is too small is refused before any copy is queued
+    small = torch.empty(full.numel() - 1, dtype=torch.uint8, pin_memory=True)
+    with pytest.raises(trace.TraceError):
+        h.record_export(codes, bs, gs, w.seg_r, out=small)
