@@ -41,11 +41,20 @@ import torch  # noqa: E402
 
 METRIC = "guided NVFP4 fake-quant GB/s (bytes in+out) and % of GB300 HBM peak"
 # algorithmic bytes per element of each kernel (reads + writes)
-KERNEL_BYTES = {"amax": 2.0, "rollout_quant": 2.8125, "guide_pack": 0.75,
-                "guide_unpack": 2.8125, "fakequant_compact": 4.4375, "fakequant_full": 4.6875}
+# (the fused rollout kernel moves x once through HBM: its quantisation pass
+# re-reads x from L2)
+KERNEL_BYTES = {"amax": 2.0, "rollout_quant": 2.8125, "rollout_fused": 2.8125,
+                "guide_pack": 0.75, "guide_unpack": 2.8125, "fakequant_compact": 4.4375,
+                "fakequant_full": 4.6875, "ste_backward": 4.125}
+
+
+def kernel_bytes(name: str, guide: str) -> float:
+    return KERNEL_BYTES["fakequant_" + guide] if name == "fakequant" else KERNEL_BYTES[name]
 
 
 def step_bytes_per_elem(guide: str) -> float:
+    """The step's work in bytes per element: every row's bytes in + out (the
+    amax row counted on both sides), however the kernels are fused."""
     fq = KERNEL_BYTES["fakequant_" + guide]
     return (KERNEL_BYTES["amax"] * 2 + KERNEL_BYTES["rollout_quant"] + KERNEL_BYTES["guide_pack"]
             + KERNEL_BYTES["guide_unpack"] + fq)
@@ -276,6 +285,8 @@ def run_ours(args, w0):
     w = synth.workload(w0.cfg, seed=plan.seed)
     elems = w.elems
     h = trace.Handle(local)
+    if args.no_fuse:
+        h.set_option("fused_amax", 0)
 
     t_gen = time.perf_counter()
     x, r = synth.make_inputs(w, dev)
@@ -331,15 +342,19 @@ def run_ours(args, w0):
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
 
+    waits = h.device_status()           # 0, or 6 if an in-kernel wait ran out
+    if waits != 0:
+        raise SystemExit("an in-kernel wait ran out during the timed steps")
     launches = sum(n for n, _ in times.values())
     bpe = step_bytes_per_elem(kind)
     value = bpe * elems * world / (ms * 1e-3) / 1e9
+    fused = times.get("rollout_fused", (0, 0.0))[0] > 0
     peak, peak_src = load_peaks()
     kernels = {}
     for name, (n, tot) in times.items():
         if n == 0:
             continue
-        b = KERNEL_BYTES["fakequant_" + kind] if name == "fakequant" else KERNEL_BYTES[name]
+        b = kernel_bytes(name, kind)
         avg = tot / n
         gbs = b * elems / (avg * 1e-3) / 1e9
         kernels[name] = {"launches": n, "avg_ms": round(avg, 4), "bytes_per_elem": b,
@@ -366,8 +381,9 @@ def run_ours(args, w0):
             "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "elements_per_gpu": elems,
                        "segments_train": w.n_seg_t, "segments_rollout": w.n_seg_r,
-                       "guide": kind, "step": "amax+rollout_quant, guide_pack, guide_unpack, "
-                                              "amax+guided_fakequant",
+                       "guide": kind,
+                       "step": ("rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
+                       + ", guide_pack, guide_unpack, amax+guided_fakequant",
                        "step_bytes_per_elem": bpe,
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replica-per-gpu x{world}"},
@@ -551,6 +567,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fuse", action="store_true",
+                    help="rollout side as two kernels (amax, then quantiser)")
     ap.add_argument("--transport", action="store_true",
                     help="time the guide record's device/host/disk round trip instead")
     args = ap.parse_args()

@@ -35,6 +35,10 @@ struct trace_ctx {
   cudaEvent_t order = nullptr;  // orders calls on the handle's scratch
   int last_error = 0;
   bool profiling = false;
+  bool fused_amax = true;
+  int64_t wave_bytes = int64_t(32) << 20;
+  uint64_t wait_ns = 1000000000ull;
+  uint32_t wait_extra = 0;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare;  // recycled timing events
 };
@@ -176,9 +180,10 @@ trace_status_t trace_create(trace_handle_t* out, int device) {
   h->device = device;
   h->sm_count = prop.multiProcessorCount;
   DeviceGuard g(device);
-  // one allocation: amax words, ticket (padded to 256 B), training scales
+  // one allocation: amax words, ticket (padded to 256 B), training scales,
+  // wave counters, error word (padded to 256 B)
   const size_t seg_bytes = sizeof(uint32_t) * TRACE_MAX_SEGMENTS;
-  const size_t bytes = seg_bytes + 256 + seg_bytes;
+  const size_t bytes = seg_bytes + 256 + seg_bytes + seg_bytes + 256;
   char* base = nullptr;
   if (cudaMalloc(&base, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -195,6 +200,8 @@ trace_status_t trace_create(trace_handle_t* out, int device) {
   h->scratch.amax_bits = (uint32_t*)base;
   h->scratch.done = (uint32_t*)(base + seg_bytes);
   h->scratch.gs_train = (float*)(base + seg_bytes + 256);
+  h->scratch.wave_cnt = (uint32_t*)(base + 2 * seg_bytes + 256);
+  h->scratch.err = (uint32_t*)(base + 3 * seg_bytes + 256);
   *out = h;
   return TRACE_OK;
 }
@@ -212,6 +219,43 @@ trace_status_t trace_destroy(trace_handle_t h) {
   cudaGetLastError();
   delete h;
   return TRACE_OK;
+}
+
+trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t value) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  switch (opt) {
+    case TRACE_OPT_FUSED_AMAX:
+      if (value != 0 && value != 1) return TRACE_ERR_INVALID_ARG;
+      h->fused_amax = value != 0;
+      return TRACE_OK;
+    case TRACE_OPT_WAVE_BYTES:
+      if (value < 4096 || value > (int64_t(40) << 20)) return TRACE_ERR_INVALID_ARG;
+      h->wave_bytes = value;
+      return TRACE_OK;
+    case TRACE_OPT_WAIT_LIMIT_NS:
+      if (value < 1000000 || value > 10000000000ll) return TRACE_ERR_INVALID_ARG;
+      h->wait_ns = (uint64_t)value;
+      return TRACE_OK;
+    case TRACE_OPT_WAIT_EXTRA:
+      if (value != 0 && value != 1) return TRACE_ERR_INVALID_ARG;
+      h->wait_extra = (uint32_t)value;
+      return TRACE_OK;
+  }
+  return TRACE_ERR_INVALID_ARG;
+}
+
+trace_status_t trace_device_status(trace_handle_t h, trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word = 0;
+  cudaError_t e = cudaStreamWaitEvent(st, h->order, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&word, h->scratch.err, sizeof(word),
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->scratch.err, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return word ? TRACE_ERR_TIMEOUT : TRACE_OK;
 }
 
 trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
@@ -239,6 +283,22 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
   if (nchunks == 0) {
     e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
   } else {
+    static thread_local tfp4::WaveParam wv;
+    bool fused = h->fused_amax && tfp4::plan_waves(sp, (int32_t)cols, h->wave_bytes, &wv);
+    if (fused) {
+      e = timed(h, TRACE_KERNEL_ROLLOUT_FUSED, st, [&] {
+        return tfp4::launch_rollout_fused(x_bf16, nchunks, cpr, sp, wv, h->scratch, gs_f32,
+                                          codes_u8, bs_e4m3, guide_bits, h->sm_count,
+                                          h->wait_extra, h->wait_ns, st);
+      });
+      // a device that cannot hold the whole grid at once takes the two-kernel path
+      if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        fused = false;
+        e = cudaSuccess;
+      }
+    }
+    if (!fused) {
     e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
       return tfp4::launch_amax(x_bf16, nchunks, cpr, sp, h->scratch, gs_f32, h->sm_count, st);
     });
@@ -247,6 +307,7 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
         return tfp4::launch_rollout_quant(x_bf16, nchunks, cpr, sp, gs_f32, codes_u8, bs_e4m3,
                                           guide_bits, h->sm_count, st);
       });
+    }
   }
   const cudaError_t e2 = end_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);

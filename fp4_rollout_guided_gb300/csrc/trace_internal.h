@@ -17,6 +17,14 @@ struct SegParam {
   int32_t off[TRACE_MAX_SEGMENTS + 1];
 };
 
+// Waves of the fused amax + quantisation kernel: wave w holds the whole
+// segments [seg0[w], seg0[w+1]); seg0[n] is the segment count.
+struct WaveParam {
+  int32_t n;
+  uint16_t seg0[TRACE_MAX_SEGMENTS + 1];
+};
+static_assert(TRACE_MAX_SEGMENTS < 65536, "wave table holds 16-bit segment indices");
+
 // Unsigned division by a runtime constant (chunk index -> row) without a
 // hardware divide: q = (mulhi(n, mul) + n) >> shift with shift = ceil(log2 d)
 // and mul = floor(2^32 * (2^shift - d) / d) + 1, exact for every 32-bit n.
@@ -46,6 +54,8 @@ struct Scratch {
   uint32_t* amax_bits;  // [TRACE_MAX_SEGMENTS]
   uint32_t* done;       // completion ticket of the amax kernel
   float* gs_train;      // [TRACE_MAX_SEGMENTS] training-side global scales
+  uint32_t* wave_cnt;   // [TRACE_MAX_SEGMENTS] fused kernel: CTAs done with a wave's amax
+  uint32_t* err;        // fused kernel: nonzero once an in-kernel wait ran out
 };
 
 // a1: per-segment amax of x, then gs[s] = amax/2688 written to gs_out.
@@ -56,6 +66,15 @@ cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegPa
 cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
                                  uint32_t* guide, int sm_count, cudaStream_t st);
+
+// a1 + a2 in one cooperative launch (see k_rollout_fused).  plan_waves
+// groups whole segments into waves of about wave_bytes of x; it returns
+// false when a segment is too large to stay in L2 between the two phases.
+bool plan_waves(const SegParam& seg, int32_t cols, int64_t wave_bytes, WaveParam* wv);
+cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
+                                 const WaveParam& wv, const Scratch& s, float* gs_out,
+                                 void* codes, void* bs, uint32_t* guide, int sm_count,
+                                 uint32_t wait_extra, uint64_t wait_ns, cudaStream_t st);
 
 // a3: codes -> compact words.
 cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,

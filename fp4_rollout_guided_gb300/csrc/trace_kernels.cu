@@ -38,6 +38,7 @@ namespace tfp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWaveSegs = 256;  // segments per wave of the fused rollout kernel
 constexpr uint32_t kAbs2 = 0x7FFF7FFFu;
 
 // ---------------------------------------------------------------------------
@@ -472,6 +473,36 @@ __device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
 // a2: rollout quantisation
 // ---------------------------------------------------------------------------
 
+// One chunk (two blocks) -> 16 code bytes, two block-scale codes and two
+// compact words, given the segment's global scale g.
+__device__ __forceinline__ void quant_chunk(const Chunk& cur, float g, uint32_t c,
+                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ bs,
+                                            uint8_t* __restrict__ guide) {
+  uint32_t a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
+  const PairScale ps = pair_scale(block_amax8(a), block_amax8(a + 8), g);
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float inv = ps.inv[q >> 1];
+    uint32_t word = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = cur.w[4 * q + k];
+      // signed x * inv keeps the input's sign in the nibble
+      const uint32_t b = e2m1x2(__fmul_rn(__uint_as_float(w << 16), inv),
+                                __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv));
+      word |= b << (8 * k);
+    }
+    out[q] = word;
+  }
+  st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
+  st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
+  if (guide)
+    st_stream2(guide + (uint64_t)c * 8u, compact_word(out[0], out[1]), compact_word(out[2], out[3]));
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_rollout_quant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
                     uint32_t steps_per_cta, const __grid_constant__ SegParam seg,
@@ -499,33 +530,519 @@ __global__ void __launch_bounds__(kThreads)
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
     if (c < nchunks) {
       const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
-      const float g = gs[s];
-      uint32_t a[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-      const PairScale ps = pair_scale(block_amax8(a), block_amax8(a + 8), g);
-      uint32_t out[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float inv = ps.inv[q >> 1];
-        uint32_t word = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t w = cur.w[4 * q + k];
-          // signed x * inv keeps the input's sign in the nibble
-          const uint32_t b = e2m1x2(__fmul_rn(__uint_as_float(w << 16), inv),
-                                    __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv));
-          word |= b << (8 * k);
-        }
-        out[q] = word;
-      }
-      st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
-      st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
-      if (guide)
-        st_stream2(guide + (uint64_t)c * 8u, compact_word(out[0], out[1]),
-                   compact_word(out[2], out[3]));
+      quant_chunk(cur, gs[s], c, codes, bs, guide);
     }
     cur = nxt;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a1 + a2 fused: segment amax and quantisation in one cooperative launch
+// ---------------------------------------------------------------------------
+//
+// The segments are grouped into waves of whole segments small enough to stay
+// in L2 (host-planned, WaveParam, at most kWaveSegs segments each).  The
+// 256-chunk steps of the call are dealt round-robin to the CTAs, one CTA
+// per SM.  In each CTA one producer thread stages steps into shared memory
+// with TMA bulk copies (cp.async.bulk, completion on mbarriers) on two
+// rings (a second thread watches the cross-CTA wave counters for it):
+//   - the amax ring streams this CTA's steps from HBM; four amax warps fold
+//     per-segment maxima into shared memory and, at the end of each wave,
+//     into amax_bits, then count the CTA done with that wave (wave_cnt);
+//   - the quantiser ring re-reads the same steps of an earlier wave, from
+//     L2, once every CTA has counted that wave; eight quantiser warps turn
+//     each staged chunk into codes, block scales and compact words with
+//     gs = amax/2688.
+// The amax stream leads the quantiser by a bounded number of steps, which
+// bounds what L2 must hold, and otherwise never waits, so HBM streaming and
+// quantisation overlap.
+//
+// The launch is cooperative (all CTAs co-resident).  Every wait is bounded:
+// the producer gives up the cross-CTA waits once nothing has moved for the
+// time limit (setting *err, the outputs are then undefined), every mbarrier
+// wait has the same limit, and the producer waits for its own copies in
+// flight before the CTA exits.
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_l2(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// One thread: true once *p >= target; false after limit_ns (or a fixed
+// number of polls, whichever comes first).
+__device__ __noinline__ bool wait_at_least(const uint32_t* p, uint32_t target, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (ld_acquire(p) >= target) return true;
+    __nanosleep(32);
+    if ((it & 31u) == 31u && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+// First step of wave-local steps [0, nst) that CTA b owns when steps are
+// dealt round-robin over the whole call, the wave's first step being global
+// step `base`.
+__device__ __forceinline__ uint32_t first_owned(uint32_t base, uint32_t b, uint32_t G) {
+  const uint32_t r = base % G;
+  return b >= r ? b - r : b + G - r;
+}
+
+// ---- TMA bulk copies and mbarriers -------------------------------------------
+
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a phase; false (and *err set) once limit_ns has passed.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                       uint32_t* err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 15u) == 15u && global_ns() - t0 > limit_ns) break;
+  }
+  atomicOr(err, 2u);
+  return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// bytes (a multiple of 16) from global src to shared dst, completing on bar
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Chunk i of a staged step (64 B at 64 i).
+__device__ __forceinline__ void smem_chunk(Chunk& c, const uint8_t* step, uint32_t i) {
+  const uint4* p = reinterpret_cast<const uint4*>(step + 64u * i);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = p[q];
+    c.w[4 * q + 0] = v.x;
+    c.w[4 * q + 1] = v.y;
+    c.w[4 * q + 2] = v.z;
+    c.w[4 * q + 3] = v.w;
+  }
+}
+
+// Packed |bf16| maximum of a 16-byte word (eight elements).
+__device__ __forceinline__ uint32_t quad_max2(uint4 v) {
+  return max_u16x2(max_u16x2(v.x & kAbs2, v.y & kAbs2), max_u16x2(v.z & kAbs2, v.w & kAbs2));
+}
+
+__device__ __forceinline__ uint32_t max2_bits(uint32_t m) {
+  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+  return (hi > lo ? hi : lo) << 16;
+}
+
+// Step cursor over the waves: the k-th owned step of wave w, dealt
+// round-robin over the whole call (global step base + k goes to CTA
+// (base + k) mod G).
+struct WaveCursor {
+  int w;
+  uint32_t base, k, nst, c0, c1;
+  __device__ __forceinline__ void enter(const SegParam& seg, const WaveParam& wv, uint32_t cpr_u,
+                                        uint32_t b, uint32_t G) {
+    // skip waves in which this CTA owns no step
+    while (w < wv.n) {
+      c0 = (uint32_t)seg.off[wv.seg0[w]] * cpr_u;
+      c1 = (uint32_t)seg.off[wv.seg0[w + 1]] * cpr_u;
+      nst = (c1 - c0 + kThreads - 1) / kThreads;
+      k = first_owned(base, b, G);
+      if (k < nst) return;
+      base += nst;
+      ++w;
+    }
+  }
+  // advances to the next owned step; returns the wave it left when a wave ends
+  __device__ __forceinline__ void next(const SegParam& seg, const WaveParam& wv, uint32_t cpr_u,
+                                       uint32_t b, uint32_t G) {
+    k += G;
+    if (k >= nst) {
+      base += nst;
+      ++w;
+      enter(seg, wv, cpr_u, b, G);
+    }
+  }
+  __device__ __forceinline__ uint32_t step_chunk() const { return c0 + k * kThreads; }
+  __device__ __forceinline__ uint32_t step_chunks() const {
+    return min((uint32_t)kThreads, c1 - step_chunk());
+  }
+};
+
+#ifndef TFP4_FUSED_SLOTS_A
+#define TFP4_FUSED_SLOTS_A 6
+#endif
+#ifndef TFP4_FUSED_SLOTS_Q
+#define TFP4_FUSED_SLOTS_Q 6
+#endif
+#ifndef TFP4_FUSED_AMAX_WARPS
+#define TFP4_FUSED_AMAX_WARPS 4
+#endif
+#ifndef TFP4_FUSED_QUANT_GROUPS
+#define TFP4_FUSED_QUANT_GROUPS 2
+#endif
+constexpr int kSlotsA = TFP4_FUSED_SLOTS_A;  // staged steps of the amax stream
+constexpr int kSlotsQ = TFP4_FUSED_SLOTS_Q;  // staged steps of the quantiser
+constexpr int kStepBytes = kThreads * 64;    // 256 chunks
+constexpr int kAmaxWarps = TFP4_FUSED_AMAX_WARPS;
+// Quantiser warps come in groups of eight (one chunk per thread of a step);
+// group g takes the staged steps n with n mod kQuantGroups == g.
+constexpr int kQuantGroups = TFP4_FUSED_QUANT_GROUPS, kQuantWarps = 8;
+// warp 0: copies; warp 1: watches the wave counters; then the amax warps
+// and the quantiser groups
+constexpr int kFirstAmaxWarp = 2;
+constexpr int kFusedThreads = 32 * (kFirstAmaxWarp + kAmaxWarps + kQuantGroups * kQuantWarps);
+static_assert(kSlotsQ % kQuantGroups == 0, "each quantiser group owns whole slots");
+// The amax stream may always run through the wave the quantiser waits for;
+// beyond it, it leads the quantiser by at most kLeadSteps staged steps (a
+// bound on what L2 must hold: kLeadSteps x 16 KB per CTA).
+#ifndef TFP4_FUSED_LEAD_STEPS
+#define TFP4_FUSED_LEAD_STEPS 24
+#endif
+constexpr uint32_t kLeadSteps = TFP4_FUSED_LEAD_STEPS;
+
+// Barrier of the amax warps only (id 1; 0 is __syncthreads).
+__device__ __forceinline__ void amax_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kAmaxWarps) : "memory");
+}
+
+struct FusedSmem {
+  alignas(128) uint8_t a[kSlotsA][kStepBytes];
+  alignas(128) uint8_t q[kSlotsQ][kStepBytes];
+  uint64_t full_a[kSlotsA], empty_a[kSlotsA], full_q[kSlotsQ], empty_q[kSlotsQ];
+  uint32_t smax[kWaveSegs];
+};
+constexpr size_t kFusedSmemBytes = sizeof(FusedSmem) + 128;
+
+#ifndef TFP4_FUSED_EVICT_FIRST
+#define TFP4_FUSED_EVICT_FIRST 1
+#endif
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    k_rollout_fused(const uint8_t* __restrict__ x, uint32_t cpr_u, FastDivU cpr,
+                    const __grid_constant__ SegParam seg, const __grid_constant__ WaveParam wv,
+                    float* __restrict__ gs_out, uint8_t* __restrict__ codes,
+                    uint8_t* __restrict__ bs, uint8_t* __restrict__ guide,
+                    uint32_t* __restrict__ amax_bits, uint32_t* __restrict__ wave_cnt,
+                    uint32_t* __restrict__ done, uint32_t* __restrict__ err,
+                    uint32_t wait_extra, uint64_t wait_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  FusedSmem& sm = *reinterpret_cast<FusedSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ int is_last;
+  __shared__ int ready_w;  // highest wave whose maxima are complete in every CTA
+  const uint32_t G = gridDim.x, b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    ready_w = -1;
+    for (int i = 0; i < kSlotsA; ++i) {
+      mbar_init(&sm.full_a[i], 1);
+      mbar_init(&sm.empty_a[i], kAmaxWarps);
+    }
+    for (int i = 0; i < kSlotsQ; ++i) {
+      mbar_init(&sm.full_q[i], 1);
+      mbar_init(&sm.empty_q[i], kQuantWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = threadIdx.x; i < kWaveSegs; i += kFusedThreads) sm.smax[i] = 0u;
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---- producer: one thread issues every copy ----
+    if (lane == 0) {
+      uint64_t evict_first;
+      asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+      WaveCursor ca = {0, 0, 0, 0, 0, 0}, cq = {0, 0, 0, 0, 0, 0};
+      ca.enter(seg, wv, cpr_u, b, G);
+      cq.enter(seg, wv, cpr_u, b, G);
+      uint32_t na = 0, nq = 0;  // copies issued into each ring
+      bool broken = false;
+      uint64_t idle_since = 0;
+      while (ca.w < wv.n || cq.w < wv.n) {
+        bool progress = false;
+        // quantiser stream: wave cq.w once every CTA has counted it
+        if (cq.w < wv.n) {
+          const uint32_t slot = nq % kSlotsQ, use = nq / kSlotsQ;
+          if ((broken || ld_acquire_cta(&ready_w) >= cq.w) &&
+              (use == 0 || mbar_test(&sm.empty_q[slot], (use - 1) & 1u))) {
+            // the consumers' generic-proxy reads of the slot come before
+            // the copy's async-proxy writes
+            fence_proxy_async();
+            const uint32_t bytes = cq.step_chunks() * 64u;
+            mbar_expect_tx(&sm.full_q[slot], bytes);
+#if TFP4_FUSED_EVICT_FIRST
+            bulk_load_hint(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes,
+                           &sm.full_q[slot], evict_first);
+#else
+            bulk_load(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes, &sm.full_q[slot]);
+#endif
+            ++nq;
+            cq.next(seg, wv, cpr_u, b, G);
+            progress = true;
+          }
+        }
+        // amax stream: through the quantiser's wave, then at most
+        // kLeadSteps ahead of it
+        if (ca.w < wv.n && (ca.w <= cq.w || na - nq < kLeadSteps)) {
+          const uint32_t slot = na % kSlotsA, use = na / kSlotsA;
+          if (use == 0 || mbar_test(&sm.empty_a[slot], (use - 1) & 1u)) {
+            fence_proxy_async();
+            const uint32_t bytes = ca.step_chunks() * 64u;
+            mbar_expect_tx(&sm.full_a[slot], bytes);
+            bulk_load(sm.a[slot], x + (uint64_t)ca.step_chunk() * 64u, bytes, &sm.full_a[slot]);
+            ++na;
+            ca.next(seg, wv, cpr_u, b, G);
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle_since = 0;
+        } else {
+          const uint64_t t = global_ns();
+          if (idle_since == 0) {
+            idle_since = t;
+          } else if (t - idle_since > wait_ns) {
+            // nothing moved for the whole limit: give up the cross-CTA waits
+            if (broken) break;
+            atomicOr(err, 1u);
+            broken = true;
+            idle_since = 0;
+          }
+          __nanosleep(32);
+        }
+      }
+      // no copy may still be in flight when the CTA exits
+      for (uint32_t i = 0; i < kSlotsA && i < na; ++i) {
+        const uint32_t n = na - 1 - i, slot = n % kSlotsA;
+        mbar_wait(&sm.full_a[slot], (n / kSlotsA) & 1u, wait_ns, err);
+      }
+      for (uint32_t i = 0; i < kSlotsQ && i < nq; ++i) {
+        const uint32_t n = nq - 1 - i, slot = n % kSlotsQ;
+        mbar_wait(&sm.full_q[slot], (n / kSlotsQ) & 1u, wait_ns, err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- watcher: publishes, wave by wave, that every CTA has counted it,
+    // and writes the global scales of the waves w with w mod G == b ----
+    if (lane == 0) {
+      bool broken = false;
+      for (int w = 0; w < wv.n; ++w) {
+        if (!broken && !wait_at_least(wave_cnt + w, G + wait_extra, wait_ns)) {
+          atomicOr(err, 1u);
+          broken = true;
+        }
+        if (b == (uint32_t)w % G) {
+          for (int s = wv.seg0[w]; s < wv.seg0[w + 1]; ++s)
+            gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
+        }
+        st_release_cta(&ready_w, w);
+      }
+    }
+  } else if (warp < kFirstAmaxWarp + kAmaxWarps) {
+    // ---- amax warps: per-segment maxima of each staged step ----
+    const int t = threadIdx.x - 32 * kFirstAmaxWarp;  // 0..127
+    WaveCursor c = {0, 0, 0, 0, 0, 0};
+    c.enter(seg, wv, cpr_u, b, G);
+    StepSeg ss;
+    ss.cur = 0;
+    uint32_t n = 0;
+    bool broken = false;
+    // every CTA counts itself done with every wave; waves in which it owns
+    // no step are counted as soon as the cursor passes them
+    int counted = 0;
+    if (t == 0)
+      for (; counted < c.w; ++counted) red_release_add(wave_cnt + counted, 1u);
+    while (c.w < wv.n) {
+      const int w = c.w;
+      const int s0 = wv.seg0[w];
+      const uint32_t slot = n % kSlotsA;
+      if (!broken) broken = !mbar_wait(&sm.full_a[slot], (n / kSlotsA) & 1u, wait_ns, err);
+      const uint32_t cs = c.step_chunk(), cnt = c.step_chunks();
+      const bool uniform = ss.update(seg, cpr.div(cs), cpr.div(cs + cnt - 1));
+      // 16-byte words dealt contiguously (a warp reads 512 B: no bank
+      // conflicts); word u belongs to chunk cs + u/4
+      const uint4* st4 = reinterpret_cast<const uint4*>(sm.a[slot]);
+      const uint32_t nu = cnt * 4;
+      if (uniform) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
+          const uint32_t u = t + 32 * kAmaxWarps * j;
+          if (u < nu) m = max_u16x2(m, quad_max2(st4[u]));
+        }
+        const uint32_t mw = __reduce_max_sync(0xFFFFFFFFu, max2_bits(m));
+        if (lane == 0) {
+          mbar_arrive(&sm.empty_a[slot]);
+          if (mw) atomicMax(&sm.smax[ss.cur - s0], mw);
+        }
+      } else {
+        for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
+          const uint32_t u = t + 32 * kAmaxWarps * j;
+          if (u < nu) {
+            const uint32_t m = max2_bits(quad_max2(st4[u]));
+            if (m) atomicMax(&sm.smax[seg_advance(seg, ss.cur, cpr.div(cs + u / 4)) - s0], m);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty_a[slot]);
+      }
+      ++n;
+      c.next(seg, wv, cpr_u, b, G);
+      if (c.w != w) {
+        // wave w done here: publish its maxima, count this CTA for it and
+        // for the skipped waves before the next one
+        amax_warps_sync();
+        for (int i = t; i < wv.seg0[w + 1] - s0; i += 32 * kAmaxWarps) {
+          const uint32_t m = sm.smax[i];
+          if (m) {
+            atomicMax(amax_bits + s0 + i, m);
+            sm.smax[i] = 0u;
+          }
+        }
+        amax_warps_sync();
+        if (t == 0)
+          for (; counted < c.w; ++counted) red_release_add(wave_cnt + counted, 1u);
+      }
+    }
+  } else {
+    // ---- quantiser warps: one chunk of each staged step per thread ----
+    const int qt = threadIdx.x - 32 * (kFirstAmaxWarp + kAmaxWarps);
+    const int group = qt / (32 * kQuantWarps), t = qt % (32 * kQuantWarps);  // t: 0..255
+    WaveCursor c = {0, 0, 0, 0, 0, 0};
+    c.enter(seg, wv, cpr_u, b, G);
+    StepSeg ss;
+    ss.cur = 0;
+    uint32_t n = 0;
+    for (; n < (uint32_t)group && c.w < wv.n; ++n) c.next(seg, wv, cpr_u, b, G);
+    bool broken = false;
+    int gseg = -1;
+    float g = 0.f;
+    while (c.w < wv.n) {
+      const uint32_t slot = n % kSlotsQ;
+      if (!broken) broken = !mbar_wait(&sm.full_q[slot], (n / kSlotsQ) & 1u, wait_ns, err);
+      const uint32_t cs = c.step_chunk(), cnt = c.step_chunks();
+      const bool uniform = ss.update(seg, cpr.div(cs), cpr.div(cs + cnt - 1));
+      if ((uint32_t)t < cnt) {
+        Chunk ch;
+        smem_chunk(ch, sm.q[slot], t);
+        const uint32_t cidx = cs + t;
+        const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(cidx));
+        if (s != gseg) {
+          gseg = s;
+          g = global_scale_of(ld_acquire(amax_bits + s));
+        }
+        quant_chunk(ch, g, cidx, codes, bs, guide);
+      }
+      // release the slot only once every lane's values are in use
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty_q[slot]);
+      for (int i = 0; i < kQuantGroups && c.w < wv.n; ++i) {
+        ++n;
+        c.next(seg, wv, cpr_u, b, G);
+      }
+    }
+  }
+
+  // The last CTA to finish re-zeroes the maxima and the wave counters for
+  // the next call (every CTA has finished reading them by then).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t ticket = atomicAdd(done, 1u);
+    is_last = (ticket == G - 1);
+  }
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    for (int s = threadIdx.x; s < seg.n; s += kFusedThreads) amax_bits[s] = 0u;
+    for (int w = threadIdx.x; w < wv.n; w += kFusedThreads) wave_cnt[w] = 0u;
+    if (threadIdx.x == 0) *done = 0u;
   }
 }
 
@@ -1125,6 +1642,80 @@ cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                                FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
                                                (uint8_t*)codes, (uint8_t*)bs, (uint8_t*)guide);
   return cudaGetLastError();
+}
+
+// Largest x bytes a single segment may hold on the fused path: two waves of
+// reads plus the writes in between stay well inside the 126 MB of L2.
+constexpr int64_t kWaveMaxBytes = int64_t(40) << 20;
+
+bool plan_waves(const SegParam& seg, int32_t cols, int64_t wave_bytes, WaveParam* wv) {
+  const int64_t row_bytes = int64_t(cols) * 2;
+  wv->n = 0;
+  int s = 0;
+  while (s < seg.n) {
+    const int start = s;
+    int64_t bytes = int64_t(seg.off[s + 1] - seg.off[s]) * row_bytes;
+    if (bytes > kWaveMaxBytes) return false;
+    ++s;
+    while (s < seg.n && s - start < kWaveSegs) {
+      const int64_t b = int64_t(seg.off[s + 1] - seg.off[s]) * row_bytes;
+      if (bytes + b > wave_bytes) break;
+      bytes += b;
+      ++s;
+    }
+    wv->seg0[wv->n++] = (uint16_t)start;
+  }
+  wv->seg0[wv->n] = (uint16_t)seg.n;
+  return true;
+}
+
+cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
+                                 const WaveParam& wv, const Scratch& s, float* gs_out,
+                                 void* codes, void* bs, uint32_t* guide, int sm_count,
+                                 uint32_t wait_extra, uint64_t wait_ns, cudaStream_t st) {
+  // the shared-memory opt-in and the occupancy, once per device
+  static std::mutex mu;
+  static int occ_of[64];
+  static bool set_for[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int occ;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set_for[dev]) {
+      e = cudaFuncSetAttribute(k_rollout_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kFusedSmemBytes);
+      if (e != cudaSuccess) return e;
+      int n = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rollout_fused, kFusedThreads,
+                                                        kFusedSmemBytes);
+      if (e != cudaSuccess) return e;
+      occ_of[dev] = n;
+      set_for[dev] = true;
+    }
+    occ = occ_of[dev];
+  }
+  if (occ < 1) return cudaErrorCooperativeLaunchTooLarge;
+  int64_t g = (int64_t)sm_count * occ;
+  const int64_t nsteps = steps_of(nchunks, kThreads);
+  if (nsteps < g) g = nsteps;
+  if (g < 1) g = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)g);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = kFusedSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_rollout_fused, (const uint8_t*)x, (uint32_t)cpr,
+                            FastDivU((uint32_t)cpr), seg, wv, gs_out, (uint8_t*)codes,
+                            (uint8_t*)bs, (uint8_t*)guide, s.amax_bits, s.wave_cnt, s.done,
+                            s.err, wait_extra, wait_ns);
 }
 
 cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,

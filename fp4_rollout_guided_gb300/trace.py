@@ -24,7 +24,9 @@ from . import build as _build
 
 GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
-KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward")
+KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward",
+           "rollout_fused")
+OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3}
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
           4: "CUDA error", 5: "out of memory", 6: "timeout"}
@@ -65,6 +67,8 @@ SIGNATURES = {
     "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
                                     P, P, P]),
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
+    "trace_set_option": (INT, [P, INT, I64]),
+    "trace_device_status": (INT, [P, P]),
     "trace_record_size": (ctypes.c_size_t, [INT, I64, I64, ctypes.c_int32]),
     "trace_record_export": (INT, [P, INT, P, P, P, I64, I64, Segments, P, ctypes.c_size_t, P]),
     "trace_record_info": (INT, [P, ctypes.c_size_t, P]),
@@ -324,6 +328,19 @@ class Handle:
         self._check("trace_record_import", st)
         return g, bs, gs, seg
 
+    # -- options and device status -----------------------------------------------
+    def set_option(self, name: str, value: int):
+        """fused_amax (0/1), wave_bytes, wait_limit_ns, wait_extra (test hook)."""
+        self._check("trace_set_option", lib().trace_set_option(self._h, OPTIONS[name], int(value)))
+
+    def device_status(self) -> int:
+        """Synchronises the current stream; 0, or 6 (timeout) if an in-kernel
+        wait of an earlier call ran out.  Clears the device error word."""
+        st = lib().trace_device_status(self._h, _stream())
+        if st not in (0, 6):
+            self._check("trace_device_status", st)
+        return st
+
     # -- profiler ---------------------------------------------------------------
     def profile(self, enable: bool = True):
         self._check("trace_profile_enable", lib().trace_profile_enable(self._h, int(enable)))
@@ -399,7 +416,7 @@ __all__: Sequence[str] = ["Handle", "TraceError", "lib", "library_path", "new_st
                           "stats_dict", "GUIDE_NONE", "GUIDE_FULL", "GUIDE_COMPACT",
                           "KERNELS", "SIGNATURES", "MAX_SEGMENTS", "RecordHeader",
                           "record_size", "record_info", "save_record", "load_record",
-                          "guided_fake_quant", "GuidedFakeQuant"]
+                          "guided_fake_quant", "GuidedFakeQuant", "OPTIONS"]
 
 
 class GuidedFakeQuant(torch.autograd.Function):

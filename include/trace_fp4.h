@@ -126,7 +126,8 @@ typedef enum {
   TRACE_KERNEL_GUIDE_UNPACK = 3,
   TRACE_KERNEL_FAKEQUANT = 4,
   TRACE_KERNEL_STE_BACKWARD = 5,
-  TRACE_KERNEL_COUNT = 6
+  TRACE_KERNEL_ROLLOUT_FUSED = 6, /* amax + quantisation in one launch */
+  TRACE_KERNEL_COUNT = 7
 } trace_kernel_id_t;
 
 typedef struct {
@@ -136,7 +137,8 @@ typedef struct {
 
 /* Creates a handle on `device`: checks for compute capability 10.3 and
  * allocates the device scratch (per-segment amax words, a completion ticket,
- * per-segment training global scales).  *out is NULL on failure. */
+ * per-segment training global scales, wave counters and an error word of
+ * the fused rollout kernel).  *out is NULL on failure. */
 TRACE_API trace_status_t trace_create(trace_handle_t* out, int device);
 
 /* Frees the handle.  The caller must have finished (synchronised) all work
@@ -152,6 +154,26 @@ TRACE_API int trace_last_cuda_error(trace_handle_t h);
 /* Library version as major*10000 + minor*100 + patch. */
 TRACE_API int trace_version(void);
 
+/* Per-handle options (trace_set_option returns TRACE_ERR_INVALID_ARG for an
+ * unknown option or a value out of range). */
+typedef enum {
+  TRACE_OPT_FUSED_AMAX = 0,    /* 1 (default): fuse amax into trace_rollout_quant
+                                  where segments fit; 0: always two kernels   */
+  TRACE_OPT_WAVE_BYTES = 1,    /* target bytes of x per wave of the fused kernel,
+                                  4 KiB .. 40 MiB (default 32 MiB)            */
+  TRACE_OPT_WAIT_LIMIT_NS = 2, /* limit of each in-kernel wait, 1 ms .. 10 s
+                                  (default 1 s)                               */
+  TRACE_OPT_WAIT_EXTRA = 3     /* test hook, 0 (default) or 1: each wait also
+                                  expects an arrival that never comes, so every
+                                  wait runs out at its limit                  */
+} trace_option_t;
+TRACE_API trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t value);
+
+/* Synchronises `stream`, then reports and clears the handle's device-side
+ * error word: TRACE_ERR_TIMEOUT if an in-kernel wait of an earlier call ran
+ * out, else TRACE_OK. */
+TRACE_API trace_status_t trace_device_status(trace_handle_t h, trace_stream_t stream);
+
 /* Rollout-side quantisation ([EN] "TRACE Core Concept", first and second
  * designs): per-segment amax and global scale, per-block E4M3 scale, per-
  * element RTN E2M1 code, and (if guide_bits != NULL) the compact guide words.
@@ -160,7 +182,12 @@ TRACE_API int trace_version(void);
  *   bs_e4m3    [rows, cols/16] out
  *   gs_f32     [n_seg] out (device)
  *   guide_bits [rows, cols/16] out, nullable
- * Two kernels: a streaming amax pass, then the quantiser. */
+ * When every segment holds at most 40 MiB of x (and TRACE_OPT_FUSED_AMAX is
+ * on) this is one cooperative kernel that reads x from HBM once: segments
+ * are taken in L2-sized waves, amax first, then quantisation from L2.  A
+ * wait inside it that runs out (TRACE_OPT_WAIT_LIMIT_NS) leaves the outputs
+ * undefined and is reported by trace_device_status.  Otherwise two kernels:
+ * a streaming amax pass, then the quantiser. */
 TRACE_API trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
                                    int64_t cols, trace_segments_t seg, void* codes_u8,
                                    void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,

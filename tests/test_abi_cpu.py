@@ -150,3 +150,8 @@ def test_record_calls_without_handle(lib):
                                    None) == 1
     assert lib.trace_record_import(None, buf, 4096, p, p, p, None) == 1
     assert lib.trace_record_info(buf, 4096, None) == 1
+
+
+def test_options_and_device_status_without_handle(lib):
+    assert lib.trace_set_option(None, 0, 1) == 1
+    assert lib.trace_device_status(None, None) == 1

@@ -89,7 +89,10 @@ def test_profiler_counts_launches(env):
     h.guide_pack(codes)
     t = h.collect()
     h.profile(False)
-    assert t["amax"][0] == 2 and t["rollout_quant"][0] == 1 and t["fakequant"][0] == 1
+    # rollout side: one fused launch (the whole tensor fits a wave); training
+    # side: amax + fake quant
+    assert t["rollout_fused"][0] == 1 and t["rollout_quant"][0] == 0
+    assert t["amax"][0] == 1 and t["fakequant"][0] == 1
     assert t["guide_pack"][0] == 1 and t["guide_unpack"][0] == 0
     assert all(ms >= 0 for _, ms in t.values())
     assert h.collect()["amax"][0] == 0

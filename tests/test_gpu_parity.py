@@ -389,3 +389,120 @@ def test_record_async_export_and_sizes(h):
     small = torch.empty(full.numel() - 1, dtype=torch.uint8, pin_memory=True)
     with pytest.raises(trace.TraceError):
         h.record_export(codes, bs, gs, w.seg_r, out=small)
+
+
+# ---------------------------------------------------------------------------
+# fused amax + quantisation (one cooperative launch) against the oracle
+# ---------------------------------------------------------------------------
+
+def _rollout_vs_oracle(h, r_cpu, seg, label):
+    codes, bs, gs, guide = h.rollout_quant(r_cpu.to(DEV), seg)
+    torch.cuda.synchronize()
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(u16(r_cpu), seg)
+    assert_same(f"{label} codes", codes.cpu().numpy(), o_codes)
+    assert_same(f"{label} bs", bs.cpu().numpy(), o_bs)
+    assert_same(f"{label} gs", gs.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    assert_same(f"{label} guide", u32(guide), o_guide)
+
+
+def _launched(h, fn):
+    h.profile(True)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        t = h.collect()
+        h.profile(False)
+    return {k: n for k, (n, _) in t.items() if n}
+
+
+@pytest.mark.parametrize("fused,wave_bytes", [(0, 16 << 20), (1, 4096), (1, 1 << 20),
+                                              (1, 16 << 20), (1, 40 << 20)])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_rollout_fused_and_split_paths(h, cfg, fused, wave_bytes):
+    w = synth.workload(cfg, small=True)
+    _, r = synth.make_inputs(w, "cpu")
+    h.set_option("fused_amax", fused)
+    h.set_option("wave_bytes", wave_bytes)
+    try:
+        ran = _launched(h, lambda: _rollout_vs_oracle(h, r, w.seg_r, f"cfg{cfg}"))
+    finally:
+        h.set_option("fused_amax", 1)
+        h.set_option("wave_bytes", 32 << 20)
+    if fused:
+        assert ran == {"rollout_fused": 1}, ran
+    else:
+        assert ran == {"amax": 1, "rollout_quant": 1}, ran
+    assert h.device_status() == 0
+
+
+def test_rollout_fused_uneven_and_empty_segments(h):
+    rows, cols = 6000, 96
+    x = rand_bf16((rows, cols), 71, scale=3.0)
+    # empty segments first, in the middle and last; sizes from 1 row to 2400
+    seg = [0, 0, 1, 1, 2401, 2401, 2413, 3000, 3000, 5999, 6000, 6000]
+    h.set_option("wave_bytes", 4096)                # about one segment per wave
+    try:
+        ran = _launched(h, lambda: _rollout_vs_oracle(h, x, seg, "uneven fused"))
+    finally:
+        h.set_option("wave_bytes", 32 << 20)
+    assert ran == {"rollout_fused": 1}
+    _rollout_vs_oracle(h, x, seg, "uneven fused, default waves")
+    assert h.device_status() == 0
+
+
+def test_rollout_large_segment_takes_two_kernels(h):
+    # one segment of 41 MiB of x is more than a fused wave may hold
+    rows, cols = 10496, 2048
+    x = rand_bf16((rows, cols), 72)
+    seg = [0, 16, rows]
+    ran = _launched(h, lambda: _rollout_vs_oracle(h, x, seg, "large segment"))
+    assert ran == {"amax": 1, "rollout_quant": 1}, ran
+
+
+def test_fused_wait_limit_reports_timeout(h):
+    """The in-kernel waits are bounded: with the test hook on, every wait
+    expects one arrival that never comes and gives up at its limit; the call
+    finishes, the status says so, and the handle keeps working."""
+    w = synth.workload(3, small=True)
+    _, r = synth.make_inputs(w, "cpu")
+    rg = r.to(DEV)
+    assert h.device_status() == 0
+    h.set_option("wait_limit_ns", 20_000_000)
+    h.set_option("wait_extra", 1)
+    try:
+        h.rollout_quant(rg, w.seg_r)
+        assert h.device_status() == 6
+    finally:
+        h.set_option("wait_extra", 0)
+        h.set_option("wait_limit_ns", 1_000_000_000)
+    assert h.device_status() == 0
+    _rollout_vs_oracle(h, r, w.seg_r, "after timeout")
+    assert h.device_status() == 0
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_fused_equals_split_full_size(h, cfg):
+    """At full size the fused kernel cycles its staging rings thousands of
+    times; its outputs must equal the two-kernel path's bit for bit (that
+    path is checked against the oracle on sampled windows above), for the
+    default wave size and a large one, on repeated calls."""
+    w = synth.workload(cfg)
+    _, r = synth.make_inputs(w, DEV)
+    h.set_option("fused_amax", 0)
+    try:
+        ref = [t.clone() for t in h.rollout_quant(r, w.seg_r)]
+    finally:
+        h.set_option("fused_amax", 1)
+    try:
+        for wave in (16 << 20, 32 << 20):
+            h.set_option("wave_bytes", wave)
+            out = h.rollout_quant(r, w.seg_r)
+            for _ in range(2):
+                ran = _launched(h, lambda: h.rollout_quant(r, w.seg_r, out=out))
+                assert ran == {"rollout_fused": 1}, ran
+                for name, a, b in zip(("codes", "bs", "gs", "guide"), out, ref):
+                    assert torch.equal(a, b), f"cfg{cfg} wave {wave >> 20} MiB: {name} differs"
+    finally:
+        h.set_option("wave_bytes", 32 << 20)
+    assert h.device_status() == 0
