@@ -61,18 +61,22 @@ def step_bytes_per_elem(guide: str) -> float:
 
 
 # DRAM bytes per element (read + write) of the dominant kernel from one ncu
-# capture (profiles/kernels_kv_rows_32x2x8192x8x128.md), valid only for the
-# kernel source it was taken on; a changed source reports traffic as null.
+# capture (profiles/), valid only for the kernel source it was taken on; a
+# changed source reports traffic as null.
 MEASURED_TRAFFIC = {
-    "fakequant_compact": {"bytes_per_elem": 4.457, "kernels_sha1": "a383b27ee778"},
+    "fakequant_compact": {"bytes_per_elem": 4.457, "kernels_sha1": "bdd56791d695"},
 }
 
 
 def kernels_sha1() -> str:
+    """Hash of the fake-quant kernel's sources (its own file and the shared
+    device helpers): a change there makes the stored traffic stale."""
     import hashlib
-    path = os.path.join(ROOT, "fp4_rollout_guided_gb300", "csrc", "trace_kernels.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()[:12]
+    h = hashlib.sha1()
+    for name in ("trace_fakequant.cu", "trace_device.cuh"):
+        with open(os.path.join(ROOT, "fp4_rollout_guided_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
 
 
 def measured_traffic(kind: str, elems: int):

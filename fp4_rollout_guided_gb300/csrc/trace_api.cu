@@ -1,6 +1,6 @@
 // trace_api.cu - the C ABI declared in include/trace_fp4.h: handle life
 // cycle, argument validation, scratch ordering, the built-in profiler, and
-// the calls that enqueue the kernels of trace_kernels.cu.
+// the calls that enqueue the kernels of trace_kernels.cu and trace_fakequant.cu.
 //
 // Method: "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts",
 // section "TRACE Core Concept" (rollout-side record, training-side guided

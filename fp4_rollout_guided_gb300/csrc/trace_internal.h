@@ -1,5 +1,6 @@
 // trace_internal.h - launch interface between the C ABI (trace_api.cu) and
-// the sm_103a kernels (trace_kernels.cu).  Not part of the public ABI.
+// the sm_103a kernels (trace_kernels.cu, trace_fakequant.cu).  Not part of the
+// public ABI.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -1,359 +1,16 @@
-// trace_kernels.cu - sm_103a kernels of the guided-NVFP4 hot path of TRACE.
+// trace_kernels.cu - sm_103a kernels of the guided-NVFP4 hot path of TRACE
+// except the training-side fake quantiser (trace_fakequant.cu): segment
+// amax, rollout quantisation (two-kernel and fused forms), guide pack and
+// unpack, and the straight-through backward.  The work decomposition and
+// arithmetic conventions are described in trace_device.cuh.
 //
 // Sources: "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts",
-// section "TRACE Core Concept" (rollout records FP4 results; training-side
-// fake quantisation picks the adjacent E2M1 point closer to the rollout's;
-// a compact record of mantissa bit + scale sets the direction) and the
-// worked example of section "Why Does FP4 Rollout 'Break' RL Training?".
-//
-// Work decomposition.  Every kernel streams a flat sequence of 32-element
-// "chunks" (two 16-element NVFP4 blocks, one STE mask word).  Rows hold
-// cols/32 chunks, so a chunk never straddles a row or a segment.  A CTA of
-// 256 threads handles a "step" of 256 consecutive chunks (16 KiB of bf16),
-// one chunk per thread, and owns a contiguous range of steps; the next
-// step's loads are issued before the current step is computed.  Segments
-// are looked up once per step (uniform across the CTA); only a step that
-// straddles a segment boundary resolves segments per thread.
-//
-// Arithmetic.  All of it is binary32 with round-to-nearest-even (explicit
-// __f*_rn intrinsics so nothing is contracted into an FMA; no flush to zero),
-// in the same operation order as the method's definition:
-//   gs = amax / 2688;  bs = e4m3(bamax / (gs * 6));  S = dec(bs) * gs;
-//   inv = 1 / S (0 if S == 0 or the reciprocal overflows);  t = |x| * inv.
-// E2M1 rounding uses directed-rounding adds against a constant C whose ulp
-// equals the E2M1 spacing of t's binade (C = 1.5 * 2^(22+e), 2^e the binade
-// of max(t, 1), t clamped to 6): fl_rz(t + C) - C, fl_rp(t + C) - C and
-// fl_rn(t + C) - C are exactly the lower, upper and nearest E2M1 points
-// (ties go to the even index because C is an even number of ulps), and the
-// last significand bit of fl_rz(t + C) is the parity of the lower index.
-#include <cuda_runtime.h>
-#include <stdint.h>
-
-#include <mutex>
-#include <unordered_map>
-
-#include "trace_internal.h"
+// section "TRACE Core Concept", and the worked example of section "Why
+// Does FP4 Rollout 'Break' RL Training?".
+#include "trace_device.cuh"
 
 namespace tfp4 {
 namespace {
-
-constexpr int kThreads = 256;
-constexpr int kWaveSegs = 256;  // segments per wave of the fused rollout kernel
-constexpr uint32_t kAbs2 = 0x7FFF7FFFu;
-
-// ---------------------------------------------------------------------------
-// memory access
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ld_stream2(const void* p) {
-  uint2 v;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
-  unsigned short v;
-  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void st_stream(void* p, uint32_t a, uint32_t b, uint32_t c,
-                                          uint32_t d) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_stream2(void* p, uint32_t a, uint32_t b) {
-  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
-}
-
-__device__ __forceinline__ void st_stream1(void* p, uint32_t a) {
-  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
-}
-
-__device__ __forceinline__ void st_stream_u16(void* p, uint32_t a) {
-  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)a) : "memory");
-}
-
-struct Chunk {
-  uint32_t w[16];  // 32 bf16: element 2i in the low half of w[i]
-};
-
-__device__ __forceinline__ void load_chunk(Chunk& c, const uint8_t* base, uint32_t chunk) {
-  const uint8_t* p = base + (uint64_t)chunk * 64u;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = ld_stream(p + 16 * q);
-    c.w[4 * q + 0] = v.x;
-    c.w[4 * q + 1] = v.y;
-    c.w[4 * q + 2] = v.z;
-    c.w[4 * q + 3] = v.w;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// segments
-// ---------------------------------------------------------------------------
-
-// Largest s with off[s] <= row (off[n] = rows > row); with empty segments the
-// non-empty one is found.
-__device__ __forceinline__ int seg_search(const SegParam& p, uint32_t row) {
-  int lo = 0, hi = p.n;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((uint32_t)p.off[mid] <= row) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ int seg_advance(const SegParam& p, int s, uint32_t row) {
-  while ((uint32_t)p.off[s + 1] <= row) ++s;
-  return s;
-}
-
-// Per-step segment resolution: `cur` follows the step's first row; update()
-// returns true when the whole step lies inside segment `cur`.
-struct StepSeg {
-  int cur;
-  __device__ __forceinline__ bool update(const SegParam& p, uint32_t r0, uint32_t r1) {
-    cur = seg_advance(p, cur, r0);
-    return (uint32_t)p.off[cur + 1] > r1;
-  }
-};
-
-// ---------------------------------------------------------------------------
-// scales
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Eight words of masked bf16 magnitudes -> binary32 bits of their maximum.
-__device__ __forceinline__ float block_amax8(const uint32_t* a) {
-  uint32_t m0 = max_u16x2(a[0], a[1]);
-  const uint32_t m1 = max_u16x2(a[2], a[3]);
-  const uint32_t m2 = max_u16x2(a[4], a[5]);
-  const uint32_t m3 = max_u16x2(a[6], a[7]);
-  m0 = max_u16x2(max_u16x2(m0, m1), max_u16x2(m2, m3));
-  const uint32_t hi = m0 >> 16, lo = m0 & 0xFFFFu;
-  return __uint_as_float((hi > lo ? hi : lo) << 16);
-}
-
-// E4M3 code -> binary32: placing the 7 magnitude bits at bit 20 gives the
-// value times 2^-120 (normal and subnormal codes alike); scaling by 2^120 is
-// exact.
-__device__ __forceinline__ float e4m3_decode(uint32_t code) {
-  return __fmul_rn(__uint_as_float(code << 20), 0x1p120f);
-}
-
-__device__ __forceinline__ float global_scale_of(uint32_t amax_bits) {
-  const float amax = __uint_as_float(amax_bits);
-  if (!(amax > 0.0f)) return 0.0f;
-  const float gs = __fdiv_rn(amax, 2688.0f);
-  return gs > 0.0f ? gs : 0.0f;
-}
-
-struct PairScale {
-  uint32_t codes;  // byte 0: block 0, byte 1: block 1
-  float S[2];
-  float inv[2];
-};
-
-__device__ __forceinline__ void real_scale(uint32_t code, float gs, float& S, float& inv) {
-  S = __fmul_rn(e4m3_decode(code), gs);
-  float r = 0.0f;
-  if (S > 0.0f) {
-    r = __frcp_rn(S);
-    if (r == __int_as_float(0x7F800000)) r = 0.0f;  // reciprocal overflow: flush
-  }
-  inv = r;
-}
-
-// Two binary32 values -> two E4M3 codes (RNE, satfinite): byte 0 = lo.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  unsigned short c;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
-  return c;
-}
-
-// Both blocks' E4M3 scales from their maxima and the segment scale.
-//
-// The method divides: q = bamax / (gs * 6), rounded once.  An IEEE division
-// costs about twenty integer-pipe instructions, so the quotient is first
-// formed as q' = bamax * fl(1 / (gs * 6)), which lies within 2.5 ulp of q.
-// E4M3 encoding is monotone, so when q' * (1 - 2^-21) and q' * (1 + 2^-21)
-// (a bracket around q) encode to the same code, that code is the code of q.
-// Otherwise -- q within a few ulps of an E4M3 rounding boundary, or a
-// reciprocal that overflows -- the correctly rounded division decides.
-// E4M3 codes of both blocks given den = gs * 6 and rden = fl(1 / den).
-__device__ __forceinline__ uint32_t pair_codes(float bamax0, float bamax1, float gs, float den,
-                                               float rden) {
-  uint32_t codes = 0;
-  if (gs > 0.0f) {
-    bool exact = !(rden < __int_as_float(0x7F800000));
-    if (!exact) {
-      const float q0 = __fmul_rn(bamax0, rden), q1 = __fmul_rn(bamax1, rden);
-      const uint32_t lo = e4m3x2(__fmul_rn(q0, 1.0f - 0x1p-21f), __fmul_rn(q1, 1.0f - 0x1p-21f));
-      const uint32_t hi = e4m3x2(__fmul_rn(q0, 1.0f + 0x1p-21f), __fmul_rn(q1, 1.0f + 0x1p-21f));
-      codes = lo;
-      exact = lo != hi;
-    }
-    if (exact) codes = e4m3x2(__fdiv_rn(bamax0, den), __fdiv_rn(bamax1, den));
-  }
-  return codes;
-}
-
-__device__ __forceinline__ PairScale pair_scale(float bamax0, float bamax1, float gs) {
-  const float den = __fmul_rn(gs, 6.0f);
-  const uint32_t codes = pair_codes(bamax0, bamax1, gs, den, gs > 0.0f ? __frcp_rn(den) : 0.0f);
-  PairScale p;
-  p.codes = codes;
-  real_scale(codes & 0xFFu, gs, p.S[0], p.inv[0]);
-  real_scale(codes >> 8, gs, p.S[1], p.inv[1]);
-  return p;
-}
-
-// STE threshold of a block in bf16 magnitude bits, doubled into two 16-bit
-// lanes with the lane top bits set: |x| > 6 * S exactly when the bf16 |x|
-// exceeds 6 * S rounded down to bf16 (truncation), so for a word of two
-// magnitudes, bit 15 / 31 of thr2 - |x| is set exactly when the element is
-// kept (no borrow crosses the lanes).
-__device__ __forceinline__ uint32_t ste_threshold2(float S) {
-  const uint32_t thr = S > 0.0f ? (__float_as_uint(__fmul_rn(6.0f, S)) >> 16) : 0x7FFFu;
-  return (thr | 0x8000u) * 0x00010001u;
-}
-
-// Per-segment table in shared memory, indexed by E4M3 code: the block's real
-// scale, its reciprocal (flush rule applied) and STE threshold.  A segment's
-// blocks take one of at most 127 scales, so the reciprocals are formed once
-// per segment instead of once per block.  Codes above 0x7E never come out of
-// the quantiser; a stored code is masked to 7 bits before the lookup.
-struct ScaleTab {
-  float2 sinv[128];
-  uint32_t thr2[128];
-};
-
-__device__ __forceinline__ void build_tab(ScaleTab& t, float gs) {
-  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
-    float S, inv;
-    real_scale((uint32_t)c, gs, S, inv);
-    t.sinv[c] = make_float2(S, inv);
-    t.thr2[c] = ste_threshold2(S);
-  }
-}
-
-// Real scales of two stored E4M3 codes (the rollout side's record).
-__device__ __forceinline__ PairScale pair_scale_stored(uint32_t codes, float gs) {
-  PairScale p;
-  p.codes = codes;
-  real_scale(codes & 0x7Fu, gs, p.S[0], p.inv[0]);
-  real_scale((codes >> 8) & 0x7Fu, gs, p.S[1], p.inv[1]);
-  return p;
-}
-
-// ---------------------------------------------------------------------------
-// packed binary32 pairs (f32x2 instructions: one issue slot for two lanes)
-// ---------------------------------------------------------------------------
-
-struct F2 {
-  float x, y;
-};
-
-#define TFP4_F2_OP(name, inst)                                                      \
-  __device__ __forceinline__ F2 name(F2 a, F2 b) {                                   \
-    F2 d;                                                                           \
-    asm("{ .reg .b64 A, B, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; " inst       \
-        " D, A, B; mov.b64 {%0, %1}, D; }"                                          \
-        : "=f"(d.x), "=f"(d.y)                                                      \
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                  \
-    return d;                                                                       \
-  }
-TFP4_F2_OP(add2_rn, "add.rn.f32x2")
-TFP4_F2_OP(add2_rz, "add.rz.f32x2")
-TFP4_F2_OP(add2_rp, "add.rp.f32x2")
-TFP4_F2_OP(sub2_rn, "sub.rn.f32x2")
-TFP4_F2_OP(mul2_rn, "mul.rn.f32x2")
-#undef TFP4_F2_OP
-
-__device__ __forceinline__ F2 fma2_rn(F2 a, F2 b, F2 c) {
-  F2 d;
-  asm("{ .reg .b64 A, B, C, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; "
-      "mov.b64 C, {%6, %7}; fma.rn.f32x2 D, A, B, C; mov.b64 {%0, %1}, D; }"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
-__device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
-
-// Multiply-add on the FMA pipe (IMAD): a * b + c, wrapping.
-__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ float fma_sat(float a, float b, float c) {
-  float d;
-  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// ---------------------------------------------------------------------------
-// E2M1
-// ---------------------------------------------------------------------------
-
-// Two signed binary32 values -> one byte of two E2M1 nibbles (lo = first).
-// Hardware RTN, ties to even, saturating at +-6, sign kept.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %1, %2; cvt.u32.u8 %0, b; }"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
-// The rounding constant for t in [0, 6]: 1.5 * 2^(22 + e) with 2^e the
-// binade of max(t, 1).
-__device__ __forceinline__ float magic_of(float tc) {
-  uint32_t e = __float_as_uint(tc) & 0x7F800000u;
-  e = e > 0x3F800000u ? e : 0x3F800000u;
-  return __uint_as_float(e + 0x0B400000u);
-}
-
-// The same constant for a pair of clamped values.  Two exact formulations:
-// TFP4_MAGIC_FMA = 1 builds it on the FMA pipe from two saturating
-// indicators, b1 = [tc > 2] and b2 = [tc > 4] (sat(tc * 2^30 - 2^31) is 0 for
-// tc <= 2 and 1 otherwise: the next binary32 above 2 is 2 + 2^-22), then
-// C = K * (1 + b1) * (1 + b2), K = 1.5 * 2^22; otherwise it takes the
-// exponent field with integer operations.  At tc = 2 or 4 both constants put
-// the (on-grid) value on the grid, so the boundary side does not matter.
-#ifndef TFP4_MAGIC_FMA
-#define TFP4_MAGIC_FMA 1
-#endif
-__device__ __forceinline__ F2 magic_pair(F2 tc) {
-#if TFP4_MAGIC_FMA
-  const float k = 0x1.8p22f;
-  const F2 b1 = {fma_sat(tc.x, 0x1p30f, -0x1p31f), fma_sat(tc.y, 0x1p30f, -0x1p31f)};
-  const F2 b2 = {fma_sat(tc.x, 0x1p30f, -0x1p32f), fma_sat(tc.y, 0x1p30f, -0x1p32f)};
-  const F2 m1 = fma2_rn(b1, splat(k), splat(k));
-  return fma2_rn(b2, m1, m1);
-#else
-  return F2{magic_of(tc.x), magic_of(tc.y)};
-#endif
-}
 
 // ---------------------------------------------------------------------------
 // a1: segment amax + global scales
@@ -1080,23 +737,6 @@ __global__ void __launch_bounds__(kThreads)
 // a4: guide unpack
 // ---------------------------------------------------------------------------
 
-// Rollout-frame decode of a pair from the compact record: for each element
-// the bracket member of t_r whose index parity equals its stored bit (a
-// point bracket ignores the bit).  gw is the block's compact word and j0 the
-// first element's index: the parity of the lower member (bit 0 of the
-// rz-sum) is moved up to the stored bit's position (16 + j) by a multiply
-// and compared there.  Returns the two E2M1 magnitudes.
-__device__ __forceinline__ F2 decode_pair(F2 tr, uint32_t gw, int j0) {
-  const F2 tc = {fminf(tr.x, 6.0f), fminf(tr.y, 6.0f)};
-  const F2 C = magic_pair(tc);
-  const F2 uz = add2_rz(tc, C), up = add2_rp(tc, C);
-  const uint32_t b0 = 1u << (16 + j0), b1 = 1u << (17 + j0);
-  const uint32_t m0 = (imad(__float_as_uint(uz.x), b0, 0u) ^ gw) & b0;
-  const uint32_t m1 = (imad(__float_as_uint(uz.y), b1, 0u) ^ gw) & b1;
-  const F2 us = {m0 ? up.x : uz.x, m1 ? up.y : uz.y};
-  return sub2_rn(us, C);
-}
-
 // Two elements of one bf16x2 word -> one byte of rollout codes.  j0 is the
 // index of the word's low element inside its 16-element block.
 __device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t gw, int j0) {
@@ -1169,342 +809,6 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// a5 + a6: training-side guided fake quantisation
-// ---------------------------------------------------------------------------
-
-// Signed E2M1 values of a byte's two nibbles (hardware E2M1 -> f16 decode).
-__device__ __forceinline__ void e2m1x2_values(uint32_t byte, float& v0, float& v1) {
-  uint32_t h;
-  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(h) : "r"(byte));
-  const unsigned short lo = (unsigned short)(h & 0xFFFFu), hi = (unsigned short)(h >> 16);
-  asm("cvt.f32.f16 %0, %1;" : "=f"(v0) : "h"(lo));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(v1) : "h"(hi));
-}
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-struct Counters {
-  uint32_t mm_rtn, mm_g, h_rtn[4], h_g[4];
-};
-
-// exact signed grid value -> signed E2M1 index (+0 and -0 both give 0)
-__device__ __forceinline__ int signed_index(float g_signed) {
-  const uint32_t n = e2m1x2(g_signed, 0.0f) & 0xFu;
-  const int m = (int)(n & 7u);
-  return (n & 8u) ? -m : m;
-}
-
-__device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) {
-  int d0 = k_rtn - k_r, d1 = k_g - k_r;
-  d0 = d0 < 0 ? -d0 : d0;
-  d1 = d1 < 0 ? -d1 : d1;
-  k.mm_rtn += d0 != 0;
-  k.mm_g += d1 != 0;
-  k.h_rtn[0] += d0 == 0;
-  k.h_rtn[1] += d0 == 1;
-  k.h_rtn[2] += d0 == 2;
-  k.h_rtn[3] += d0 >= 3;
-  k.h_g[0] += d1 == 0;
-  k.h_g[1] += d1 == 1;
-  k.h_g[2] += d1 == 2;
-  k.h_g[3] += d1 >= 3;
-}
-
-__device__ __forceinline__ float fmul_sat(float a, float b) {
-  float d;
-  asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-
-// Training side of one pair of elements.  ax holds |x|; St holds the
-// training scale carrying each element's sign, vr the rollout's
-// reconstructed values with the rollout's signs, so the candidates
-// v_c = G[c] * St are the signed values the method compares and the chosen
-// one is the signed output.  ym receives the chosen signed values; with
-// WANT_G, gsel / grtn receive the chosen and the RTN E2M1 magnitudes.
-//
-// The choice: hi wins when |d_hi| < |d_lo|, or on equality when RTN is hi.
-// diff = |d_lo| - |d_hi| is exact in sign (and +0 only on equality), and
-// RTN-is-hi is bits(s_rn) - bits(s_rz), 0 or 1, so hi <=> bits(diff) +
-// rtn_hi - 1 >= 0 as a signed integer; the select is done on the bit
-// patterns: y = v_hi - lo * (v_hi - v_lo) with lo = 0 or 1.
-template <bool GUIDED, bool WANT_G>
-__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2& ym, F2& gsel,
-                                           F2& grtn) {
-  const F2 t = mul2_rn(ax, splat(inv_t));
-  const F2 tc = {fminf(t.x, 6.0f), fminf(t.y, 6.0f)};
-  const F2 C = magic_pair(tc);
-  const F2 sn = add2_rn(tc, C);
-  if (!GUIDED) {
-    const F2 g = sub2_rn(sn, C);
-    ym = mul2_rn(g, St);
-    gsel = g;
-    grtn = g;
-    return;
-  }
-  const F2 sz = add2_rz(tc, C), sp = add2_rp(tc, C);
-  const F2 glo = sub2_rn(sz, C), ghi = sub2_rn(sp, C);
-  const F2 vlo = mul2_rn(glo, St), vhi = mul2_rn(ghi, St);
-  const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
-  const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
-  const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
-#if TFP4_SELECT_IMAD
-  // lo = key >> 31 as the high word of key * 2; v_lo - v_hi on bit patterns
-  const uint32_t k0 = __float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x);
-  const uint32_t k1 = __float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y);
-  const uint32_t lo0 = __umulhi(k0, 2u), lo1 = __umulhi(k1, 2u);
-  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
-  ym = F2{__uint_as_float(imad(lo0, imad(h0, 0xFFFFFFFFu, __float_as_uint(vlo.x)), h0)),
-          __uint_as_float(imad(lo1, imad(h1, 0xFFFFFFFFu, __float_as_uint(vlo.y)), h1))};
-#else
-  const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
-  const uint32_t lo1 = (__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y)) >> 31;
-  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
-  ym = F2{__uint_as_float(imad(lo0, __float_as_uint(vlo.x) - h0, h0)),
-          __uint_as_float(imad(lo1, __float_as_uint(vlo.y) - h1, h1))};
-#endif
-  if (WANT_G) {
-    gsel = F2{lo0 ? glo.x : ghi.x, lo1 ? glo.y : ghi.y};
-    grtn = F2{sn.x != sz.x ? ghi.x : glo.x, sn.y != sz.y ? ghi.y : glo.y};
-  }
-}
-
-// Spreads the 16 low bits of v to the even bit positions.
-__device__ __forceinline__ uint32_t spread16(uint32_t v) {
-  v = (v | (v << 8)) & 0x00FF00FFu;
-  v = (v | (v << 4)) & 0x0F0F0F0Fu;
-  v = (v | (v << 2)) & 0x33333333u;
-  v = (v | (v << 1)) & 0x55555555u;
-  return v;
-}
-
-#ifndef TFP4_FQ_PREFETCH
-#define TFP4_FQ_PREFETCH 0
-#endif
-#ifndef TFP4_FQ_MIN_CTAS
-#define TFP4_FQ_MIN_CTAS 4
-#endif
-template <int KIND, bool MASK, bool CODES, bool STATS>
-__global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
-    k_fakequant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
-                uint32_t steps_per_cta, const __grid_constant__ SegParam seg_t,
-                const float* __restrict__ gs_t, const __grid_constant__ SegParam seg_r,
-                const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
-                const float* __restrict__ gs_r, uint8_t* __restrict__ y,
-                uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
-                trace_stats_t* __restrict__ stats) {
-  constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
-  const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
-  uint32_t step = blockIdx.x * steps_per_cta;
-  const uint32_t step_end = min(step + steps_per_cta, nsteps);
-  StepSeg st, sr;
-  st.cur = 0;
-  sr.cur = 0;
-  if (step < step_end) {
-    const uint32_t r0 = cpr.div(step * kThreads);
-    st.cur = seg_search(seg_t, r0);
-    if (GUIDED) sr.cur = seg_search(seg_r, r0);
-  }
-  Counters cnt = {};
-  uint32_t n_done = 0;
-  __shared__ ScaleTab tab_t, tab_r;
-  int tseg = -1, rseg = -1;                 // segments the tables hold
-  float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
-
-  Chunk cur, nxt;
-  uint4 gcur = make_uint4(0, 0, 0, 0), gnxt = make_uint4(0, 0, 0, 0);
-  uint32_t bcur = 0, bnxt = 0;
-  if (step < step_end) {
-    const uint32_t c = step * kThreads + threadIdx.x;
-    if (c < nchunks) {
-      load_chunk(cur, x, c);
-      if (KIND == TRACE_GUIDE_COMPACT) {
-        const uint2 v = ld_stream2(guide + (uint64_t)c * 8u);
-        gcur.x = v.x;
-        gcur.y = v.y;
-      } else if (KIND == TRACE_GUIDE_FULL) {
-        gcur = ld_stream(guide + (uint64_t)c * 16u);
-      }
-      if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)c * 2u);
-    }
-  }
-  for (; step < step_end; ++step) {
-    const uint32_t c0 = step * kThreads;
-    const uint32_t c = c0 + threadIdx.x;
-    if (TFP4_FQ_PREFETCH && step + 1 < step_end) {
-      const uint32_t cn = c + kThreads;
-      if (cn < nchunks) {
-        load_chunk(nxt, x, cn);
-        if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint2 v = ld_stream2(guide + (uint64_t)cn * 8u);
-          gnxt.x = v.x;
-          gnxt.y = v.y;
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          gnxt = ld_stream(guide + (uint64_t)cn * 16u);
-        }
-        if (GUIDED) bnxt = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
-      }
-    }
-    const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kThreads, nchunks) - 1);
-    const bool uni_t = st.update(seg_t, r0, r1);
-    const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
-    // refresh the scale tables when the (uniform) segment changes
-    const bool new_t = uni_t && st.cur != tseg;
-    const bool new_r = GUIDED && uni_r && sr.cur != rseg;
-    if (new_t || new_r) {
-      __syncthreads();
-      if (new_t) {
-        tseg = st.cur;
-        seg_gs = gs_t[tseg];
-        seg_den = __fmul_rn(seg_gs, 6.0f);
-        seg_rden = seg_gs > 0.0f ? __frcp_rn(seg_den) : 0.0f;
-        build_tab(tab_t, seg_gs);
-      }
-      if (new_r) {
-        rseg = sr.cur;
-        build_tab(tab_r, gs_r[rseg]);
-      }
-      __syncthreads();
-    }
-    if (c < nchunks) {
-      int s_t = st.cur, s_r = sr.cur;
-      if (!uni_t || !uni_r) {
-        const uint32_t row = cpr.div(c);
-        if (!uni_t) s_t = seg_advance(seg_t, st.cur, row);
-        if (GUIDED && !uni_r) s_r = seg_advance(seg_r, sr.cur, row);
-      }
-      uint32_t a[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-      PairScale pt, pr = {};
-      uint32_t thr2[2];
-      if (uni_t) {
-        pt.codes = pair_codes(block_amax8(a), block_amax8(a + 8), seg_gs, seg_den, seg_rden);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const uint32_t code = (pt.codes >> (8 * b)) & 0xFFu;
-          const float2 e = tab_t.sinv[code];
-          pt.S[b] = e.x;
-          pt.inv[b] = e.y;
-          thr2[b] = tab_t.thr2[code];
-        }
-      } else {
-        pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
-        thr2[0] = ste_threshold2(pt.S[0]);
-        thr2[1] = ste_threshold2(pt.S[1]);
-      }
-      if (GUIDED) {
-        if (uni_r) {
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const float2 e = tab_r.sinv[(bcur >> (8 * b)) & 0x7Fu];
-            pr.S[b] = e.x;
-            pr.inv[b] = e.y;
-          }
-        } else {
-          pr = pair_scale_stored(bcur, gs_r[s_r]);
-        }
-      }
-
-      uint32_t ybits[4];
-      uint32_t cbytes[16];
-      uint32_t kept = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int b = i >> 3;        // block of this word
-        const int j0 = (i & 7) * 2;  // index of its low element in the block
-        const uint32_t w = cur.w[i];
-        const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)), __uint_as_float(a[i] & 0xFFFF0000u)};
-        const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
-        const uint32_t Stb = __float_as_uint(pt.S[b]);
-        const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
-        F2 vr = {0.0f, 0.0f};
-        F2 grs = {0.0f, 0.0f};  // signed rollout magnitudes (statistics)
-        if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint32_t gw = b ? gcur.y : gcur.x;
-          const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw, j0);
-          const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
-          const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
-          const uint32_t Sb = __float_as_uint(pr.S[b]);
-          vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
-          if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
-                              __uint_as_float(__float_as_uint(gr.y) | sr1)};
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
-          float g0, g1;
-          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
-          vr = mul2_rn(F2{g0, g1}, splat(pr.S[b]));
-          if (STATS) grs = F2{g0, g1};
-        }
-        F2 ym, gsel, grtn;
-        train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, ym, gsel, grtn);
-        ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
-        if ((i & 3) == 3)
-          st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-        if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
-        if (CODES || STATS) {
-          const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
-          const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
-          if (CODES) cbytes[i] = e2m1x2(g0, g1);
-          if (STATS && GUIDED) {
-            count(cnt, signed_index(grs.x),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.x) | sx0)), signed_index(g0));
-            count(cnt, signed_index(grs.y),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.y) | sx1)), signed_index(g1));
-          }
-        }
-      }
-      // word i left its two bits at positions i and 16 + i: interleave
-      if (MASK) kept = spread16(kept & 0xFFFFu) | (spread16(kept >> 16) << 1);
-      if (MASK) st_stream1(mask + (uint64_t)c * 4u, kept);
-      if (CODES) {
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = cbytes[4 * q] | (cbytes[4 * q + 1] << 8) | (cbytes[4 * q + 2] << 16) |
-                 (cbytes[4 * q + 3] << 24);
-        st_stream(codes_t + (uint64_t)c * 16u, o[0], o[1], o[2], o[3]);
-      }
-      if (STATS) n_done += 32;
-    }
-    if (TFP4_FQ_PREFETCH) {
-      cur = nxt;
-      gcur = gnxt;
-      bcur = bnxt;
-    } else if (step + 1 < step_end) {
-      const uint32_t cn = c + kThreads;
-      if (cn < nchunks) {
-        load_chunk(cur, x, cn);
-        if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint2 v = ld_stream2(guide + (uint64_t)cn * 8u);
-          gcur.x = v.x;
-          gcur.y = v.y;
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          gcur = ld_stream(guide + (uint64_t)cn * 16u);
-        }
-        if (GUIDED) bcur = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
-      }
-    }
-  }
-  if (STATS) {
-    const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
-                            cnt.h_rtn[1], cnt.h_rtn[2], cnt.h_rtn[3], cnt.h_g[0],
-                            cnt.h_g[1],   cnt.h_g[2],   cnt.h_g[3]};
-    unsigned long long* dst = reinterpret_cast<unsigned long long*>(stats);
-#pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      if (!GUIDED && k > 0) break;
-      const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, v[k]);
-      if ((threadIdx.x & 31) == 0 && tot) atomicAdd(dst + k, (unsigned long long)tot);
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // straight-through backward: grad_in = grad_out where the mask bit is 1, +0
 // elsewhere.  One chunk (32 elements, one mask word) per thread per step;
 // each mask bit pair becomes a 0xFFFF / 0x0000 lane mask for a bf16x2 word.
@@ -1549,73 +853,6 @@ __global__ void __launch_bounds__(kThreads)
         for (int q = 0; q < 4; ++q) st_stream(p + 16 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// launch planning: persistent grids of (occupancy x SM count) CTAs, each
-// owning a contiguous range of steps
-// ---------------------------------------------------------------------------
-
-struct Plan {
-  int grid;
-  uint32_t steps_per_cta;
-};
-
-int occupancy_of(const void* kernel) {
-  static std::mutex mu;
-  static std::unordered_map<const void*, int> cache;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(kernel);
-  if (it != cache.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess) {
-    cudaGetLastError();
-    n = 1;
-  }
-  if (n < 1) n = 1;
-  cache[kernel] = n;
-  return n;
-}
-
-Plan plan_for(const void* kernel, int64_t nsteps, int sm_count) {
-  int64_t g = (int64_t)sm_count * occupancy_of(kernel);
-  if (nsteps < g) g = nsteps;
-  if (g < 1) g = 1;
-  Plan p;
-  p.grid = (int)g;
-  p.steps_per_cta = (uint32_t)((nsteps + g - 1) / g);
-  return p;
-}
-
-int64_t steps_of(int64_t nchunks, int64_t per_step) { return (nchunks + per_step - 1) / per_step; }
-
-template <int KIND, bool MASK, bool CODES, bool STATS>
-cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegParam& seg_r,
-                      int sm_count, cudaStream_t st) {
-  auto kern = k_fakequant<KIND, MASK, CODES, STATS>;
-  const Plan p = plan_for((const void*)kern, steps_of(a.nchunks, kThreads), sm_count);
-  kern<<<p.grid, kThreads, 0, st>>>((const uint8_t*)a.x, (uint32_t)a.nchunks,
-                                    FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
-                                    seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
-                                    a.gs_r, (uint8_t*)a.y, (uint8_t*)a.mask,
-                                    (uint8_t*)a.codes_t, a.stats);
-  return cudaGetLastError();
-}
-
-template <int KIND>
-cudaError_t fq_dispatch(const FakequantArgs& a, const SegParam& t, const SegParam& r, int sm,
-                        cudaStream_t st) {
-  const int sel = ((a.mask != nullptr) << 2) | ((a.codes_t != nullptr) << 1) | (a.stats != nullptr);
-  switch (sel) {
-    case 0: return fq_launch<KIND, false, false, false>(a, t, r, sm, st);
-    case 1: return fq_launch<KIND, false, false, true>(a, t, r, sm, st);
-    case 2: return fq_launch<KIND, false, true, false>(a, t, r, sm, st);
-    case 3: return fq_launch<KIND, false, true, true>(a, t, r, sm, st);
-    case 4: return fq_launch<KIND, true, false, false>(a, t, r, sm, st);
-    case 5: return fq_launch<KIND, true, false, true>(a, t, r, sm, st);
-    case 6: return fq_launch<KIND, true, true, false>(a, t, r, sm, st);
-    default: return fq_launch<KIND, true, true, true>(a, t, r, sm, st);
   }
 }
 
@@ -1745,16 +982,6 @@ cudaError_t launch_ste_backward(const void* g, const uint32_t* mask, int64_t nch
   k_ste_backward<<<p.grid, kThreads, 0, st>>>((const uint8_t*)g, (const uint8_t*)mask,
                                               (uint32_t)nchunks, p.steps_per_cta, (uint8_t*)out);
   return cudaGetLastError();
-}
-
-cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
-                             const SegParam& seg_r, int sm_count, cudaStream_t st) {
-  switch (a.kind) {
-    case TRACE_GUIDE_FULL: return fq_dispatch<TRACE_GUIDE_FULL>(a, seg_t, seg_r, sm_count, st);
-    case TRACE_GUIDE_COMPACT:
-      return fq_dispatch<TRACE_GUIDE_COMPACT>(a, seg_t, seg_r, sm_count, st);
-    default: return fq_dispatch<TRACE_GUIDE_NONE>(a, seg_t, seg_r, sm_count, st);
-  }
 }
 
 }  // namespace tfp4
