@@ -83,6 +83,9 @@ def _load():
             "orc_guide_unpack": (INT, [P, P, P, P, P, I32, I64, I64, P]),
             "orc_train_fakequant": (INT, [P, I64, I64, P, I32, INT, P, P, P, P,
                                           I32, P, P, P, P]),
+            "orc_mma_scales_bytes": (I64, [I64, I64]),
+            "orc_mma_scales": (INT, [P, I64, I64, P]),
+            "orc_nvfp4_gemm": (INT, [P, P, F32, P, P, F32, I64, I64, I64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -272,3 +275,29 @@ def ste_backward(g, mask):
     out = np.zeros((rows, cols), dtype=np.uint16)
     _check(_load().orc_ste_backward(_ptr(g), _ptr(mask), rows, cols, _ptr(out)), "ste_backward")
     return out
+
+
+def mma_scales(bs, rows, cols):
+    """Row-major block scales uint8[rows, cols/16] -> the tensor-core tiled
+    layout (uint8, zero-padded to 128-row x 4-column tiles)."""
+    bs = np.ascontiguousarray(bs, dtype=np.uint8).reshape(rows, cols // 16)
+    n = _load().orc_mma_scales_bytes(rows, cols)
+    if n < 0:
+        raise ValueError("mma_scales: bad shape")
+    out = np.zeros(n, dtype=np.uint8)
+    _check(_load().orc_mma_scales(_ptr(bs), rows, cols, _ptr(out)), "mma_scales")
+    return out
+
+
+def nvfp4_gemm(a_codes, a_bs, a_gs, b_codes, b_bs, b_gs):
+    """d[m, n] = fl32(a_gs * b_gs) * sum_k A[i, k] B[j, k] in float64."""
+    a_codes = np.ascontiguousarray(a_codes, dtype=np.uint8)
+    b_codes = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    m, k = a_codes.shape[0], a_codes.shape[1] * 2
+    n = b_codes.shape[0]
+    a_bs = np.ascontiguousarray(a_bs, dtype=np.uint8)
+    b_bs = np.ascontiguousarray(b_bs, dtype=np.uint8)
+    d = np.zeros((m, n), dtype=np.float64)
+    _check(_load().orc_nvfp4_gemm(_ptr(a_codes), _ptr(a_bs), float(a_gs), _ptr(b_codes),
+                                  _ptr(b_bs), float(b_gs), m, n, k, _ptr(d)), "nvfp4_gemm")
+    return d

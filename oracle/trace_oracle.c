@@ -538,3 +538,54 @@ int orc_ste_backward(const uint16_t* g, const uint32_t* mask, int64_t rows, int6
     }
   return 0;
 }
+
+/* ---- block scales for tensor cores, and the NVFP4 GEMM that uses them ---- */
+
+static int64_t ceil_to(int64_t v, int64_t q) { return (v + q - 1) / q * q; }
+
+int64_t orc_mma_scales_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols <= 0 || cols % 16) return -1;
+  return ceil_to(rows, 128) * ceil_to(cols / 16, 4);
+}
+
+/* Layout per NVIDIA's cuBLAS documentation, "1D block scaling factors
+ * layout": 512-byte tiles of 128 rows x 4 scale columns, tiles running along
+ * the scale columns, (r, c) inside a tile at 16 (r mod 32) + 4 (r div 32) + c. */
+int orc_mma_scales(const uint8_t* bs, int64_t rows, int64_t cols, uint8_t* out) {
+  int64_t bytes = orc_mma_scales_bytes(rows, cols);
+  if (bytes < 0) return -1;
+  int64_t sc = cols / 16;                  /* scale columns               */
+  int64_t tiles_per_row = ceil_to(sc, 4) / 4;
+  for (int64_t i = 0; i < bytes; ++i) out[i] = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < sc; ++c) {
+      int64_t tile = (r / 128) * tiles_per_row + c / 4;
+      int64_t rr = r % 128, cc = c % 4;
+      out[tile * 512 + 16 * (rr % 32) + 4 * (rr / 32) + cc] = bs[r * sc + c];
+    }
+  return 0;
+}
+
+static double nvfp4_value(const uint8_t* codes, const uint8_t* bs, int64_t cols, int64_t r,
+                          int64_t c) {
+  int64_t e = r * cols + c;
+  uint8_t byte = codes[e / 2];
+  int nib = (e % 2) ? (byte >> 4) : (byte & 15);
+  double v = (double)orc_e2m1_value(nib & 7) * (double)orc_e4m3_decode(bs[r * (cols / 16) + c / 16]);
+  return (nib & 8) ? -v : v;
+}
+
+int orc_nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_bs, float a_gs,
+                   const uint8_t* b_codes, const uint8_t* b_bs, float b_gs,
+                   int64_t m, int64_t n, int64_t k, double* d) {
+  if (m < 0 || n < 0 || k <= 0 || k % 32) return -1;
+  float alpha = a_gs * b_gs;               /* binary32, as the GEMM's scale */
+  for (int64_t i = 0; i < m; ++i)
+    for (int64_t j = 0; j < n; ++j) {
+      double acc = 0.0;
+      for (int64_t q = 0; q < k; ++q)
+        acc += nvfp4_value(a_codes, a_bs, k, i, q) * nvfp4_value(b_codes, b_bs, k, j, q);
+      d[i * n + j] = (double)alpha * acc;
+    }
+  return 0;
+}

@@ -126,6 +126,28 @@ int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,
                               const int64_t* seg_r, int32_t n_seg_r, uint16_t* y,
                               uint32_t* mask, uint8_t* codes_t, uint64_t* stats);
 
+/* ---- block scales for tensor cores, and the NVFP4 GEMM that uses them ----
+ *
+ * Block-scaled tensor-core GEMMs (cuBLASLt scale mode VEC16_UE4M3; NVIDIA's
+ * cuBLAS documentation, "1D block scaling factors layout") take the E4M3
+ * block scales of an operand [rows, cols] in tiles of 128 rows x 4 scale
+ * columns (64 elements of the inner dimension), 512 bytes per tile, tiles
+ * ordered along the scale columns first.  Inside a tile the scale of
+ * (row r, scale column c) is byte 16 * (r mod 32) + 4 * (r div 32) + c.
+ * Rows are padded to a multiple of 128 and scale columns to a multiple of 4
+ * with zero bytes. */
+int64_t orc_mma_scales_bytes(int64_t rows, int64_t cols);
+int orc_mma_scales(const uint8_t* bs, int64_t rows, int64_t cols, uint8_t* out);
+
+/* The NVFP4 GEMM a rollout engine runs on these operands:
+ *   d [m, n] = fl32(a_gs * b_gs) * sum_k A[i, k] * B[j, k]
+ * with A [m, k] and B [n, k] given as codes + row-major block scales (one
+ * global scale each), element value = E2M1(code) * E4M3(bs) and the sum taken
+ * in double (each product has at most 14 significant bits). */
+int orc_nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_bs, float a_gs,
+                   const uint8_t* b_codes, const uint8_t* b_bs, float b_gs,
+                   int64_t m, int64_t n, int64_t k, double* d);
+
 #ifdef __cplusplus
 }
 #endif

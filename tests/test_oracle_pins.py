@@ -723,3 +723,71 @@ def test_ste_backward_against_numpy_unpackbits(orc):
     grad = np.full((1, 64), 0x3F80, np.uint16)             # all ones
     gi = orc.ste_backward(grad, mask)
     assert gi[0, 35] == 0 and np.all(np.delete(gi[0], 35) == 0x3F80)
+
+
+# ---------------------------------------------------------------------------
+# tensor-core block-scale layout and the NVFP4 GEMM (the consumer of the
+# rollout codes); the layout is NVIDIA's documented interface, not the
+# article's, and is pinned against the hardware library by the GPU GEMM test
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (130, 80), (256, 64), (129, 2048), (300, 96)])
+def test_mma_scales_as_tile_reshape(orc, rows, cols):
+    """The tiled layout restated as a tensor reshape: pad to (R, C), split
+    rows into (tile, 4 groups of 32) and columns into (tile, 4), order the
+    axes (row tile, column tile, row in group, group, column in tile)."""
+    g = np.random.default_rng(rows * 7 + cols)
+    sc = cols // 16
+    bs = g.integers(1, 256, size=(rows, sc), dtype=np.uint8)
+    R, C = -(-rows // 128) * 128, -(-sc // 4) * 4
+    pad = np.zeros((R, C), dtype=np.uint8)
+    pad[:rows, :sc] = bs
+    want = pad.reshape(R // 128, 4, 32, C // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+    got = orc.mma_scales(bs, rows, cols)
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
+def test_mma_scales_places_every_scale_once(orc):
+    rows, cols = 200, 112
+    sc = cols // 16
+    ids = np.arange(rows * sc, dtype=np.int64)
+    # encode each position's identity in two layouts of distinct bytes
+    lo = orc.mma_scales((ids % 251 + 1).astype(np.uint8), rows, cols)
+    hi = orc.mma_scales((ids // 251 + 1).astype(np.uint8), rows, cols)
+    filled = lo != 0
+    assert filled.sum() == rows * sc and np.array_equal(filled, hi != 0)
+    key = (hi[filled].astype(np.int64) - 1) * 251 + (lo[filled].astype(np.int64) - 1)
+    assert np.array_equal(np.sort(key), ids)
+    # row 33, scale column 2 of the first tile: 16 * 1 + 4 * 1 + 2
+    assert (hi[22] - 1) * 251 + (lo[22] - 1) == 33 * sc + 2
+
+
+def _dequant(codes, bs, rows, cols):
+    nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(rows, cols)
+    val = OCP_E2M1[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+    s = torch.from_numpy(bs.copy()).view(torch.float8_e4m3fn).double().numpy()
+    return val * np.repeat(s, 16, axis=1)
+
+
+def test_nvfp4_gemm_matches_dequantised_matmul(orc):
+    g = np.random.default_rng(5)
+    m, n, k = 7, 5, 96
+    a_codes = g.integers(0, 256, size=(m, k // 2), dtype=np.uint8)
+    b_codes = g.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    a_bs = g.integers(0x20, 0x50, size=(m, k // 16), dtype=np.uint8)
+    b_bs = g.integers(0x20, 0x50, size=(n, k // 16), dtype=np.uint8)
+    a_gs, b_gs = np.float32(0.0123), np.float32(3.5e-3)
+    d = orc.nvfp4_gemm(a_codes, a_bs, a_gs, b_codes, b_bs, b_gs)
+    ref = _dequant(a_codes, a_bs, m, k) @ _dequant(b_codes, b_bs, n, k).T
+    alpha = float(np.float32(a_gs * b_gs))
+    np.testing.assert_allclose(d, alpha * ref, rtol=1e-12, atol=0)
+
+
+def test_nvfp4_gemm_closed_form(orc):
+    m, n, k = 3, 4, 64
+    ones = np.full((m, k // 2), 0x22, dtype=np.uint8)       # E2M1 1.0 in both nibbles
+    neg = np.full((n, k // 2), 0xAA, dtype=np.uint8)        # E2M1 -1.0
+    s1 = np.full((m, k // 16), 0x38, dtype=np.uint8)        # E4M3 1.0
+    s2 = np.full((n, k // 16), 0x40, dtype=np.uint8)        # E4M3 2.0
+    d = orc.nvfp4_gemm(ones, s1, 0.5, neg, s2, 0.25)
+    assert np.all(d == -k * 2.0 * 0.125)
