@@ -560,6 +560,71 @@ def run_transport(args, w):
     return 0
 
 
+def run_gemm(args):
+    """The f4 consumer: NVFP4 GEMM over rollout codes on one GPU.  Weights W
+    [N, K] are quantised once; each step quantises the activations X [M, K]
+    (rollout quantiser writing the scales in the tensor-core tile layout) and runs
+    Y = X W^T (cuBLASLt block-scaled E2M1 GEMM, bf16 out).  Prints one JSON
+    line with the GEMM's TFLOP/s against the FP4 tensor peak."""
+    from fp4_rollout_guided_gb300 import build, trace
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    h = trace.Handle(0)
+    M, N, K = args.gemm_shape
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    x = (torch.randn((M, K), generator=g, device=dev) * 2.0).to(torch.bfloat16)
+    w = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    b = h.nvfp4_operand(w)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    a = h.nvfp4_operand(x)
+
+    def step():
+        h.nvfp4_operand(x, out=a)
+        h.nvfp4_gemm(a, b, out=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    h.profile(True)
+    for _ in range(args.steps):
+        step()
+    t = h.collect()
+    h.profile(False)
+    torch.cuda.synchronize()
+    flops = 2.0 * M * N * K
+    g_n, g_ms = t["nvfp4_gemm"]
+    gemm_ms = g_ms / max(g_n, 1)
+    peak, src = load_peaks()
+    bf16_peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] \
+        if src == "measured" else 1900.0
+    fp4_peak = bf16_peak * 13.5 / 2.25      # dense FP4 / BF16 nominal ratio
+    tflops = flops / (gemm_ms * 1e-3) / 1e12
+    quant = {k: round(v[1] / max(v[0], 1), 4) for k, v in t.items() if v[0] and k != "nvfp4_gemm"}
+    line = {"metric": "NVFP4 GEMM over rollout codes (TFLOP/s)", "value": round(tflops, 1),
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "e2m1",
+            "data": "synthetic",
+            "config": {"workload": f"Y[{M},{N}] = X[{M},{K}] W[{N},{K}]^T, X quantised each step",
+                       "out": "bf16"},
+            "gemm_ms": round(gemm_ms, 4), "quantise_ms": quant,
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
+                         "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tflops / fp4_peak, 4),
+                         "peak_source": f"{src} bf16 x 6 (dense FP4 / BF16 nominal)"}}
+    print(json.dumps(line), flush=True)
+    h.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,6 +638,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse", action="store_true",
                     help="rollout side as two kernels (amax, then quantiser)")
+    ap.add_argument("--gemm", action="store_true",
+                    help="time the NVFP4 GEMM over rollout codes instead")
+    ap.add_argument("--gemm-shape", type=int, nargs=3, default=[16384, 8192, 8192],
+                    metavar=("M", "N", "K"))
     ap.add_argument("--transport", action="store_true",
                     help="time the guide record's device/host/disk round trip instead")
     args = ap.parse_args()
@@ -583,6 +652,8 @@ def main():
         return run_reference(args, w)
     if args.transport:
         return run_transport(args, w)
+    if args.gemm:
+        return run_gemm(args)
     return run_ours(args, w)
 
 

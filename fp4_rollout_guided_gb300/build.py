@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtrace_fp4.so")
-SOURCES = ["trace_kernels.cu", "trace_fakequant.cu", "trace_api.cu", "trace_noalloc.cu"]
+SOURCES = ["trace_kernels.cu", "trace_fakequant.cu", "trace_gemm.cu", "trace_api.cu",
+           "trace_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC",
@@ -55,9 +56,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: s
     os.makedirs(out, exist_ok=True)
     cc = nvcc()
 
+    # where the NVFP4 GEMM looks for cuBLASLt if the loader's search fails
+    lib_dir = os.path.realpath(os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(cc))),
+                                            "lib64"))
+
     def compile_one(src):
         obj = os.path.join(out, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, f'-DTRACE_CUDA_LIB_DIR="{lib_dir}"', *extra_flags, "-c",
+               os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -71,7 +77,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: s
         for _, log in results:
             print(log)
     tmp = lib_path + f".{os.getpid()}.tmp"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -39,6 +39,10 @@ struct trace_ctx {
   int64_t wave_bytes = int64_t(32) << 20;
   uint64_t wait_ns = 1000000000ull;
   uint32_t wait_extra = 0;
+  float* gemm_scalars = nullptr;  // alpha, beta of the NVFP4 GEMM (device)
+  void* lt = nullptr;          // cuBLASLt handle of the NVFP4 GEMM
+  void* gemm_ws = nullptr;     // its workspace
+  size_t gemm_ws_bytes = 0;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare;  // recycled timing events
 };
@@ -155,6 +159,7 @@ const char* trace_status_string(trace_status_t s) {
     case TRACE_ERR_CUDA: return "CUDA error";
     case TRACE_ERR_OOM: return "out of device memory";
     case TRACE_ERR_TIMEOUT: return "device wait timed out";
+    case TRACE_ERR_LIBRARY: return "cuBLASLt missing or refused the operation";
   }
   return "unknown status";
 }
@@ -181,9 +186,9 @@ trace_status_t trace_create(trace_handle_t* out, int device) {
   h->sm_count = prop.multiProcessorCount;
   DeviceGuard g(device);
   // one allocation: amax words, ticket (padded to 256 B), training scales,
-  // wave counters, error word (padded to 256 B)
+  // wave counters, error word (padded to 256 B), GEMM alpha/beta (256 B)
   const size_t seg_bytes = sizeof(uint32_t) * TRACE_MAX_SEGMENTS;
-  const size_t bytes = seg_bytes + 256 + seg_bytes + seg_bytes + 256;
+  const size_t bytes = seg_bytes + 256 + seg_bytes + seg_bytes + 256 + 256;
   char* base = nullptr;
   if (cudaMalloc(&base, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -202,6 +207,7 @@ trace_status_t trace_create(trace_handle_t* out, int device) {
   h->scratch.gs_train = (float*)(base + seg_bytes + 256);
   h->scratch.wave_cnt = (uint32_t*)(base + 2 * seg_bytes + 256);
   h->scratch.err = (uint32_t*)(base + 3 * seg_bytes + 256);
+  h->gemm_scalars = (float*)(base + 3 * seg_bytes + 512);
   *out = h;
   return TRACE_OK;
 }
@@ -215,6 +221,8 @@ trace_status_t trace_destroy(trace_handle_t h) {
   }
   for (auto e : h->spare) cudaEventDestroy(e);
   if (h->order) cudaEventDestroy(h->order);
+  tfp4::lt_destroy(h->lt);
+  if (h->gemm_ws) cudaFree(h->gemm_ws);
   cudaFree(h->scratch.amax_bits);
   cudaGetLastError();
   delete h;
@@ -258,16 +266,25 @@ trace_status_t trace_device_status(trace_handle_t h, trace_stream_t stream) {
   return word ? TRACE_ERR_TIMEOUT : TRACE_OK;
 }
 
-trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
-                                   int64_t cols, trace_segments_t seg, void* codes_u8,
-                                   void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
-                                   trace_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// trace_rollout_quant and trace_rollout_quant_mma: block scales row-major
+// (bs_e4m3) and/or in the tensor-core tile layout (bs_mma).
+trace_status_t rollout_quant_impl(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                  int64_t cols, trace_segments_t seg, void* codes_u8,
+                                  void* bs_e4m3, void* bs_mma, float* gs_f32,
+                                  uint32_t* guide_bits, trace_stream_t stream) {
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
   const bool empty = rows == 0;
-  for (const void* p : {x_bf16, (const void*)codes_u8, (const void*)bs_e4m3})
+  for (const void* p : {x_bf16, (const void*)codes_u8})
     if ((s = check_tensor(p, empty)) != TRACE_OK) return s;
+  if (!bs_e4m3 && !bs_mma && !empty) return TRACE_ERR_INVALID_ARG;
+  if (bs_e4m3 && (s = check_tensor(bs_e4m3, empty)) != TRACE_OK) return s;
+  if (bs_mma && (s = check_tensor(bs_mma, empty)) != TRACE_OK) return s;
   if (guide_bits && (s = check_tensor(guide_bits)) != TRACE_OK) return s;
   if (!gs_f32) return TRACE_ERR_INVALID_ARG;
   if (!aligned(gs_f32, 4)) return TRACE_ERR_ALIGNMENT;
@@ -280,15 +297,20 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
   if (e != cudaSuccess) return cuda_fail(h, e);
   const int64_t nchunks = rows * (cols / 32);
   const int32_t cpr = (int32_t)(cols / 32);
-  if (nchunks == 0) {
+  const tfp4::MmaOut mma{(uint8_t*)bs_mma, (uint32_t)((cols / 16 + 3) / 4)};
+  // the tile layout's padding (rows past a multiple of 128, scale columns
+  // past a multiple of 4) is zero
+  if (bs_mma && (rows % 128 != 0 || (cols / 16) % 4 != 0))
+    e = cudaMemsetAsync(bs_mma, 0, (size_t)tfp4::mma_scales_bytes(rows, cols), st);
+  if (e == cudaSuccess && nchunks == 0) {
     e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
-  } else {
+  } else if (e == cudaSuccess) {
     static thread_local tfp4::WaveParam wv;
     bool fused = h->fused_amax && tfp4::plan_waves(sp, (int32_t)cols, h->wave_bytes, &wv);
     if (fused) {
       e = timed(h, TRACE_KERNEL_ROLLOUT_FUSED, st, [&] {
         return tfp4::launch_rollout_fused(x_bf16, nchunks, cpr, sp, wv, h->scratch, gs_f32,
-                                          codes_u8, bs_e4m3, guide_bits, h->sm_count,
+                                          codes_u8, bs_e4m3, mma, guide_bits, h->sm_count,
                                           h->wait_extra, h->wait_ns, st);
       });
       // a device that cannot hold the whole grid at once takes the two-kernel path
@@ -299,20 +321,41 @@ trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t
       }
     }
     if (!fused) {
-    e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
-      return tfp4::launch_amax(x_bf16, nchunks, cpr, sp, h->scratch, gs_f32, h->sm_count, st);
-    });
-    if (e == cudaSuccess)
-      e = timed(h, TRACE_KERNEL_ROLLOUT_QUANT, st, [&] {
-        return tfp4::launch_rollout_quant(x_bf16, nchunks, cpr, sp, gs_f32, codes_u8, bs_e4m3,
-                                          guide_bits, h->sm_count, st);
+      e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
+        return tfp4::launch_amax(x_bf16, nchunks, cpr, sp, h->scratch, gs_f32, h->sm_count, st);
       });
+      if (e == cudaSuccess)
+        e = timed(h, TRACE_KERNEL_ROLLOUT_QUANT, st, [&] {
+          return tfp4::launch_rollout_quant(x_bf16, nchunks, cpr, sp, gs_f32, codes_u8, bs_e4m3,
+                                            mma, guide_bits, h->sm_count, st);
+        });
     }
   }
   const cudaError_t e2 = end_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (e2 != cudaSuccess) return cuda_fail(h, e2);
   return TRACE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+trace_status_t trace_rollout_quant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                   int64_t cols, trace_segments_t seg, void* codes_u8,
+                                   void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
+                                   trace_stream_t stream) {
+  if (!bs_e4m3 && rows > 0) return TRACE_ERR_INVALID_ARG;
+  return rollout_quant_impl(h, x_bf16, rows, cols, seg, codes_u8, bs_e4m3, nullptr, gs_f32,
+                            guide_bits, stream);
+}
+
+trace_status_t trace_rollout_quant_mma(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                       int64_t cols, trace_segments_t seg, void* codes_u8,
+                                       void* bs_e4m3, void* bs_mma, float* gs_f32,
+                                       uint32_t* guide_bits, trace_stream_t stream) {
+  return rollout_quant_impl(h, x_bf16, rows, cols, seg, codes_u8, bs_e4m3, bs_mma, gs_f32,
+                            guide_bits, stream);
 }
 
 trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,
@@ -573,6 +616,77 @@ extern "C" trace_status_t trace_record_import(trace_handle_t h, const void* host
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(gs, src + hd.gs_offset, sizeof(float) * hd.n_seg, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+// ---- f4: tensor-core scale layout and the NVFP4 GEMM -------------------------
+
+extern "C" size_t trace_block_scales_mma_bytes(int64_t rows, int64_t cols) {
+  if (check_shape(rows, cols) != TRACE_OK) return 0;
+  const int64_t b = tfp4::mma_scales_bytes(rows, cols);
+  return b < 0 ? 0 : (size_t)b;
+}
+
+extern "C" trace_status_t trace_block_scales_mma(trace_handle_t h, const void* bs_e4m3,
+                                                 int64_t rows, int64_t cols, void* out,
+                                                 trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  const bool empty = rows == 0;
+  if (!bs_e4m3 && !empty) return TRACE_ERR_INVALID_ARG;
+  if ((s = check_tensor(out, empty)) != TRACE_OK) return s;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaError_t e = timed(h, TRACE_KERNEL_MMA_SCALES, st, [&] {
+    return tfp4::launch_mma_scales(bs_e4m3, rows, cols, out, h->sm_count, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return TRACE_OK;
+}
+
+extern "C" trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes,
+                                           const void* a_scales_mma, const float* a_gs,
+                                           const void* b_codes, const void* b_scales_mma,
+                                           const float* b_gs, int64_t m, int64_t n, int64_t k,
+                                           void* d, trace_out_t d_type, trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || k % 32) return TRACE_ERR_INVALID_ARG;
+  if (check_shape(m, k) != TRACE_OK || check_shape(n, k) != TRACE_OK) return TRACE_ERR_INVALID_ARG;
+  if (d_type != TRACE_OUT_F32 && d_type != TRACE_OUT_BF16) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s;
+  for (const void* p : {a_codes, a_scales_mma, b_codes, b_scales_mma, (const void*)d})
+    if ((s = check_tensor(p)) != TRACE_OK) return s;
+  if (!a_gs || !b_gs) return TRACE_ERR_INVALID_ARG;
+  if (!tfp4::lt_available()) return TRACE_ERR_LIBRARY;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!h->gemm_ws) {
+    const size_t ws = size_t(32) << 20;
+    if (cudaMalloc(&h->gemm_ws, ws) != cudaSuccess) {
+      cudaGetLastError();
+      h->gemm_ws = nullptr;
+      return TRACE_ERR_OOM;
+    }
+    h->gemm_ws_bytes = ws;
+  }
+  cudaError_t e = begin_call(h, st);
+  if (e == cudaSuccess) e = tfp4::launch_gemm_scalars(a_gs, b_gs, h->gemm_scalars, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int rc = 0;
+  e = timed(h, TRACE_KERNEL_NVFP4_GEMM, st, [&] {
+    rc = tfp4::lt_nvfp4_gemm(&h->lt, h->gemm_ws, h->gemm_ws_bytes, a_codes, a_scales_mma,
+                             b_codes, b_scales_mma, h->gemm_scalars, m, n, k, d,
+                             d_type == TRACE_OUT_BF16, st);
+    return cudaSuccess;
+  });
+  const cudaError_t e2 = end_call(h, st);
+  if (rc != 0) {
+    h->last_error = rc;
+    return TRACE_ERR_LIBRARY;
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (e2 != cudaSuccess) return cuda_fail(h, e2);
   return TRACE_OK;
 }
 

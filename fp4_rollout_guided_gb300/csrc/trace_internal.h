@@ -30,9 +30,10 @@ static_assert(TRACE_MAX_SEGMENTS < 65536, "wave table holds 16-bit segment indic
 // hardware divide: q = (mulhi(n, mul) + n) >> shift with shift = ceil(log2 d)
 // and mul = floor(2^32 * (2^shift - d) / d) + 1, exact for every 32-bit n.
 struct FastDivU {
-  uint32_t mul, shift;
-  explicit FastDivU(uint32_t d) {
+  uint32_t mul, shift, d;
+  explicit FastDivU(uint32_t d_) : d(d_) {
     uint32_t l = 0;
+    const uint32_t d = d_;
     while ((1ull << l) < d) ++l;
     shift = l;
     mul = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
@@ -63,10 +64,19 @@ struct Scratch {
 cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
                         const Scratch& s, float* gs_out, int sm_count, cudaStream_t st);
 
-// a2: RTN codes, block scales, compact words (guide may be null).
+// Block scales in the tensor-core tile layout, written by the rollout
+// quantiser next to (or instead of) the row-major ones: 512-byte tiles of
+// 128 rows x 4 scale columns, tiles_per_row tiles along a row band.
+struct MmaOut {
+  uint8_t* p;  // null: not written
+  uint32_t tiles_per_row;
+};
+
+// a2: RTN codes, block scales (row-major and/or tile layout; either may be
+// null), compact words (guide may be null).
 cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
-                                 uint32_t* guide, int sm_count, cudaStream_t st);
+                                 MmaOut mma, uint32_t* guide, int sm_count, cudaStream_t st);
 
 // a1 + a2 in one cooperative launch (see k_rollout_fused).  plan_waves
 // groups whole segments into waves of about wave_bytes of x; it returns
@@ -74,7 +84,7 @@ cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
 bool plan_waves(const SegParam& seg, int32_t cols, int64_t wave_bytes, WaveParam* wv);
 cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
                                  const WaveParam& wv, const Scratch& s, float* gs_out,
-                                 void* codes, void* bs, uint32_t* guide, int sm_count,
+                                 void* codes, void* bs, MmaOut mma, uint32_t* guide, int sm_count,
                                  uint32_t wait_extra, uint64_t wait_ns, cudaStream_t st);
 
 // a3: codes -> compact words.
@@ -108,5 +118,20 @@ struct FakequantArgs {
 };
 cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
                              const SegParam& seg_r, int sm_count, cudaStream_t st);
+
+// f4: block scales in the tensor-core tile layout, and the NVFP4 GEMM
+// through cuBLASLt (trace_gemm.cu).
+int64_t mma_scales_bytes(int64_t rows, int64_t cols);
+cudaError_t launch_mma_scales(const void* bs, int64_t rows, int64_t cols, void* out, int sm_count,
+                              cudaStream_t st);
+cudaError_t launch_gemm_scalars(const float* gs_a, const float* gs_b, float* out,
+                                cudaStream_t st);
+bool lt_available();
+void lt_destroy(void* lt);
+// 0 on success, -1 if cuBLASLt cannot be loaded, else a cublasStatus_t.
+int lt_nvfp4_gemm(void** lt, void* workspace, size_t ws_bytes, const void* a_codes,
+                  const void* a_scales, const void* b_codes, const void* b_scales,
+                  const float* alpha_beta, int64_t m, int64_t n, int64_t k, void* d, int d_bf16,
+                  cudaStream_t st);
 
 }  // namespace tfp4

@@ -134,6 +134,7 @@ __device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
 // compact words, given the segment's global scale g.
 __device__ __forceinline__ void quant_chunk(const Chunk& cur, float g, uint32_t c,
                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ bs,
+                                            const MmaOut& mma, const FastDivU& cpr,
                                             uint8_t* __restrict__ guide) {
   uint32_t a[16];
 #pragma unroll
@@ -155,7 +156,15 @@ __device__ __forceinline__ void quant_chunk(const Chunk& cur, float g, uint32_t 
     out[q] = word;
   }
   st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
-  st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
+  if (bs) st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
+  if (mma.p) {
+    // chunk q of row r holds scale columns 2q, 2q + 1: adjacent bytes of the
+    // tile (r / 128, q / 2) at 16 (r mod 32) + 4 ((r / 32) mod 4) + 2 (q mod 2)
+    const uint32_t r = cpr.div(c), q = c - r * cpr.d;
+    const uint64_t off = ((uint64_t)(r >> 7) * mma.tiles_per_row + (q >> 1)) * 512u +
+                         ((r & 31u) << 4) + (((r >> 5) & 3u) << 2) + ((q & 1u) << 1);
+    st_stream_u16(mma.p + off, ps.codes);
+  }
   if (guide)
     st_stream2(guide + (uint64_t)c * 8u, compact_word(out[0], out[1]), compact_word(out[2], out[3]));
 }
@@ -164,7 +173,7 @@ __global__ void __launch_bounds__(kThreads)
     k_rollout_quant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
                     uint32_t steps_per_cta, const __grid_constant__ SegParam seg,
                     const float* __restrict__ gs, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ bs, uint8_t* __restrict__ guide) {
+                    uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide) {
   const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
   uint32_t step = blockIdx.x * steps_per_cta;
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kThreads)
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
     if (c < nchunks) {
       const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
-      quant_chunk(cur, gs[s], c, codes, bs, guide);
+      quant_chunk(cur, gs[s], c, codes, bs, mma, cpr, guide);
     }
     cur = nxt;
   }
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     k_rollout_fused(const uint8_t* __restrict__ x, uint32_t cpr_u, FastDivU cpr,
                     const __grid_constant__ SegParam seg, const __grid_constant__ WaveParam wv,
                     float* __restrict__ gs_out, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ bs, uint8_t* __restrict__ guide,
+                    uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide,
                     uint32_t* __restrict__ amax_bits, uint32_t* __restrict__ wave_cnt,
                     uint32_t* __restrict__ done, uint32_t* __restrict__ err,
                     uint32_t wait_extra, uint64_t wait_ns) {
@@ -674,7 +683,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           gseg = s;
           g = global_scale_of(ld_acquire(amax_bits + s));
         }
-        quant_chunk(ch, g, cidx, codes, bs, guide);
+        quant_chunk(ch, g, cidx, codes, bs, mma, cpr, guide);
       }
       // release the slot only once every lane's values are in use
       __syncwarp();
@@ -873,11 +882,12 @@ cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegPa
 
 cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
-                                 uint32_t* guide, int sm_count, cudaStream_t st) {
+                                 MmaOut mma, uint32_t* guide, int sm_count, cudaStream_t st) {
   const Plan p = plan_for((const void*)k_rollout_quant, steps_of(nchunks, kThreads), sm_count);
   k_rollout_quant<<<p.grid, kThreads, 0, st>>>((const uint8_t*)x, (uint32_t)nchunks,
                                                FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
-                                               (uint8_t*)codes, (uint8_t*)bs, (uint8_t*)guide);
+                                               (uint8_t*)codes, (uint8_t*)bs, mma,
+                                               (uint8_t*)guide);
   return cudaGetLastError();
 }
 
@@ -908,7 +918,7 @@ bool plan_waves(const SegParam& seg, int32_t cols, int64_t wave_bytes, WaveParam
 
 cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
                                  const WaveParam& wv, const Scratch& s, float* gs_out,
-                                 void* codes, void* bs, uint32_t* guide, int sm_count,
+                                 void* codes, void* bs, MmaOut mma, uint32_t* guide, int sm_count,
                                  uint32_t wait_extra, uint64_t wait_ns, cudaStream_t st) {
   // the shared-memory opt-in and the occupancy, once per device
   static std::mutex mu;
@@ -951,7 +961,7 @@ cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, co
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_rollout_fused, (const uint8_t*)x, (uint32_t)cpr,
                             FastDivU((uint32_t)cpr), seg, wv, gs_out, (uint8_t*)codes,
-                            (uint8_t*)bs, (uint8_t*)guide, s.amax_bits, s.wave_cnt, s.done,
+                            (uint8_t*)bs, mma, (uint8_t*)guide, s.amax_bits, s.wave_cnt, s.done,
                             s.err, wait_extra, wait_ns);
 }
 

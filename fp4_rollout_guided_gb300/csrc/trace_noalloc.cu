@@ -137,7 +137,7 @@ trace_status_t trace_rollout_quant_noalloc(const void* x_bf16, int64_t rows, int
       e = tfp4::launch_amax(x_bf16, nchunks, cpr, sp, sc, gs_f32, slot->sm_count, s);
     if (e == cudaSuccess)
       e = tfp4::launch_rollout_quant(x_bf16, nchunks, cpr, sp, gs_f32, codes_u8, bs_e4m3,
-                                     guide_bits, slot->sm_count, s);
+                                     tfp4::MmaOut{nullptr, 0}, guide_bits, slot->sm_count, s);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -25,11 +25,11 @@ from . import build as _build
 GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
 KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward",
-           "rollout_fused")
+           "rollout_fused", "mma_scales", "nvfp4_gemm")
 OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3}
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
-          4: "CUDA error", 5: "out of memory", 6: "timeout"}
+          4: "CUDA error", 5: "out of memory", 6: "timeout", 7: "cuBLASLt missing or refused"}
 
 
 class TraceError(RuntimeError):
@@ -69,6 +69,10 @@ SIGNATURES = {
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
     "trace_set_option": (INT, [P, INT, I64]),
     "trace_device_status": (INT, [P, P]),
+    "trace_rollout_quant_mma": (INT, [P, P, I64, I64, Segments, P, P, P, P, P, P]),
+    "trace_block_scales_mma_bytes": (ctypes.c_size_t, [I64, I64]),
+    "trace_block_scales_mma": (INT, [P, P, I64, I64, P, P]),
+    "trace_nvfp4_gemm": (INT, [P, P, P, P, P, P, P, I64, I64, I64, P, INT, P]),
     "trace_record_size": (ctypes.c_size_t, [INT, I64, I64, ctypes.c_int32]),
     "trace_record_export": (INT, [P, INT, P, P, P, I64, I64, Segments, P, ctypes.c_size_t, P]),
     "trace_record_info": (INT, [P, ctypes.c_size_t, P]),
@@ -327,6 +331,84 @@ class Handle:
         st = lib().trace_record_import(self._h, p, n, _ptr(g), _ptr(bs), _ptr(gs), _stream())
         self._check("trace_record_import", st)
         return g, bs, gs, seg
+
+    # -- f4: NVFP4 GEMM over rollout codes --------------------------------------------
+    def block_scales_mma(self, bs: torch.Tensor, rows: int, cols: int, out=None):
+        """Row-major block scales uint8[rows, cols/16] -> tensor-core tile layout."""
+        n = lib().trace_block_scales_mma_bytes(rows, cols)
+        if n == 0:
+            raise TraceError("trace_block_scales_mma_bytes", 1)
+        if out is None:
+            out = torch.empty(n, dtype=torch.uint8, device=self.device)
+        _need(bs, torch.uint8, (rows, cols // 16), "bs", self.device)
+        _need(out, torch.uint8, (n,), "scales_mma", self.device)
+        self._check("trace_block_scales_mma",
+                    lib().trace_block_scales_mma(self._h, _ptr(bs), rows, cols, _ptr(out),
+                                                 _stream()))
+        return out
+
+    def rollout_quant_mma(self, x: torch.Tensor, seg=None, *, row_major: bool = False,
+                          guide: bool = False, out=None):
+        """rollout_quant writing the block scales in the tensor-core tile
+        layout -> (codes, bs row-major or None, bs tile layout, gs, guide or None)."""
+        rows, cols = x.shape
+        n_seg = 1 if seg is None else len(seg) - 1
+        nb = lib().trace_block_scales_mma_bytes(rows, cols)
+        if nb == 0 and rows > 0:
+            raise TraceError("trace_block_scales_mma_bytes", 1)
+        dev = self.device
+        if out is None:
+            out = (torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
+                   torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+                   if row_major else None,
+                   torch.empty((nb,), dtype=torch.uint8, device=dev),
+                   torch.empty((n_seg,), dtype=torch.float32, device=dev),
+                   torch.empty((rows, cols // 16), dtype=torch.int32, device=dev)
+                   if guide else None)
+        codes, bs, mma, gs, gd = out
+        _need(x, torch.bfloat16, (rows, cols), "x", dev)
+        _need(codes, torch.uint8, (rows, cols // 2), "codes", dev)
+        if bs is not None:
+            _need(bs, torch.uint8, (rows, cols // 16), "bs", dev)
+        _need(mma, torch.uint8, (nb,), "bs_mma", dev)
+        _need(gs, torch.float32, (n_seg,), "gs", dev)
+        if gd is not None:
+            _need(gd, torch.int32, (rows, cols // 16), "guide", dev)
+        keep = []
+        st = lib().trace_rollout_quant_mma(self._h, _ptr(x), rows, cols,
+                                           _segments(seg, rows, keep), _ptr(codes), _ptr(bs),
+                                           _ptr(mma), _ptr(gs), _ptr(gd), _stream())
+        self._check("trace_rollout_quant_mma", st)
+        return codes, bs, mma, gs, gd
+
+    def nvfp4_operand(self, x: torch.Tensor, out=None):
+        """One NVFP4 GEMM operand from bf16 x [rows, k] through the rollout
+        quantiser (one segment, scales written in the tile layout):
+        -> (codes, scales in tile layout, gs)."""
+        o = None if out is None else (out[0], None, out[1], out[2], None)
+        codes, _, mma, gs, _ = self.rollout_quant_mma(x, None, out=o)
+        return codes, mma, gs
+
+    def nvfp4_gemm(self, a, b, out=None, out_dtype=torch.float32):
+        """a, b: (codes [rows, k/2], scales_mma, gs [1]) -> d [m, n] =
+        fl32(gs_a * gs_b) * sum_k A[i, k] B[j, k]."""
+        a_codes, a_sc, a_gs = a
+        b_codes, b_sc, b_gs = b
+        m, k = a_codes.shape[0], a_codes.shape[1] * 2
+        n = b_codes.shape[0]
+        if out is None:
+            out = torch.empty((m, n), dtype=out_dtype, device=self.device)
+        kind = {torch.float32: 0, torch.bfloat16: 1}[out.dtype]
+        _need(out, out.dtype, (m, n), "d", self.device)
+        _need(b_codes, torch.uint8, (n, k // 2), "b_codes", self.device)
+        for t, name in ((a_sc, "a_scales"), (b_sc, "b_scales"), (a_gs, "a_gs"), (b_gs, "b_gs")):
+            if t.device != self.device:
+                raise ValueError(f"{name}: expected a tensor on {self.device}")
+        self._check("trace_nvfp4_gemm",
+                    lib().trace_nvfp4_gemm(self._h, _ptr(a_codes), _ptr(a_sc), _ptr(a_gs),
+                                           _ptr(b_codes), _ptr(b_sc), _ptr(b_gs), m, n, k,
+                                           _ptr(out), kind, _stream()))
+        return out
 
     # -- options and device status -----------------------------------------------
     def set_option(self, name: str, value: int):

@@ -90,7 +90,10 @@ typedef enum {
   TRACE_ERR_UNSUPPORTED_DEVICE = 3, /* no device, or not compute capability 10.3 */
   TRACE_ERR_CUDA = 4,               /* a CUDA call failed; see trace_last_cuda_error */
   TRACE_ERR_OOM = 5,                /* device scratch could not be allocated     */
-  TRACE_ERR_TIMEOUT = 6             /* reserved: a bounded device wait gave up   */
+  TRACE_ERR_TIMEOUT = 6,            /* a bounded device wait gave up (reported by
+                                       trace_device_status)                      */
+  TRACE_ERR_LIBRARY = 7             /* cuBLASLt is missing or refused the GEMM;
+                                       its status is in trace_last_cuda_error     */
 } trace_status_t;
 
 typedef enum {
@@ -127,7 +130,9 @@ typedef enum {
   TRACE_KERNEL_FAKEQUANT = 4,
   TRACE_KERNEL_STE_BACKWARD = 5,
   TRACE_KERNEL_ROLLOUT_FUSED = 6, /* amax + quantisation in one launch */
-  TRACE_KERNEL_COUNT = 7
+  TRACE_KERNEL_MMA_SCALES = 7,    /* block scales -> tensor-core tile layout */
+  TRACE_KERNEL_NVFP4_GEMM = 8,    /* the cuBLASLt GEMM (all of its kernels)  */
+  TRACE_KERNEL_COUNT = 9
 } trace_kernel_id_t;
 
 typedef struct {
@@ -291,6 +296,53 @@ TRACE_API trace_status_t trace_record_info(const void* host_src, size_t src_byte
 TRACE_API trace_status_t trace_record_import(trace_handle_t h, const void* host_src,
                                              size_t src_bytes, void* guide, void* bs,
                                              float* gs, trace_stream_t stream);
+
+/* ---- f4: the rollout codes as operands of an NVFP4 tensor-core GEMM -----
+ * ([EN] "TRACE Core Concept": rollout runs weights and activations in
+ * NVFP4.)  Block-scaled tensor-core GEMMs take E4M3 block scales in NVIDIA's
+ * tile layout (cuBLAS documentation, "1D block scaling factors layout"):
+ * 512-byte tiles of 128 rows x 4 scale columns (64 elements), tiles running
+ * along the scale columns, the scale of (r, c) inside a tile at byte
+ * 16 * (r mod 32) + 4 * (r div 32) + c, rows padded to a multiple of 128
+ * and scale columns to a multiple of 4 with zeros. */
+
+/* Bytes of that layout for an operand [rows, cols] (0 for a bad shape). */
+TRACE_API size_t trace_block_scales_mma_bytes(int64_t rows, int64_t cols);
+
+/* Rearranges row-major block scales bs_e4m3 [rows, cols/16] (as written by
+ * trace_rollout_quant) into the tile layout at out (16-byte aligned,
+ * trace_block_scales_mma_bytes(rows, cols) bytes, padding written as 0). */
+TRACE_API trace_status_t trace_block_scales_mma(trace_handle_t h, const void* bs_e4m3,
+                                                int64_t rows, int64_t cols, void* out,
+                                                trace_stream_t stream);
+
+/* trace_rollout_quant that also (or only) writes the block scales in the
+ * tile layout: bs_e4m3 [rows, cols/16] row-major and bs_mma
+ * (trace_block_scales_mma_bytes(rows, cols) bytes, 16-byte aligned) may
+ * each be NULL, not both.  The scales are written from the quantiser's
+ * registers, so the layout costs no extra pass. */
+TRACE_API trace_status_t trace_rollout_quant_mma(trace_handle_t h, const void* x_bf16,
+                                                 int64_t rows, int64_t cols,
+                                                 trace_segments_t seg, void* codes_u8,
+                                                 void* bs_e4m3, void* bs_mma, float* gs_f32,
+                                                 uint32_t* guide_bits, trace_stream_t stream);
+
+typedef enum { TRACE_OUT_F32 = 0, TRACE_OUT_BF16 = 1 } trace_out_t;
+
+/* NVFP4 GEMM over rollout codes: d [m, n] (row-major) =
+ *   fl32(a_gs[0] * b_gs[0]) * sum_k A[i, k] * B[j, k],
+ * A [m, k] and B [n, k] given as codes ([rows, k/2], element 2i in the low
+ * nibble) and block scales in the tile layout, a_gs / b_gs device pointers
+ * to one global scale each (a single segment per operand).  The
+ * contraction is cuBLASLt's block-scaled E2M1 GEMM with FP32 accumulation,
+ * loaded at the first call; a handle keeps its cuBLASLt handle and a
+ * 32 MiB workspace (allocated at that call).  k must be a multiple of 32.
+ * Returns TRACE_ERR_LIBRARY if cuBLASLt is missing or refuses the shape. */
+TRACE_API trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes,
+                                          const void* a_scales_mma, const float* a_gs,
+                                          const void* b_codes, const void* b_scales_mma,
+                                          const float* b_gs, int64_t m, int64_t n, int64_t k,
+                                          void* d, trace_out_t d_type, trace_stream_t stream);
 
 /* Rollout-side quantisation without a handle and without any device
  * allocation.  The paper has no counterpart: this is a deployment variant of

@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(7):
+    for code in range(8):
         s = lib.trace_status_string(code)
         assert isinstance(s, bytes) and s
     assert lib.trace_status_string(99) == b"unknown status"
@@ -155,3 +155,19 @@ def test_record_calls_without_handle(lib):
 def test_options_and_device_status_without_handle(lib):
     assert lib.trace_set_option(None, 0, 1) == 1
     assert lib.trace_device_status(None, None) == 1
+
+
+def test_mma_scale_bytes_match_the_oracle(lib):
+    import oracle
+    oracle.build()
+    for rows, cols in ((1, 32), (130, 96), (256, 64), (4097, 4096)):
+        assert lib.trace_block_scales_mma_bytes(rows, cols) == \
+            oracle._load().orc_mma_scales_bytes(rows, cols)
+    assert lib.trace_block_scales_mma_bytes(4, 48) == 0
+    assert lib.trace_block_scales_mma_bytes(-1, 32) == 0
+
+
+def test_gemm_calls_without_handle(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.trace_block_scales_mma(None, p, 4, 32, p, None) == 1
+    assert lib.trace_nvfp4_gemm(None, p, p, p, p, p, p, 16, 16, 64, p, 0, None) == 1

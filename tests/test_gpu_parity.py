@@ -506,3 +506,91 @@ def test_fused_equals_split_full_size(h, cfg):
     finally:
         h.set_option("wave_bytes", 32 << 20)
     assert h.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# f4: block scales in the tensor-core tile layout, NVFP4 GEMM over rollout
+# codes (cuBLASLt); a wrong tile layout would put wrong scales on whole
+# 16-element blocks and miss the oracle by O(1)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (130, 96), (256, 64), (300, 2048), (4097, 128)])
+def test_mma_scales_bit_exact(h, rows, cols):
+    g = torch.Generator().manual_seed(rows + cols)
+    bs = torch.randint(1, 255, (rows, cols // 16), generator=g, dtype=torch.int32).to(torch.uint8)
+    got = h.block_scales_mma(bs.to(DEV), rows, cols)
+    torch.cuda.synchronize()
+    assert_same("mma scales", got.cpu().numpy(), oracle.mma_scales(bs.numpy(), rows, cols))
+
+
+def _student_t(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    z = torch.randn(shape, generator=g)
+    chi = (torch.randn((4,) + tuple(shape), generator=g) ** 2).sum(0) / 4
+    return (2.0 * z / chi.sqrt()).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 256, 512), (128, 384, 1024), (512, 128, 256)])
+def test_nvfp4_gemm_against_oracle(h, m, n, k):
+    x = _student_t((m, k), 11 + m)
+    w = _student_t((n, k), 13 + n)
+    a = h.nvfp4_operand(x.to(DEV))
+    b = h.nvfp4_operand(w.to(DEV))
+    d = h.nvfp4_gemm(a, b)
+    d16 = h.nvfp4_gemm(a, b, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    # the operands are the oracle's, bit for bit
+    a_codes, a_bs, a_gs, _ = oracle.rollout_quant(u16(x), None)
+    b_codes, b_bs, b_gs, _ = oracle.rollout_quant(u16(w), None)
+    assert_same("A codes", a[0].cpu().numpy(), a_codes)
+    assert_same("A scales", a[1].cpu().numpy(), oracle.mma_scales(a_bs, m, k))
+    assert_same("B codes", b[0].cpu().numpy(), b_codes)
+    ref = oracle.nvfp4_gemm(a_codes, a_bs, a_gs[0], b_codes, b_bs, b_gs[0])
+    mag = oracle.nvfp4_gemm(a_codes & 0x77, a_bs, a_gs[0], b_codes & 0x77, b_bs, b_gs[0])
+    # FP32 accumulation of exact products: |err| <= k * 2^-24 * sum |terms|
+    # (plus the final scaling), a bound far below a misplaced block scale
+    err = np.abs(d.cpu().double().numpy() - ref)
+    bound = k * 2.0 ** -24 * mag + 2.0 ** -126
+    assert np.all(err <= bound), float((err / bound).max())
+    assert float(np.abs(ref).max()) > 0
+    err16 = np.abs(d16.cpu().double().numpy() - ref)
+    assert np.all(err16 <= bound + 2.0 ** -8 * np.abs(ref)), float(err16.max())
+
+
+def test_nvfp4_gemm_closed_form(h):
+    m, n, k = 128, 128, 256
+    x = torch.full((m, k), 1.5, dtype=torch.bfloat16, device=DEV)
+    w = torch.full((n, k), -2.0, dtype=torch.bfloat16, device=DEV)
+    d = h.nvfp4_gemm(h.nvfp4_operand(x), h.nvfp4_operand(w))
+    torch.cuda.synchronize()
+    # every element quantises to code 7 (6.0) with block scale 448 (E4M3 max):
+    # the sum is exactly -k * 2688^2, scaled by fl32(gs_x * gs_w), gs = amax/2688
+    gs_x = np.float32(1.5) / np.float32(2688.0)
+    gs_w = np.float32(2.0) / np.float32(2688.0)
+    want = np.float32(gs_x * gs_w) * np.float32(-k * 2688.0 * 2688.0)
+    assert torch.all(d == float(want)), (float(d[0, 0]), float(want))
+
+
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("rows,cols,seg", [(130, 96, None), (256, 64, [0, 100, 256]),
+                                           (300, 2048, [0, 1, 299, 300]), (1, 32, None),
+                                           (4097, 128, [0, 2000, 4097])])
+def test_rollout_quant_writes_tile_layout_scales(h, fused, rows, cols, seg):
+    x = rand_bf16((rows, cols), rows * 3 + cols, scale=2.0)
+    h.set_option("fused_amax", fused)
+    try:
+        codes, bs, mma, gs, gd = h.rollout_quant_mma(x.to(DEV), seg, row_major=True, guide=True)
+        # the tile layout alone, with nothing else requested
+        codes2, none_bs, mma2, _, _ = h.rollout_quant_mma(x.to(DEV), seg)
+        torch.cuda.synchronize()
+    finally:
+        h.set_option("fused_amax", 1)
+    assert none_bs is None
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(u16(x), seg)
+    assert_same("codes", codes.cpu().numpy(), o_codes)
+    assert_same("bs", bs.cpu().numpy(), o_bs)
+    assert_same("guide", u32(gd), o_guide)
+    want = oracle.mma_scales(o_bs, rows, cols)
+    assert_same("tile scales", mma.cpu().numpy(), want)
+    assert_same("tile scales alone", mma2.cpu().numpy(), want)
+    assert_same("codes alone", codes2.cpu().numpy(), o_codes)
