@@ -758,7 +758,32 @@ __device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t 
   return e2m1x2(g0, g1);
 }
 
-__global__ void __launch_bounds__(kThreads)
+#ifndef TFP4_UNPACK_V2
+#define TFP4_UNPACK_V2 1
+#endif
+
+// Eight bits (bit k = sign of element k) -> bit 3 of nibble k of a word.
+__device__ __forceinline__ uint32_t signs_to_nibbles(uint32_t s8) {
+  uint32_t t = (s8 | (s8 << 12)) & 0x000F000Fu;
+  t = (t | (t << 6)) & 0x03030303u;
+  t = (t | (t << 3)) & 0x11111111u;
+  return t << 3;
+}
+
+// Two elements of one bf16x2 word -> one byte of unsigned rollout codes
+// (the magnitudes' indices; the signs are added per eight elements).
+__device__ __forceinline__ uint32_t unpack_pair_mag(uint32_t w, float inv, uint32_t gw, int j0) {
+  const uint32_t a = w & kAbs2;
+  const F2 ax = {__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)};
+  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw, j0);
+  return e2m1x2(g.x, g.y);
+}
+
+#ifndef TFP4_UNPACK_MIN_CTAS
+#define TFP4_UNPACK_MIN_CTAS 4
+#endif
+
+__global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
     k_guide_unpack(const uint8_t* __restrict__ x, const uint8_t* __restrict__ guide,
                    const uint8_t* __restrict__ bs_r, const float* __restrict__ gs_r,
                    uint32_t nchunks, FastDivU cpr, uint32_t steps_per_cta,
@@ -768,6 +793,10 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
   StepSeg ss;
   ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
+#if TFP4_UNPACK_V2
+  __shared__ ScaleTab tab;
+  int tseg = -1;
+#endif
 
   Chunk cur, nxt;
   uint2 gcur = make_uint2(0, 0), gnxt = make_uint2(0, 0);
@@ -793,9 +822,31 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint32_t last = min(c0 + kThreads, nchunks) - 1;
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+#if TFP4_UNPACK_V2
+    // per-segment table of S and 1/S for every code (rebuilt when a uniform
+    // step enters a new segment)
+    if (uniform && ss.cur != tseg) {
+      __syncthreads();
+      tseg = ss.cur;
+      build_tab(tab, gs_r[tseg]);
+      __syncthreads();
+    }
+#endif
     if (c < nchunks) {
       const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
+#if TFP4_UNPACK_V2
+      float inv[2];
+      if (uniform) {
+        inv[0] = tab.sinv[bcur & 0x7Fu].y;
+        inv[1] = tab.sinv[(bcur >> 8) & 0x7Fu].y;
+      } else {
+        const PairScale ps = pair_scale_stored(bcur, gs_r[s]);
+        inv[0] = ps.inv[0];
+        inv[1] = ps.inv[1];
+      }
+#else
       const PairScale ps = pair_scale_stored(bcur, gs_r[s]);
+#endif
       uint32_t out[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -805,8 +856,16 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int j0 = (q & 1) * 8 + 2 * k;
+#if TFP4_UNPACK_V2
+          word |= unpack_pair_mag(cur.w[4 * q + k], inv[b], gw, j0) << (8 * k);
+#else
           word |= unpack_pair(cur.w[4 * q + k], ps.inv[b], gw, j0) << (8 * k);
+#endif
         }
+#if TFP4_UNPACK_V2
+        // the record's signs of these eight elements onto the nibbles
+        word |= signs_to_nibbles((gw >> ((q & 1) * 8)) & 0xFFu);
+#endif
         out[q] = word;
       }
       st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
