@@ -130,16 +130,61 @@ __device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
 // a2: rollout quantisation
 // ---------------------------------------------------------------------------
 
-// One chunk (two blocks) -> 16 code bytes, two block-scale codes and two
-// compact words, given the segment's global scale g.
-__device__ __forceinline__ void quant_chunk(const Chunk& cur, float g, uint32_t c,
-                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ bs,
-                                            const MmaOut& mma, const FastDivU& cpr,
-                                            uint8_t* __restrict__ guide) {
+// The two block maxima of a chunk.
+__device__ __forceinline__ void chunk_bamax(const Chunk& cur, float& b0, float& b1) {
   uint32_t a[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-  const PairScale ps = pair_scale(block_amax8(a), block_amax8(a + 8), g);
+  b0 = block_amax8(a);
+  b1 = block_amax8(a + 8);
+}
+
+// Per-segment table of 1/S for every E4M3 code (S = dec(code) * gs), built
+// by the n threads tid = 0..n-1 of a CTA or warp group.
+__device__ __forceinline__ void build_inv_tab(float* inv, float gs, int tid, int n) {
+  for (int c = tid; c < 128; c += n) {
+    float S, r;
+    real_scale((uint32_t)c, gs, S, r);
+    inv[c] = r;
+  }
+}
+
+// Block-scale codes of a chunk and their reciprocal scales, with the
+// segment's constants (den = gs * 6, rden = 1 / den) and 1/S table.
+__device__ __forceinline__ PairScale chunk_scale_tab(const Chunk& cur, float gs, float den,
+                                                     float rden, const float* inv_tab) {
+  float b0, b1;
+  chunk_bamax(cur, b0, b1);
+  PairScale ps;
+  ps.codes = pair_codes(b0, b1, gs, den, rden);
+  ps.inv[0] = inv_tab[ps.codes & 0x7Fu];
+  ps.inv[1] = inv_tab[(ps.codes >> 8) & 0x7Fu];
+  return ps;
+}
+
+// The same from the global scale alone (a step that straddles segments).
+__device__ __forceinline__ PairScale chunk_scale(const Chunk& cur, float gs) {
+  float b0, b1;
+  chunk_bamax(cur, b0, b1);
+  return pair_scale(b0, b1, gs);
+}
+
+// Per-segment constants of the rollout scale (den, rden, 1/S table).
+struct SegScale {
+  float gs, den, rden;
+  __device__ __forceinline__ void set(float g) {
+    gs = g;
+    den = __fmul_rn(g, 6.0f);
+    rden = g > 0.0f ? __frcp_rn(den) : 0.0f;
+  }
+};
+
+// One chunk (two blocks) -> 16 code bytes, two block-scale codes and two
+// compact words, given its block-scale codes and reciprocal scales.
+__device__ __forceinline__ void quant_chunk(const Chunk& cur, const PairScale& ps, uint32_t c,
+                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ bs,
+                                            const MmaOut& mma, const FastDivU& cpr,
+                                            uint8_t* __restrict__ guide) {
   uint32_t out[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -179,6 +224,9 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
   StepSeg ss;
   ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
+  __shared__ float inv_tab[128];
+  int tseg = -1;
+  SegScale sc = {0.f, 0.f, 0.f};
 
   Chunk cur, nxt;
   if (step < step_end) {
@@ -194,9 +242,18 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint32_t last = min(c0 + kThreads, nchunks) - 1;
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+    if (uniform && ss.cur != tseg) {
+      __syncthreads();
+      tseg = ss.cur;
+      sc.set(gs[tseg]);
+      build_inv_tab(inv_tab, sc.gs, threadIdx.x, kThreads);
+      __syncthreads();
+    }
     if (c < nchunks) {
-      const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
-      quant_chunk(cur, gs[s], c, codes, bs, mma, cpr, guide);
+      const PairScale ps =
+          uniform ? chunk_scale_tab(cur, sc.gs, sc.den, sc.rden, inv_tab)
+                  : chunk_scale(cur, gs[seg_advance(seg, ss.cur, cpr.div(c))]);
+      quant_chunk(cur, ps, c, codes, bs, mma, cpr, guide);
     }
     cur = nxt;
   }
@@ -208,8 +265,8 @@ __global__ void __launch_bounds__(kThreads)
 //
 // The segments are grouped into waves of whole segments small enough to stay
 // in L2 (host-planned, WaveParam, at most kWaveSegs segments each).  The
-// 256-chunk steps of the call are dealt round-robin to the CTAs, one CTA
-// per SM.  In each CTA one producer thread stages steps into shared memory
+// 256-chunk steps of each wave are split into contiguous ranges, one per
+// CTA, one CTA per SM.  In each CTA one producer thread stages steps into shared memory
 // with TMA bulk copies (cp.async.bulk, completion on mbarriers) on two
 // rings (a second thread watches the cross-CTA wave counters for it):
 //   - the amax ring streams this CTA's steps from HBM; four amax warps fold
@@ -277,13 +334,6 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
   return v;
 }
 
-// First step of wave-local steps [0, nst) that CTA b owns when steps are
-// dealt round-robin over the whole call, the wave's first step being global
-// step `base`.
-__device__ __forceinline__ uint32_t first_owned(uint32_t base, uint32_t b, uint32_t G) {
-  const uint32_t r = base % G;
-  return b >= r ? b - r : b + G - r;
-}
 
 // ---- TMA bulk copies and mbarriers -------------------------------------------
 
@@ -384,12 +434,15 @@ __device__ __forceinline__ uint32_t max2_bits(uint32_t m) {
   return (hi > lo ? hi : lo) << 16;
 }
 
-// Step cursor over the waves: the k-th owned step of wave w, dealt
-// round-robin over the whole call (global step base + k goes to CTA
-// (base + k) mod G).
+// Step cursor over the waves.  Contiguous dealing: CTA b owns the steps
+// [b nst / G, (b + 1) nst / G) of each wave of nst steps, so consecutive
+// steps of a CTA mostly stay in one segment (better when a wave holds many
+// small segments: fewer global-scale lookups).  Round-robin dealing: global
+// step base + k goes to CTA (base + k) mod G (better when a wave holds few
+// large segments: all CTAs stream neighbouring steps).  The host picks.
 struct WaveCursor {
   int w;
-  uint32_t base, k, nst, c0, c1;
+  uint32_t kend, k, nst, c0, c1, base, contig;
   __device__ __forceinline__ void enter(const SegParam& seg, const WaveParam& wv, uint32_t cpr_u,
                                         uint32_t b, uint32_t G) {
     // skip waves in which this CTA owns no step
@@ -397,18 +450,24 @@ struct WaveCursor {
       c0 = (uint32_t)seg.off[wv.seg0[w]] * cpr_u;
       c1 = (uint32_t)seg.off[wv.seg0[w + 1]] * cpr_u;
       nst = (c1 - c0 + kThreads - 1) / kThreads;
-      k = first_owned(base, b, G);
-      if (k < nst) return;
-      base += nst;
+      if (contig) {
+        k = (uint32_t)((uint64_t)b * nst / G);
+        kend = (uint32_t)((uint64_t)(b + 1) * nst / G);
+      } else {
+        const uint32_t r = base % G;
+        k = b >= r ? b - r : b + G - r;
+        kend = nst;
+        base += nst;
+      }
+      if (k < kend) return;
       ++w;
     }
   }
-  // advances to the next owned step; returns the wave it left when a wave ends
+  // advances to the next owned step, entering the next wave at a wave's end
   __device__ __forceinline__ void next(const SegParam& seg, const WaveParam& wv, uint32_t cpr_u,
                                        uint32_t b, uint32_t G) {
-    k += G;
-    if (k >= nst) {
-      base += nst;
+    k += contig ? 1u : G;
+    if (k >= kend) {
       ++w;
       enter(seg, wv, cpr_u, b, G);
     }
@@ -456,6 +515,7 @@ __device__ __forceinline__ void amax_warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(32 * kAmaxWarps) : "memory");
 }
 
+
 struct FusedSmem {
   alignas(128) uint8_t a[kSlotsA][kStepBytes];
   alignas(128) uint8_t q[kSlotsQ][kStepBytes];
@@ -475,7 +535,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide,
                     uint32_t* __restrict__ amax_bits, uint32_t* __restrict__ wave_cnt,
                     uint32_t* __restrict__ done, uint32_t* __restrict__ err,
-                    uint32_t wait_extra, uint64_t wait_ns) {
+                    uint32_t wait_extra, uint64_t wait_ns, uint32_t contig) {
   extern __shared__ uint8_t smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -504,7 +564,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (lane == 0) {
       uint64_t evict_first;
       asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
-      WaveCursor ca = {0, 0, 0, 0, 0, 0}, cq = {0, 0, 0, 0, 0, 0};
+      WaveCursor ca = {0, 0, 0, 0, 0, 0, 0, contig}, cq = {0, 0, 0, 0, 0, 0, 0, contig};
       ca.enter(seg, wv, cpr_u, b, G);
       cq.enter(seg, wv, cpr_u, b, G);
       uint32_t na = 0, nq = 0;  // copies issued into each ring
@@ -593,7 +653,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   } else if (warp < kFirstAmaxWarp + kAmaxWarps) {
     // ---- amax warps: per-segment maxima of each staged step ----
     const int t = threadIdx.x - 32 * kFirstAmaxWarp;  // 0..127
-    WaveCursor c = {0, 0, 0, 0, 0, 0};
+    WaveCursor c = {0, 0, 0, 0, 0, 0, 0, contig};
     c.enter(seg, wv, cpr_u, b, G);
     StepSeg ss;
     ss.cur = 0;
@@ -660,7 +720,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // ---- quantiser warps: one chunk of each staged step per thread ----
     const int qt = threadIdx.x - 32 * (kFirstAmaxWarp + kAmaxWarps);
     const int group = qt / (32 * kQuantWarps), t = qt % (32 * kQuantWarps);  // t: 0..255
-    WaveCursor c = {0, 0, 0, 0, 0, 0};
+    WaveCursor c = {0, 0, 0, 0, 0, 0, 0, contig};
     c.enter(seg, wv, cpr_u, b, G);
     StepSeg ss;
     ss.cur = 0;
@@ -683,7 +743,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           gseg = s;
           g = global_scale_of(ld_acquire(amax_bits + s));
         }
-        quant_chunk(ch, g, cidx, codes, bs, mma, cpr, guide);
+        quant_chunk(ch, chunk_scale(ch, g), cidx, codes, bs, mma, cpr, guide);
       }
       // release the slot only once every lane's values are in use
       __syncwarp();
@@ -1004,6 +1064,8 @@ cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, co
     occ = occ_of[dev];
   }
   if (occ < 1) return cudaErrorCooperativeLaunchTooLarge;
+  // contiguous step ranges when a wave averages three or more segments
+  const uint32_t contig = seg.n >= 3 * wv.n ? 1u : 0u;
   int64_t g = (int64_t)sm_count * occ;
   const int64_t nsteps = steps_of(nchunks, kThreads);
   if (nsteps < g) g = nsteps;
@@ -1021,7 +1083,7 @@ cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, co
   return cudaLaunchKernelEx(&cfg, k_rollout_fused, (const uint8_t*)x, (uint32_t)cpr,
                             FastDivU((uint32_t)cpr), seg, wv, gs_out, (uint8_t*)codes,
                             (uint8_t*)bs, mma, (uint8_t*)guide, s.amax_bits, s.wave_cnt, s.done,
-                            s.err, wait_extra, wait_ns);
+                            s.err, wait_extra, wait_ns, contig);
 }
 
 cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,
