@@ -594,3 +594,29 @@ def test_rollout_quant_writes_tile_layout_scales(h, fused, rows, cols, seg):
     assert_same("tile scales", mma.cpu().numpy(), want)
     assert_same("tile scales alone", mma2.cpu().numpy(), want)
     assert_same("codes alone", codes2.cpu().numpy(), o_codes)
+
+
+# ---------------------------------------------------------------------------
+# the host-streamed step (pieces of training segments on three streams)
+# equals the one-call step bit for bit
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg,min_rows", [(2, 1), (3, 1), (3, 5000), (5, 1)])
+def test_host_streamed_step_matches_one_call(h, cfg, min_rows):
+    from fp4_rollout_guided_gb300 import pipeline
+    w = synth.workload(cfg, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    g = run_everything(h, x, r, w.seg_t, w.seg_r, stats=False)
+    streamer = pipeline.HostStreamedStep(h, w.rows, w.cols, w.seg_t, w.seg_r, "compact",
+                                         min_piece_rows=min_rows)
+    x_h, r_h = x.pin_memory(), r.pin_memory()
+    outs = streamer.host_outputs()
+    for _ in range(2):
+        streamer.run(x_h, r_h, outs)
+    torch.cuda.synchronize()
+    y_h, m_h, gd_h, bs_h, gs_h = outs
+    assert_same("streamed y", u16(y_h), g["fq"]["compact"][0])
+    assert_same("streamed mask", m_h.numpy().view(np.uint32), g["fq"]["compact"][1])
+    assert_same("streamed guide", gd_h.numpy().view(np.uint32), g["guide"])
+    assert_same("streamed bs", bs_h.numpy(), g["bs"])
+    assert_same("streamed gs", gs_h.numpy().view(np.uint32), g["gs"].view(np.uint32))

@@ -119,3 +119,20 @@ def test_two_rank_gloo_plan_and_timing():
     assert gathered[0][0] == 0 and gathered[0][1] == gathered[1][0] and gathered[1][1] == 64
     assert all(r[2] == 2.5 for r in res)            # max over ranks of 1.5 and 2.5
     assert {r[3] for r in res} == {0, 1}            # weak scaling: one seed per rank
+
+
+def test_pipeline_pieces_cover_the_rows():
+    from fp4_rollout_guided_gb300 import pipeline
+    for cfg in (1, 2, 3, 4, 5):
+        w = synth.workload(cfg)
+        for min_rows in (1, 100000):
+            ps = pipeline.plan_pieces(w.seg_t, w.seg_r, min_rows)
+            assert ps[0].r0 == 0 and ps[-1].r1 == w.rows
+            assert all(p.r1 == q.r0 and p.s1 == q.s0 for p, q in zip(ps, ps[1:]))
+            assert ps[0].s0 == 0 and ps[-1].s1 == w.n_seg_r
+            for p in ps:
+                assert p.seg_r[0] == 0 and p.seg_r[-1] == p.r1 - p.r0
+                assert p.seg_t[0] == 0 and p.seg_t[-1] == p.r1 - p.r0
+                assert len(p.seg_r) == p.s1 - p.s0 + 1
+    with pytest.raises(ValueError):
+        pipeline.plan_pieces([0, 5, 10], [0, 4, 10])
