@@ -26,7 +26,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(trace_[a-z_0-9]+)\s*\(", text)))
 
 
-def test_header_declares_the_surveyed_entry_points():
+def test_header_declares_the_hot_path_entry_points():
     names = declared_functions()
     for need in ("trace_create", "trace_destroy", "trace_status_string", "trace_last_cuda_error",
                  "trace_rollout_quant", "trace_guide_pack", "trace_guide_unpack",
