@@ -620,3 +620,37 @@ def test_host_streamed_step_matches_one_call(h, cfg, min_rows):
     assert_same("streamed guide", gd_h.numpy().view(np.uint32), g["guide"])
     assert_same("streamed bs", bs_h.numpy(), g["bs"])
     assert_same("streamed gs", gs_h.numpy().view(np.uint32), g["gs"].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# seeded fuzz: random shapes, independent random segment tables (empty
+# segments included), value scales over six decades, drift from tiny to
+# unrelated, fused and split rollout paths, random wave sizes
+# ---------------------------------------------------------------------------
+
+def _random_table(rng, rows, n):
+    cuts = np.sort(rng.integers(0, rows + 1, size=n - 1)) if n > 1 else np.array([], np.int64)
+    return [0] + [int(c) for c in cuts] + [rows]
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_against_oracle(h, case):
+    rng = np.random.default_rng(1000 + case)
+    rows = int(rng.integers(1, 2500))
+    cols = int(rng.choice([32, 64, 96, 128, 160, 2048]))
+    seg_t = _random_table(rng, rows, int(rng.integers(1, 12)))
+    seg_r = _random_table(rng, rows, int(rng.integers(1, 40)))
+    scale = float(10.0 ** rng.uniform(-3, 3))
+    g = torch.Generator().manual_seed(case)
+    x = (torch.randn((rows, cols), generator=g) * scale).to(torch.bfloat16)
+    sigma = float(rng.choice([2.0 ** -10, 2.0 ** -6, 0.25, 4.0]))
+    r = (x.float() * (1 + sigma * torch.randn((rows, cols), generator=g))).to(torch.bfloat16)
+    assert torch.isfinite(r.float()).all()
+    h.set_option("fused_amax", int(rng.integers(0, 2)))
+    h.set_option("wave_bytes", int(rng.choice([4096, 1 << 16, 1 << 20, 32 << 20])))
+    try:
+        check_all(h, x, r, seg_t, seg_r, f"fuzz{case}")
+    finally:
+        h.set_option("fused_amax", 1)
+        h.set_option("wave_bytes", 32 << 20)
+    assert h.device_status() == 0
