@@ -545,6 +545,47 @@ def run_transport(args, w):
     return 0
 
 
+def run_backward(args, w):
+    """The straight-through backward (grad_in = grad_out where the STE mask
+    bit is 1) over the workload, with the mask of one guided fake
+    quantisation of its training tensor.  Prints one JSON line."""
+    from fp4_rollout_guided_gb300 import build, synth, trace
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    h = trace.Handle(0)
+    x, r = synth.make_inputs(w, dev)
+    codes, bs, gs, guide = h.rollout_quant(r, w.seg_r)
+    y, mask, _, _ = h.train_fakequant(x, w.seg_t, "compact", guide, bs, gs, w.seg_r)
+    del r, codes, guide, y
+    g = x  # any bf16 tensor of the shape serves as the incoming gradient
+    out = torch.empty_like(g)
+    for _ in range(args.warmup):
+        h.ste_backward(g, mask, out=out)
+    torch.cuda.synchronize()
+    h.profile(True)
+    for _ in range(args.steps):
+        h.ste_backward(g, mask, out=out)
+    t = h.collect()
+    h.profile(False)
+    torch.cuda.synchronize()
+    n, tot = t["ste_backward"]
+    ms = tot / max(n, 1)
+    bpe = KERNEL_BYTES["ste_backward"]
+    gbs = bpe * w.elems / (ms * 1e-3) / 1e9
+    peak, src = load_peaks()
+    line = {"metric": "STE backward GB/s (bytes in+out)", "value": round(gbs, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "elements": w.elems, "bytes_per_elem": bpe},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_source": src},
+            "gpu_launches": n}
+    print(json.dumps(line), flush=True)
+    h.close()
+    return 0
+
+
 def run_gemm(args):
     """The f4 consumer: NVFP4 GEMM over rollout codes on one GPU.  Weights W
     [N, K] are quantised once; each step quantises the activations X [M, K]
@@ -623,6 +664,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse", action="store_true",
                     help="rollout side as two kernels (amax, then quantiser)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the straight-through backward instead")
     ap.add_argument("--gemm", action="store_true",
                     help="time the NVFP4 GEMM over rollout codes instead")
     ap.add_argument("--gemm-shape", type=int, nargs=3, default=[16384, 8192, 8192],
@@ -639,6 +682,8 @@ def main():
         return run_transport(args, w)
     if args.gemm:
         return run_gemm(args)
+    if args.backward:
+        return run_backward(args, w)
     return run_ours(args, w)
 
 

@@ -939,46 +939,57 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
 // ---------------------------------------------------------------------------
 // straight-through backward: grad_in = grad_out where the mask bit is 1, +0
 // elsewhere.  One chunk (32 elements, one mask word) per thread per step;
-// each mask bit pair becomes a 0xFFFF / 0x0000 lane mask for a bf16x2 word.
+// each mask bit pair becomes a 0xFFFF / 0x0000 lane mask for a bf16x2 word
+// (a mask byte's even and odd bits are first compacted into one word).
 // ---------------------------------------------------------------------------
 
 constexpr int kSteChunks = 2;  // chunks per thread per step (bytes in flight)
 
+// Bits 0, 2, ..., 30 of x -> bits 0..15.
+__device__ __forceinline__ uint32_t compact_even16(uint32_t x) {
+  x &= 0x55555555u;
+  x = (x | (x >> 1)) & 0x33333333u;
+  x = (x | (x >> 2)) & 0x0F0F0F0Fu;
+  x = (x | (x >> 4)) & 0x00FF00FFu;
+  return (x | (x >> 8)) & 0x0000FFFFu;
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_ste_backward(const uint8_t* __restrict__ g, const uint8_t* __restrict__ mask,
                    uint32_t nchunks, uint32_t steps_per_cta, uint8_t* __restrict__ out) {
+  // a step is kSteChunks x 256 chunks; each warp instruction moves 512
+  // contiguous bytes: thread t takes 16-byte words t + 256 j of the step
+  // (eight elements, one byte of the mask)
   constexpr uint32_t kStep = kThreads * kSteChunks;
+  constexpr int kWords = 4 * kSteChunks;  // 16-byte words per thread per step
   const uint32_t nsteps = (nchunks + kStep - 1) / kStep;
+  const uint32_t nwords = nchunks * 4u;
   uint32_t step = blockIdx.x * steps_per_cta;
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
   for (; step < step_end; ++step) {
-    Chunk v[kSteChunks];
-    uint32_t m[kSteChunks];
+    uint4 v[kWords];
+    uint32_t mb[kWords];
 #pragma unroll
-    for (int k = 0; k < kSteChunks; ++k) {
-      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
-      if (c < nchunks) {
-        load_chunk(v[k], g, c);
-        unsigned int mw;
-        asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(mw) : "l"(mask + (uint64_t)c * 4u));
-        m[k] = mw;
+    for (int j = 0; j < kWords; ++j) {
+      const uint32_t u = step * kStep * 4u + j * kThreads + threadIdx.x;
+      if (u < nwords) {
+        v[j] = ld_stream(g + (uint64_t)u * 16u);
+        unsigned short b;
+        asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(b) : "l"(mask + u));
+        mb[j] = b;
       }
     }
 #pragma unroll
-    for (int k = 0; k < kSteChunks; ++k) {
-      const uint32_t c = step * kStep + k * kThreads + threadIdx.x;
-      if (c < nchunks) {
-        uint32_t o[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          // bits 2i, 2i+1 -> lane masks (0 - bit keeps all 16 lane bits)
-          const uint32_t lo = (0u - ((m[k] >> (2 * i)) & 1u)) & 0x0000FFFFu;
-          const uint32_t hi = (0u - ((m[k] >> (2 * i + 1)) & 1u)) & 0xFFFF0000u;
-          o[i] = v[k].w[i] & (lo | hi);
-        }
-        uint8_t* p = out + (uint64_t)c * 64u;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) st_stream(p + 16 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    for (int j = 0; j < kWords; ++j) {
+      const uint32_t u = step * kStep * 4u + j * kThreads + threadIdx.x;
+      if (u < nwords) {
+        // mask byte: bit 2i / 2i+1 keeps the low / high element of bf16x2 word i
+        const uint32_t P = compact_even16(mb[j]) | (compact_even16(mb[j] >> 1) << 16);
+        const uint4 w = v[j];
+        st_stream(out + (uint64_t)u * 16u, w.x & imad(P & 0x00010001u, 0xFFFFu, 0u),
+                  w.y & imad((P >> 1) & 0x00010001u, 0xFFFFu, 0u),
+                  w.z & imad((P >> 2) & 0x00010001u, 0xFFFFu, 0u),
+                  w.w & imad((P >> 3) & 0x00010001u, 0xFFFFu, 0u));
       }
     }
   }
