@@ -329,34 +329,19 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
-// The rounding constant for t in [0, 6]: 1.5 * 2^(22 + e) with 2^e the
-// binade of max(t, 1).
-__device__ __forceinline__ float magic_of(float tc) {
-  uint32_t e = __float_as_uint(tc) & 0x7F800000u;
-  e = e > 0x3F800000u ? e : 0x3F800000u;
-  return __uint_as_float(e + 0x0B400000u);
-}
-
-// The same constant for a pair of clamped values.  Two exact formulations:
-// TFP4_MAGIC_FMA = 1 builds it on the FMA pipe from two saturating
-// indicators, b1 = [tc > 2] and b2 = [tc > 4] (sat(tc * 2^30 - 2^31) is 0 for
-// tc <= 2 and 1 otherwise: the next binary32 above 2 is 2 + 2^-22), then
-// C = K * (1 + b1) * (1 + b2), K = 1.5 * 2^22; otherwise it takes the
-// exponent field with integer operations.  At tc = 2 or 4 both constants put
-// the (on-grid) value on the grid, so the boundary side does not matter.
-#ifndef TFP4_MAGIC_FMA
-#define TFP4_MAGIC_FMA 1
-#endif
+// The rounding constant for a pair of clamped values t in [0, 6]:
+// C = 1.5 * 2^(22 + e) with 2^e the binade of max(t, 1), built on the FMA
+// pipe from two saturating indicators, b1 = [t > 2] and b2 = [t > 4]
+// (sat(t * 2^30 - 2^31) is 0 for t <= 2 and 1 otherwise: the next binary32
+// above 2 is 2 + 2^-22), then C = K * (1 + b1) * (1 + b2), K = 1.5 * 2^22.
+// At t = 2 or 4 either constant puts the (on-grid) value on the grid, so
+// the boundary side does not matter.
 __device__ __forceinline__ F2 magic_pair(F2 tc) {
-#if TFP4_MAGIC_FMA
   const float k = 0x1.8p22f;
   const F2 b1 = {fma_sat(tc.x, 0x1p30f, -0x1p31f), fma_sat(tc.y, 0x1p30f, -0x1p31f)};
   const F2 b2 = {fma_sat(tc.x, 0x1p30f, -0x1p32f), fma_sat(tc.y, 0x1p30f, -0x1p32f)};
   const F2 m1 = fma2_rn(b1, splat(k), splat(k));
   return fma2_rn(b2, m1, m1);
-#else
-  return F2{magic_of(tc.x), magic_of(tc.y)};
-#endif
 }
 
 // Rollout-frame decode of a pair from the compact record: for each element

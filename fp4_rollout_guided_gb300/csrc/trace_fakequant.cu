@@ -56,12 +56,6 @@ __device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) 
   k.h_g[3] += d1 >= 3;
 }
 
-__device__ __forceinline__ float fmul_sat(float a, float b) {
-  float d;
-  asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-
 // Training side of one pair of elements.  ax holds |x|; St holds the
 // training scale carrying each element's sign, vr the rollout's
 // reconstructed values with the rollout's signs, so the candidates
@@ -94,21 +88,11 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2&
   const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
   const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
   const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
-#if TFP4_SELECT_IMAD
-  // lo = key >> 31 as the high word of key * 2; v_lo - v_hi on bit patterns
-  const uint32_t k0 = __float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x);
-  const uint32_t k1 = __float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y);
-  const uint32_t lo0 = __umulhi(k0, 2u), lo1 = __umulhi(k1, 2u);
-  const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
-  ym = F2{__uint_as_float(imad(lo0, imad(h0, 0xFFFFFFFFu, __float_as_uint(vlo.x)), h0)),
-          __uint_as_float(imad(lo1, imad(h1, 0xFFFFFFFFu, __float_as_uint(vlo.y)), h1))};
-#else
   const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
   const uint32_t lo1 = (__float_as_uint(diff1) + __float_as_uint(sn.y) + ~__float_as_uint(sz.y)) >> 31;
   const uint32_t h0 = __float_as_uint(vhi.x), h1 = __float_as_uint(vhi.y);
   ym = F2{__uint_as_float(imad(lo0, __float_as_uint(vlo.x) - h0, h0)),
           __uint_as_float(imad(lo1, __float_as_uint(vlo.y) - h1, h1))};
-#endif
   if (WANT_G) {
     gsel = F2{lo0 ? glo.x : ghi.x, lo1 ? glo.y : ghi.y};
     grtn = F2{sn.x != sz.x ? ghi.x : glo.x, sn.y != sz.y ? ghi.y : glo.y};
@@ -124,9 +108,6 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
-#ifndef TFP4_FQ_PREFETCH
-#define TFP4_FQ_PREFETCH 0
-#endif
 #ifndef TFP4_FQ_MIN_CTAS
 #define TFP4_FQ_MIN_CTAS 4
 #endif
@@ -157,9 +138,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   int tseg = -1, rseg = -1;                 // segments the tables hold
   float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
 
-  Chunk cur, nxt;
-  uint4 gcur = make_uint4(0, 0, 0, 0), gnxt = make_uint4(0, 0, 0, 0);
-  uint32_t bcur = 0, bnxt = 0;
+  // the next step's inputs are loaded at the end of the current step
+  Chunk cur;
+  uint4 gcur = make_uint4(0, 0, 0, 0);
+  uint32_t bcur = 0;
   if (step < step_end) {
     const uint32_t c = step * kThreads + threadIdx.x;
     if (c < nchunks) {
@@ -177,20 +159,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   for (; step < step_end; ++step) {
     const uint32_t c0 = step * kThreads;
     const uint32_t c = c0 + threadIdx.x;
-    if (TFP4_FQ_PREFETCH && step + 1 < step_end) {
-      const uint32_t cn = c + kThreads;
-      if (cn < nchunks) {
-        load_chunk(nxt, x, cn);
-        if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint2 v = ld_stream2(guide + (uint64_t)cn * 8u);
-          gnxt.x = v.x;
-          gnxt.y = v.y;
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          gnxt = ld_stream(guide + (uint64_t)cn * 16u);
-        }
-        if (GUIDED) bnxt = ld_stream_u16(bs_r + (uint64_t)cn * 2u);
-      }
-    }
     const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kThreads, nchunks) - 1);
     const bool uni_t = st.update(seg_t, r0, r1);
     const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
@@ -313,11 +281,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       if (STATS) n_done += 32;
     }
-    if (TFP4_FQ_PREFETCH) {
-      cur = nxt;
-      gcur = gnxt;
-      bcur = bnxt;
-    } else if (step + 1 < step_end) {
+    if (step + 1 < step_end) {
       const uint32_t cn = c + kThreads;
       if (cn < nchunks) {
         load_chunk(cur, x, cn);

@@ -806,22 +806,6 @@ __global__ void __launch_bounds__(kThreads)
 // a4: guide unpack
 // ---------------------------------------------------------------------------
 
-// Two elements of one bf16x2 word -> one byte of rollout codes.  j0 is the
-// index of the word's low element inside its 16-element block.
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, float inv, uint32_t gw, int j0) {
-  const uint32_t a = w & kAbs2;
-  const F2 ax = {__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)};
-  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw, j0);
-  // signs from the record; E2M1 conversion of exact grid points gives indices
-  const float g0 = __uint_as_float(__float_as_uint(g.x) | ((gw << (31 - j0)) & 0x80000000u));
-  const float g1 = __uint_as_float(__float_as_uint(g.y) | ((gw << (30 - j0)) & 0x80000000u));
-  return e2m1x2(g0, g1);
-}
-
-#ifndef TFP4_UNPACK_V2
-#define TFP4_UNPACK_V2 1
-#endif
-
 // Eight bits (bit k = sign of element k) -> bit 3 of nibble k of a word.
 __device__ __forceinline__ uint32_t signs_to_nibbles(uint32_t s8) {
   uint32_t t = (s8 | (s8 << 12)) & 0x000F000Fu;
@@ -853,10 +837,8 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
   StepSeg ss;
   ss.cur = step < step_end ? seg_search(seg, cpr.div(step * kThreads)) : 0;
-#if TFP4_UNPACK_V2
   __shared__ ScaleTab tab;
   int tseg = -1;
-#endif
 
   Chunk cur, nxt;
   uint2 gcur = make_uint2(0, 0), gnxt = make_uint2(0, 0);
@@ -882,7 +864,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
     }
     const uint32_t last = min(c0 + kThreads, nchunks) - 1;
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
-#if TFP4_UNPACK_V2
     // per-segment table of S and 1/S for every code (rebuilt when a uniform
     // step enters a new segment)
     if (uniform && ss.cur != tseg) {
@@ -891,10 +872,8 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
       build_tab(tab, gs_r[tseg]);
       __syncthreads();
     }
-#endif
     if (c < nchunks) {
       const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(c));
-#if TFP4_UNPACK_V2
       float inv[2];
       if (uniform) {
         inv[0] = tab.sinv[bcur & 0x7Fu].y;
@@ -904,9 +883,6 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
         inv[0] = ps.inv[0];
         inv[1] = ps.inv[1];
       }
-#else
-      const PairScale ps = pair_scale_stored(bcur, gs_r[s]);
-#endif
       uint32_t out[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -916,16 +892,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int j0 = (q & 1) * 8 + 2 * k;
-#if TFP4_UNPACK_V2
           word |= unpack_pair_mag(cur.w[4 * q + k], inv[b], gw, j0) << (8 * k);
-#else
-          word |= unpack_pair(cur.w[4 * q + k], ps.inv[b], gw, j0) << (8 * k);
-#endif
         }
-#if TFP4_UNPACK_V2
         // the record's signs of these eight elements onto the nibbles
         word |= signs_to_nibbles((gw >> ((q & 1) * 8)) & 0xFFu);
-#endif
         out[q] = word;
       }
       st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
