@@ -420,7 +420,9 @@ def measure_e2e(args, h, w, x, r, step, dev, bpe, outs):
     in_bytes = x.numel() * 2 * 2
     out_bytes = sum(t.numel() * t.element_size() for t in (y, mask, guide, bs, gs))
     need = in_bytes + out_bytes
-    avail = mem_available_bytes()
+    # every local rank pins its own buffers: share the host's free memory
+    local_ranks = max(1, int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+    avail = mem_available_bytes() // local_ranks
     scope = "whole workload"
     rows = w.rows
     if avail and need * 1.6 > avail:
