@@ -148,7 +148,7 @@ cudaError_t end_call(trace_ctx* h, cudaStream_t st) { return cudaEventRecord(h->
 
 extern "C" {
 
-int trace_version(void) { return 100; }
+int trace_version(void) { return 200; }
 
 const char* trace_status_string(trace_status_t s) {
   switch (s) {

@@ -30,8 +30,9 @@
  *   - Packed E2M1 codes: uint8 [rows, cols/2]; element 2i is the low nibble
  *     of byte i; nibble = (sign << 3) | m, m = 0..7 indexes the magnitudes
  *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  The sign is always the input's sign.
- *   - Block scales: uint8 E4M3 codes [rows, cols/16], plain row-major (not
- *     the tensor-core scale-factor swizzle).
+ *   - Block scales: uint8 E4M3 codes [rows, cols/16], plain row-major;
+ *     trace_rollout_quant_mma can also write them in the tensor-core tile
+ *     layout of block-scaled GEMMs.
  *   - Global scales: float [n_seg], gs = amax / (6 * 448) per segment.
  *   - Compact guide: uint32 [rows, cols/16]; for element j of a block, bit j
  *     is its sign and bit 16+j the low bit of its E2M1 index (the single
@@ -45,8 +46,11 @@
  *     over all rows.  The table travels in the kernel's parameter block; the
  *     caller may free it as soon as the call returns.
  *   - All tensor pointers are caller-owned DEVICE pointers on the handle's
- *     device, 16-byte aligned.  Calls enqueue work on `stream` and never
- *     synchronise the host.  Global scales never leave the device.
+ *     device, 16-byte aligned (host pointers only where a call says so).
+ *     Calls enqueue work on `stream` and never synchronise the host, except
+ *     trace_device_status and the first trace_nvfp4_gemm of a handle (which
+ *     allocates its workspace).  Global scales never leave the device unless
+ *     a record is exported.
  *   - Errors: argument errors return before anything is enqueued.  A failed
  *     launch returns TRACE_ERR_CUDA and the raw cudaError_t is available from
  *     trace_last_cuda_error.  Nothing aborts and no exception crosses the ABI.

@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
         s = lib.trace_status_string(code)
         assert isinstance(s, bytes) and s
     assert lib.trace_status_string(99) == b"unknown status"
-    assert lib.trace_version() == 100
+    assert lib.trace_version() == 200
 
 
 def test_create_rejects_bad_devices(lib):
