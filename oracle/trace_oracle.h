@@ -139,7 +139,8 @@ int orc_train_fakequant_given(const uint16_t* x, int64_t rows, int64_t cols,
 int64_t orc_mma_scales_bytes(int64_t rows, int64_t cols);
 int orc_mma_scales(const uint8_t* bs, int64_t rows, int64_t cols, uint8_t* out);
 
-/* The NVFP4 GEMM a rollout engine runs on these operands:
+/* The NVFP4 GEMM a rollout engine runs on these operands ([EN] "TRACE Core
+ * Concept": rollout runs weights and activations in FP4):
  *   d [m, n] = fl32(a_gs * b_gs) * sum_k A[i, k] * B[j, k]
  * with A [m, k] and B [n, k] given as codes + row-major block scales (one
  * global scale each), element value = E2M1(code) * E4M3(bs) and the sum taken
