@@ -64,18 +64,23 @@ def step_bytes_per_elem(guide: str) -> float:
 # capture (profiles/), valid only for the kernel source it was taken on; a
 # changed source reports traffic as null.
 MEASURED_TRAFFIC = {
-    "fakequant_compact": {"bytes_per_elem": 4.456, "kernels_sha1": "e9436299ae6f"},
+    "fakequant_compact": {"bytes_per_elem": 4.456, "kernels_sha1": "8507a7862b2e"},
 }
 
 
 def kernels_sha1() -> str:
-    """Hash of the fake-quant kernel's sources (its own file and the shared
-    device helpers): a change there makes the stored traffic stale."""
+    """Hash of the fake-quant kernel's code (its own file and the shared
+    device helpers, comments and blank space removed): a code change there
+    makes the stored traffic stale, a comment edit does not."""
     import hashlib
+    import re
     h = hashlib.sha1()
     for name in ("trace_fakequant.cu", "trace_device.cuh"):
-        with open(os.path.join(ROOT, "fp4_rollout_guided_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fp4_rollout_guided_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

@@ -8,14 +8,17 @@
 // a compact record of mantissa bit + scale sets the direction) and the
 // worked example of section "Why Does FP4 Rollout 'Break' RL Training?".
 //
-// Work decomposition.  Every kernel streams a flat sequence of 32-element
+// Work decomposition.  Kernels stream a flat sequence of 32-element
 // "chunks" (two 16-element NVFP4 blocks, one STE mask word).  Rows hold
 // cols/32 chunks, so a chunk never straddles a row or a segment.  A CTA of
 // 256 threads handles a "step" of 256 consecutive chunks (16 KiB of bf16),
 // one chunk per thread, and owns a contiguous range of steps; the next
 // step's loads are issued before the current step is computed.  Segments
 // are looked up once per step (uniform across the CTA); only a step that
-// straddles a segment boundary resolves segments per thread.
+// straddles a segment boundary resolves segments per thread.  Two kernels
+// differ: the fused rollout kernel stages steps with TMA bulk copies and
+// splits its CTA into copy, amax and quantiser warps, and the STE backward
+// gives each thread one 16-byte word of eight elements per instruction.
 //
 // Arithmetic.  All of it is binary32 with round-to-nearest-even (explicit
 // __f*_rn intrinsics so nothing is contracted into an FMA; no flush to zero),
