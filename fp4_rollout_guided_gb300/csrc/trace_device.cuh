@@ -147,6 +147,20 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Lane-wise max(|a|, |b|) of two bf16 pairs.  The lanes' sign bits come
+// out as the xor of the inputs' signs, so every consumer masks them; the
+// magnitudes are exact for finite inputs.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// A pair of bf16 lanes (signs ignored) -> binary32 bits of the larger |lane|.
+__device__ __forceinline__ uint32_t absmax_lanes_bits(uint32_t m) {
+  return (absmax_bf16x2(m, m >> 16) << 16) & 0x7FFF0000u;
+}
+
 // Eight words of masked bf16 magnitudes -> binary32 bits of their maximum.
 __device__ __forceinline__ float block_amax8(const uint32_t* a) {
   uint32_t m0 = max_u16x2(a[0], a[1]);
@@ -329,6 +343,22 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   asm("{ .reg .b8 b; cvt.rn.satfinite.e2m1x2.f32 b, %1, %2; cvt.u32.u8 %0, b; }"
       : "=r"(r)
       : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four pairs -> one word of eight E2M1 nibbles, pair k in byte k (first
+// value of a pair in the low nibble).
+__device__ __forceinline__ uint32_t e2m1x8(F2 p0, F2 p1, F2 p2, F2 p3) {
+  uint32_t r;
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3}; }"
+      : "=r"(r)
+      : "f"(p0.x), "f"(p0.y), "f"(p1.x), "f"(p1.y), "f"(p2.x), "f"(p2.y), "f"(p3.x),
+        "f"(p3.y));
   return r;
 }
 

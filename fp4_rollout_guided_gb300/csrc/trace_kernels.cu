@@ -7,6 +7,11 @@
 // Sources: "Alibaba Qwen Proposes TRACE for 5.4x Faster FP4 RL Rollouts",
 // section "TRACE Core Concept", and the worked example of section "Why
 // Does FP4 Rollout 'Break' RL Training?".
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "trace_device.cuh"
 
 namespace tfp4 {
@@ -110,33 +115,44 @@ __global__ void __launch_bounds__(kThreads)
 // compact word helpers
 // ---------------------------------------------------------------------------
 
-// Eight nibbles -> the 8 bits found at nibble bit `b` (0: index LSB, 3: sign).
-__device__ __forceinline__ uint32_t gather_nibble_bit(uint32_t w, int b) {
-  uint32_t v = (w >> b) & 0x11111111u;
-  v = (v | (v >> 3)) & 0x03030303u;
-  v = (v | (v >> 6)) & 0x000F000Fu;
-  v = (v | (v >> 12)) & 0x000000FFu;
-  return v;
+// Bits b (0: index LSB, 3: sign) of the eight nibbles of w, nibble i at bit
+// 24 + i (bits 0..23 hold junk).  After the mask and fold, nibbles 2j and
+// 2j + 1 sit in bits s, s + 1 of byte j (s = 0 for the LSB, 3 for the sign);
+// the multiply adds byte j shifted by 24 - s - 6j, which lands the pair at
+// bits 24 + 2j.  The other partial products fall in disjoint bit pairs below
+// bit 24 or above bit 31, so no carry reaches the result.
+__device__ __forceinline__ uint32_t nibble_lsb_hi(uint32_t w) {
+  const uint32_t v = w & 0x11111111u;
+  return ((v | (v >> 3)) & 0x03030303u) * 0x01041040u;  // 2^24 + 2^18 + 2^12 + 2^6
+}
+__device__ __forceinline__ uint32_t nibble_sign_hi(uint32_t w) {
+  const uint32_t v = w & 0x88888888u;
+  return ((v | (v >> 3)) & 0x18181818u) * 0x00208208u;  // 2^21 + 2^15 + 2^9 + 2^3
 }
 
 // Sixteen nibbles (one block, two words) -> compact word.
 __device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
-  const uint32_t sgn = gather_nibble_bit(c0, 3) | (gather_nibble_bit(c1, 3) << 8);
-  const uint32_t lsb = gather_nibble_bit(c0, 0) | (gather_nibble_bit(c1, 0) << 8);
-  return sgn | (lsb << 16);
+  const uint32_t sgn = __byte_perm(nibble_sign_hi(c0), nibble_sign_hi(c1), 0x0073u);
+  const uint32_t lsb = __byte_perm(nibble_lsb_hi(c0), nibble_lsb_hi(c1), 0x0073u);
+  return __byte_perm(sgn, lsb, 0x5410u);
 }
 
 // ---------------------------------------------------------------------------
 // a2: rollout quantisation
 // ---------------------------------------------------------------------------
 
-// The two block maxima of a chunk.
+// The two block maxima of a chunk (bf16 abs-max on the raw words).
 __device__ __forceinline__ void chunk_bamax(const Chunk& cur, float& b0, float& b1) {
-  uint32_t a[16];
+  uint32_t m[2];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-  b0 = block_amax8(a);
-  b1 = block_amax8(a + 8);
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t* w = cur.w + 8 * b;
+    const uint32_t m01 = absmax_bf16x2(absmax_bf16x2(w[0], w[1]), absmax_bf16x2(w[2], w[3]));
+    const uint32_t m23 = absmax_bf16x2(absmax_bf16x2(w[4], w[5]), absmax_bf16x2(w[6], w[7]));
+    m[b] = absmax_lanes_bits(absmax_bf16x2(m01, m23));
+  }
+  b0 = __uint_as_float(m[0]);
+  b1 = __uint_as_float(m[1]);
 }
 
 // Per-segment table of 1/S for every E4M3 code (S = dec(code) * gs), built
@@ -188,17 +204,15 @@ __device__ __forceinline__ void quant_chunk(const Chunk& cur, const PairScale& p
   uint32_t out[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float inv = ps.inv[q >> 1];
-    uint32_t word = 0;
+    // signed x * inv keeps the input's sign in the nibble
+    const F2 inv = splat(ps.inv[q >> 1]);
+    F2 t[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w = cur.w[4 * q + k];
-      // signed x * inv keeps the input's sign in the nibble
-      const uint32_t b = e2m1x2(__fmul_rn(__uint_as_float(w << 16), inv),
-                                __fmul_rn(__uint_as_float(w & 0xFFFF0000u), inv));
-      word |= b << (8 * k);
+      t[k] = mul2_rn(F2{__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)}, inv);
     }
-    out[q] = word;
+    out[q] = e2m1x8(t[0], t[1], t[2], t[3]);
   }
   st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
   if (bs) st_stream_u16(bs + (uint64_t)c * 2u, ps.codes);
@@ -354,17 +368,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 }
 
 // Non-blocking: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -425,14 +428,12 @@ __device__ __forceinline__ void smem_chunk(Chunk& c, const uint8_t* step, uint32
 }
 
 // Packed |bf16| maximum of a 16-byte word (eight elements).
+// Lane-wise |max| of a 16-byte word (lane signs junk: see absmax_bf16x2).
 __device__ __forceinline__ uint32_t quad_max2(uint4 v) {
-  return max_u16x2(max_u16x2(v.x & kAbs2, v.y & kAbs2), max_u16x2(v.z & kAbs2, v.w & kAbs2));
+  return absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
 }
 
-__device__ __forceinline__ uint32_t max2_bits(uint32_t m) {
-  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
-  return (hi > lo ? hi : lo) << 16;
-}
+__device__ __forceinline__ uint32_t max2_bits(uint32_t m) { return absmax_lanes_bits(m); }
 
 // Step cursor over the waves.  Contiguous dealing: CTA b owns the steps
 // [b nst / G, (b + 1) nst / G) of each wave of nst steps, so consecutive
@@ -497,8 +498,9 @@ constexpr int kAmaxWarps = TFP4_FUSED_AMAX_WARPS;
 // Quantiser warps come in groups of eight (one chunk per thread of a step);
 // group g takes the staged steps n with n mod kQuantGroups == g.
 constexpr int kQuantGroups = TFP4_FUSED_QUANT_GROUPS, kQuantWarps = 8;
-// warp 0: copies; warp 1: watches the wave counters; then the amax warps
-// and the quantiser groups
+// warp 0: the amax stream's copies; warp 1: watches the wave counters and
+// issues the quantiser stream's copies; then the amax warps and the
+// quantiser groups
 constexpr int kFirstAmaxWarp = 2;
 constexpr int kFusedThreads = 32 * (kFirstAmaxWarp + kAmaxWarps + kQuantGroups * kQuantWarps);
 static_assert(kSlotsQ % kQuantGroups == 0, "each quantiser group owns whole slots");
@@ -516,17 +518,61 @@ __device__ __forceinline__ void amax_warps_sync() {
 }
 
 
+// Slots are 1024-byte aligned: a 128-byte-swizzled TMA tile repeats its
+// pattern every eight 128-byte rows.
 struct FusedSmem {
-  alignas(128) uint8_t a[kSlotsA][kStepBytes];
-  alignas(128) uint8_t q[kSlotsQ][kStepBytes];
+  alignas(1024) uint8_t a[kSlotsA][kStepBytes];
+  alignas(1024) uint8_t q[kSlotsQ][kStepBytes];
   uint64_t full_a[kSlotsA], empty_a[kSlotsA], full_q[kSlotsQ], empty_q[kSlotsQ];
   uint32_t smax[kWaveSegs];
 };
-constexpr size_t kFusedSmemBytes = sizeof(FusedSmem) + 128;
+constexpr size_t kFusedSmemBytes = sizeof(FusedSmem) + 1024;
+static_assert(kFusedSmemBytes <= 227 * 1024, "one CTA per SM within the shared-memory opt-in");
 
-#ifndef TFP4_FUSED_EVICT_FIRST
-#define TFP4_FUSED_EVICT_FIRST 1
-#endif
+// Swizzled staging (cols % 64 == 0): x is a 2-D tensor of 128-byte rows (two
+// chunks each) and a step is one box of 128 rows, copied with 128-byte
+// swizzle: 16-byte unit u of row r lands at unit u ^ (r mod 8).  Chunk i of
+// the step is half i % 2 of row i / 2, so a quarter-warp reading one unit of
+// eight consecutive chunks touches eight different bank groups.
+__device__ __forceinline__ void smem_chunk_swz(Chunk& c, const uint8_t* step, uint32_t i) {
+  const uint32_t row = i >> 1, h = (i & 1u) << 2, sw = row & 7u;
+  const uint8_t* base = step + row * 128u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + (((h + q) ^ sw) << 4));
+    c.w[4 * q + 0] = v.x;
+    c.w[4 * q + 1] = v.y;
+    c.w[4 * q + 2] = v.z;
+    c.w[4 * q + 3] = v.w;
+  }
+}
+
+// Step-local chunk held by physical 16-byte unit u of a swizzled step.
+__device__ __forceinline__ uint32_t swz_unit_chunk(uint32_t u) {
+  const uint32_t row = u >> 3;
+  return 2u * row + ((((u & 7u) ^ (row & 7u))) >> 2);
+}
+
+__device__ __forceinline__ void tensor_load_2d(void* dst, const CUtensorMap* map, uint32_t c0,
+                                               uint32_t c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tensor_load_2d_hint(void* dst, const CUtensorMap* map,
+                                                    uint32_t c0, uint32_t c1, uint64_t* bar,
+                                                    uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+      "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
     k_rollout_fused(const uint8_t* __restrict__ x, uint32_t cpr_u, FastDivU cpr,
@@ -535,17 +581,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide,
                     uint32_t* __restrict__ amax_bits, uint32_t* __restrict__ wave_cnt,
                     uint32_t* __restrict__ done, uint32_t* __restrict__ err,
-                    uint32_t wait_extra, uint64_t wait_ns, uint32_t contig) {
+                    uint32_t wait_extra, uint64_t wait_ns, uint32_t contig,
+                    const __grid_constant__ CUtensorMap xmap, uint32_t swz) {
   extern __shared__ uint8_t smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ int is_last;
-  __shared__ int ready_w;  // highest wave whose maxima are complete in every CTA
+  // the quantiser producer's position: the wave it waits for or streams, and
+  // its copies issued (the amax producer's lead bound)
+  __shared__ int q_wave, q_issued;
   const uint32_t G = gridDim.x, b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    ready_w = -1;
+    q_wave = 0;
+    q_issued = 0;
     for (int i = 0; i < kSlotsA; ++i) {
       mbar_init(&sm.full_a[i], 1);
       mbar_init(&sm.empty_a[i], kAmaxWarps);
@@ -560,85 +610,67 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __syncthreads();
 
   if (warp == 0) {
-    // ---- producer: one thread issues every copy ----
+    // ---- amax producer: streams the CTA's steps from HBM into ring A ----
     if (lane == 0) {
-      uint64_t evict_first;
-      asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
-      WaveCursor ca = {0, 0, 0, 0, 0, 0, 0, contig}, cq = {0, 0, 0, 0, 0, 0, 0, contig};
+      WaveCursor ca = {0, 0, 0, 0, 0, 0, 0, contig};
       ca.enter(seg, wv, cpr_u, b, G);
-      cq.enter(seg, wv, cpr_u, b, G);
-      uint32_t na = 0, nq = 0;  // copies issued into each ring
+      uint32_t na = 0;  // copies issued
       bool broken = false;
-      uint64_t idle_since = 0;
-      while (ca.w < wv.n || cq.w < wv.n) {
-        bool progress = false;
-        // quantiser stream: wave cq.w once every CTA has counted it
-        if (cq.w < wv.n) {
-          const uint32_t slot = nq % kSlotsQ, use = nq / kSlotsQ;
-          if ((broken || ld_acquire_cta(&ready_w) >= cq.w) &&
-              (use == 0 || mbar_test(&sm.empty_q[slot], (use - 1) & 1u))) {
-            // the consumers' generic-proxy reads of the slot come before
-            // the copy's async-proxy writes
-            fence_proxy_async();
-            const uint32_t bytes = cq.step_chunks() * 64u;
-            mbar_expect_tx(&sm.full_q[slot], bytes);
-#if TFP4_FUSED_EVICT_FIRST
-            bulk_load_hint(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes,
-                           &sm.full_q[slot], evict_first);
-#else
-            bulk_load(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes, &sm.full_q[slot]);
-#endif
-            ++nq;
-            cq.next(seg, wv, cpr_u, b, G);
-            progress = true;
+      while (ca.w < wv.n) {
+        // through the quantiser producer's wave, then at most kLeadSteps
+        // steps ahead of its issued copies
+        if (!broken) {
+          const uint64_t t0 = global_ns();
+          uint32_t nap = 32;
+          for (uint32_t it = 0;; ++it) {
+            if (ca.w <= ld_acquire_cta(&q_wave) ||
+                na - (uint32_t)ld_acquire_cta(&q_issued) < kLeadSteps)
+              break;
+            __nanosleep(nap);
+            nap = nap < 1024u ? 2u * nap : nap;
+            if ((it & 7u) == 7u && (global_ns() - t0 > wait_ns || it > (1u << 22))) {
+              atomicOr(err, 1u);
+              broken = true;
+              break;
+            }
           }
         }
-        // amax stream: through the quantiser's wave, then at most
-        // kLeadSteps ahead of it
-        if (ca.w < wv.n && (ca.w <= cq.w || na - nq < kLeadSteps)) {
-          const uint32_t slot = na % kSlotsA, use = na / kSlotsA;
-          if (use == 0 || mbar_test(&sm.empty_a[slot], (use - 1) & 1u)) {
-            fence_proxy_async();
-            const uint32_t bytes = ca.step_chunks() * 64u;
-            mbar_expect_tx(&sm.full_a[slot], bytes);
-            bulk_load(sm.a[slot], x + (uint64_t)ca.step_chunk() * 64u, bytes, &sm.full_a[slot]);
-            ++na;
-            ca.next(seg, wv, cpr_u, b, G);
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_since = 0;
+        const uint32_t slot = na % kSlotsA, use = na / kSlotsA;
+        if (use > 0 && !mbar_wait(&sm.empty_a[slot], (use - 1) & 1u, wait_ns, err)) break;
+        // the consumers' generic-proxy reads of the slot come before the
+        // copy's async-proxy writes
+        fence_proxy_async();
+        if (swz) {
+          mbar_expect_tx(&sm.full_a[slot], kStepBytes);
+          tensor_load_2d(sm.a[slot], &xmap, 0u, ca.step_chunk() >> 1, &sm.full_a[slot]);
         } else {
-          const uint64_t t = global_ns();
-          if (idle_since == 0) {
-            idle_since = t;
-          } else if (t - idle_since > wait_ns) {
-            // nothing moved for the whole limit: give up the cross-CTA waits
-            if (broken) break;
-            atomicOr(err, 1u);
-            broken = true;
-            idle_since = 0;
-          }
-          __nanosleep(32);
+          const uint32_t bytes = ca.step_chunks() * 64u;
+          mbar_expect_tx(&sm.full_a[slot], bytes);
+          bulk_load(sm.a[slot], x + (uint64_t)ca.step_chunk() * 64u, bytes, &sm.full_a[slot]);
         }
+        ++na;
+        ca.next(seg, wv, cpr_u, b, G);
       }
       // no copy may still be in flight when the CTA exits
       for (uint32_t i = 0; i < kSlotsA && i < na; ++i) {
         const uint32_t n = na - 1 - i, slot = n % kSlotsA;
         mbar_wait(&sm.full_a[slot], (n / kSlotsA) & 1u, wait_ns, err);
       }
-      for (uint32_t i = 0; i < kSlotsQ && i < nq; ++i) {
-        const uint32_t n = nq - 1 - i, slot = n % kSlotsQ;
-        mbar_wait(&sm.full_q[slot], (n / kSlotsQ) & 1u, wait_ns, err);
-      }
     }
   } else if (warp == 1) {
-    // ---- watcher: publishes, wave by wave, that every CTA has counted it,
-    // and writes the global scales of the waves w with w mod G == b ----
+    // ---- quantiser producer: wave by wave, waits until every CTA has
+    // counted the wave's maxima, writes the global scales of the waves w
+    // with w mod G == b, then re-reads the CTA's steps of the wave (now from
+    // L2) into ring Q ----
     if (lane == 0) {
-      bool broken = false;
-      for (int w = 0; w < wv.n; ++w) {
+      uint64_t evict_first;
+      asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+      WaveCursor cq = {0, 0, 0, 0, 0, 0, 0, contig};
+      cq.enter(seg, wv, cpr_u, b, G);
+      uint32_t nq = 0;  // copies issued
+      bool broken = false, dead = false;
+      for (int w = 0; w < wv.n && !dead; ++w) {
+        st_release_cta(&q_wave, w);
         if (!broken && !wait_at_least(wave_cnt + w, G + wait_extra, wait_ns)) {
           atomicOr(err, 1u);
           broken = true;
@@ -647,7 +679,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int s = wv.seg0[w]; s < wv.seg0[w + 1]; ++s)
             gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
         }
-        st_release_cta(&ready_w, w);
+        for (; cq.w == w; cq.next(seg, wv, cpr_u, b, G)) {
+          const uint32_t slot = nq % kSlotsQ, use = nq / kSlotsQ;
+          if (use > 0 && !mbar_wait(&sm.empty_q[slot], (use - 1) & 1u, wait_ns, err)) {
+            dead = true;
+            break;
+          }
+          fence_proxy_async();
+          if (swz) {
+            mbar_expect_tx(&sm.full_q[slot], kStepBytes);
+            tensor_load_2d_hint(sm.q[slot], &xmap, 0u, cq.step_chunk() >> 1, &sm.full_q[slot],
+                                evict_first);
+          } else {
+            const uint32_t bytes = cq.step_chunks() * 64u;
+            mbar_expect_tx(&sm.full_q[slot], bytes);
+            bulk_load_hint(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes,
+                           &sm.full_q[slot], evict_first);
+          }
+          ++nq;
+          st_release_cta(&q_issued, (int)nq);
+        }
+      }
+      // lift the amax producer's lead bound before leaving
+      st_release_cta(&q_wave, wv.n);
+      for (uint32_t i = 0; i < kSlotsQ && i < nq; ++i) {
+        const uint32_t n = nq - 1 - i, slot = n % kSlotsQ;
+        mbar_wait(&sm.full_q[slot], (n / kSlotsQ) & 1u, wait_ns, err);
       }
     }
   } else if (warp < kFirstAmaxWarp + kAmaxWarps) {
@@ -677,10 +734,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t nu = cnt * 4;
       if (uniform) {
         uint32_t m = 0;
+        if (swz) {
+          // a swizzled step holds whole rows; skip units of chunks past cnt
 #pragma unroll
-        for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
-          const uint32_t u = t + 32 * kAmaxWarps * j;
-          if (u < nu) m = max_u16x2(m, quad_max2(st4[u]));
+          for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
+            const uint32_t u = t + 32 * kAmaxWarps * j;
+            if (swz_unit_chunk(u) < cnt) m = absmax_bf16x2(m, quad_max2(st4[u]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
+            const uint32_t u = t + 32 * kAmaxWarps * j;
+            if (u < nu) m = absmax_bf16x2(m, quad_max2(st4[u]));
+          }
         }
         const uint32_t mw = __reduce_max_sync(0xFFFFFFFFu, max2_bits(m));
         if (lane == 0) {
@@ -690,9 +756,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       } else {
         for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
           const uint32_t u = t + 32 * kAmaxWarps * j;
-          if (u < nu) {
+          const uint32_t lc = swz ? swz_unit_chunk(u) : u / 4;  // step-local chunk
+          if (lc < cnt) {
             const uint32_t m = max2_bits(quad_max2(st4[u]));
-            if (m) atomicMax(&sm.smax[seg_advance(seg, ss.cur, cpr.div(cs + u / 4)) - s0], m);
+            if (m) atomicMax(&sm.smax[seg_advance(seg, ss.cur, cpr.div(cs + lc)) - s0], m);
           }
         }
         __syncwarp();
@@ -736,7 +803,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const bool uniform = ss.update(seg, cpr.div(cs), cpr.div(cs + cnt - 1));
       if ((uint32_t)t < cnt) {
         Chunk ch;
-        smem_chunk(ch, sm.q[slot], t);
+        if (swz)
+          smem_chunk_swz(ch, sm.q[slot], t);
+        else
+          smem_chunk(ch, sm.q[slot], t);
         const uint32_t cidx = cs + t;
         const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(cidx));
         if (s != gseg) {
@@ -814,13 +884,12 @@ __device__ __forceinline__ uint32_t signs_to_nibbles(uint32_t s8) {
   return t << 3;
 }
 
-// Two elements of one bf16x2 word -> one byte of unsigned rollout codes
-// (the magnitudes' indices; the signs are added per eight elements).
-__device__ __forceinline__ uint32_t unpack_pair_mag(uint32_t w, float inv, uint32_t gw, int j0) {
+// Two elements of one bf16x2 word -> their E2M1 magnitudes in the rollout
+// frame (the signs are added per eight elements).
+__device__ __forceinline__ F2 unpack_pair_mag(uint32_t w, float inv, uint32_t gw, int j0) {
   const uint32_t a = w & kAbs2;
   const F2 ax = {__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)};
-  const F2 g = decode_pair(mul2_rn(ax, splat(inv)), gw, j0);
-  return e2m1x2(g.x, g.y);
+  return decode_pair(mul2_rn(ax, splat(inv)), gw, j0);
 }
 
 #ifndef TFP4_UNPACK_MIN_CTAS
@@ -888,15 +957,12 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
       for (int q = 0; q < 4; ++q) {
         const int b = q >> 1;
         const uint32_t gw = b ? gcur.y : gcur.x;
-        uint32_t word = 0;
+        F2 g[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j0 = (q & 1) * 8 + 2 * k;
-          word |= unpack_pair_mag(cur.w[4 * q + k], inv[b], gw, j0) << (8 * k);
-        }
+        for (int k = 0; k < 4; ++k)
+          g[k] = unpack_pair_mag(cur.w[4 * q + k], inv[b], gw, (q & 1) * 8 + 2 * k);
         // the record's signs of these eight elements onto the nibbles
-        word |= signs_to_nibbles((gw >> ((q & 1) * 8)) & 0xFFu);
-        out[q] = word;
+        out[q] = e2m1x8(g[0], g[1], g[2], g[3]) | signs_to_nibbles((gw >> ((q & 1) * 8)) & 0xFFu);
       }
       st_stream(codes + (uint64_t)c * 16u, out[0], out[1], out[2], out[3]);
     }
@@ -1016,6 +1082,46 @@ bool plan_waves(const SegParam& seg, int32_t cols, int64_t wave_bytes, WaveParam
   return true;
 }
 
+#ifndef TFP4_FUSED_SWIZZLE
+#define TFP4_FUSED_SWIZZLE 1
+#endif
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// x viewed as rows of 128 bytes (two chunks), one box = one step of 128 rows,
+// copied with 128-byte swizzle.  Returns false (bulk copies are used) when the
+// rows of x hold an odd number of chunks or the encoder is unavailable.
+bool encode_step_map(const void* x, int64_t nchunks, int32_t cpr, CUtensorMap* map) {
+  if (!TFP4_FUSED_SWIZZLE || (cpr & 1) || (nchunks & 1) || nchunks < 2 ||
+      (reinterpret_cast<uintptr_t>(x) & 15u))
+    return false;
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dim[2] = {64, (cuuint64_t)(nchunks / 2)};
+  const cuuint64_t stride[1] = {128};
+  const cuuint32_t box[2] = {64, kStepBytes / 128};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(x), dim, stride, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, const SegParam& seg,
                                  const WaveParam& wv, const Scratch& s, float* gs_out,
                                  void* codes, void* bs, MmaOut mma, uint32_t* guide, int sm_count,
@@ -1061,10 +1167,13 @@ cudaError_t launch_rollout_fused(const void* x, int64_t nchunks, int32_t cpr, co
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  CUtensorMap xmap;
+  memset(&xmap, 0, sizeof(xmap));
+  const uint32_t swz = encode_step_map(x, nchunks, cpr, &xmap) ? 1u : 0u;
   return cudaLaunchKernelEx(&cfg, k_rollout_fused, (const uint8_t*)x, (uint32_t)cpr,
                             FastDivU((uint32_t)cpr), seg, wv, gs_out, (uint8_t*)codes,
                             (uint8_t*)bs, mma, (uint8_t*)guide, s.amax_bits, s.wave_cnt, s.done,
-                            s.err, wait_extra, wait_ns, contig);
+                            s.err, wait_extra, wait_ns, contig, xmap, swz);
 }
 
 cudaError_t launch_guide_pack(const void* codes, int64_t nchunks, uint32_t* guide,
