@@ -328,7 +328,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 
 // One thread: true once *p >= target; false after limit_ns (or a fixed
 // number of polls, whichever comes first).
+// Bounded waits read the global timer only once a wait has lasted a while:
+// a timer read costs far more than a poll, and on a producer's path it would
+// be paid on every step.
 __device__ __noinline__ bool wait_at_least(const uint32_t* p, uint32_t target, uint64_t limit_ns) {
+  for (uint32_t it = 0; it < 64; ++it) {
+    if (ld_acquire(p) >= target) return true;
+    __nanosleep(32);
+  }
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 22); ++it) {
     if (ld_acquire(p) >= target) return true;
@@ -380,9 +387,10 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for a phase; false (and *err set) once limit_ns has passed.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                       uint32_t* err) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                            uint32_t* err) {
+  for (uint32_t it = 0; it < 16; ++it)
+    if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 22); ++it) {
     if (mbar_try(bar, parity)) return true;
@@ -390,6 +398,11 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t 
   }
   atomicOr(err, 2u);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                          uint32_t* err) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, limit_ns, err);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -620,18 +633,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // through the quantiser producer's wave, then at most kLeadSteps
         // steps ahead of its issued copies
         if (!broken) {
-          const uint64_t t0 = global_ns();
+          uint64_t t0 = 0;
           uint32_t nap = 32;
-          for (uint32_t it = 0;; ++it) {
+          for (uint32_t it = 1;; ++it) {
             if (ca.w <= ld_acquire_cta(&q_wave) ||
                 na - (uint32_t)ld_acquire_cta(&q_issued) < kLeadSteps)
               break;
             __nanosleep(nap);
             nap = nap < 1024u ? 2u * nap : nap;
-            if ((it & 7u) == 7u && (global_ns() - t0 > wait_ns || it > (1u << 22))) {
-              atomicOr(err, 1u);
-              broken = true;
-              break;
+            if ((it & 7u) == 0u) {
+              const uint64_t t = global_ns();
+              if (t0 == 0) {
+                t0 = t;
+              } else if (t - t0 > wait_ns || it > (1u << 22)) {
+                atomicOr(err, 1u);
+                broken = true;
+                break;
+              }
             }
           }
         }
