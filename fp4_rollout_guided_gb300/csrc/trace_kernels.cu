@@ -752,7 +752,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t nu = cnt * 4;
       if (uniform) {
         uint32_t m = 0;
-        if (swz) {
+        if (cnt == (uint32_t)kThreads) {
+          // a full step: every unit holds data
+#pragma unroll
+          for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j)
+            m = absmax_bf16x2(m, quad_max2(st4[t + 32 * kAmaxWarps * j]));
+        } else if (swz) {
           // a swizzled step holds whole rows; skip units of chunks past cnt
 #pragma unroll
           for (int j = 0; j < kStepBytes / 16 / (32 * kAmaxWarps); ++j) {
