@@ -451,6 +451,33 @@ def test_rollout_fused_uneven_and_empty_segments(h):
     assert h.device_status() == 0
 
 
+@pytest.mark.parametrize("cols", [64, 96, 2048])
+@pytest.mark.parametrize("offset_bytes", [16, 48, 112])
+def test_rollout_input_16_byte_aligned_only(h, cols, offset_bytes):
+    # x starts 16 bytes past a 128-byte boundary or more: the fused kernel's
+    # tensor-map staging (cols % 64 == 0) and its bulk copies (cols = 96)
+    # must not depend on more than the documented 16-byte alignment
+    rows = 700
+    x = rand_bf16((rows, cols), 73 + cols, scale=2.0)
+    seg = [0, 5, 333, 640, rows]
+    buf = torch.empty(rows * cols + 64, dtype=torch.bfloat16, device=DEV)
+    off = offset_bytes // 2
+    xv = buf[off:off + rows * cols].view(rows, cols)
+    assert xv.data_ptr() % 16 == 0 and xv.data_ptr() % 128 != 0
+    xv.copy_(x.to(DEV))
+    ran = _launched(h, lambda: h.rollout_quant(xv, seg))
+    assert ran == {"rollout_fused": 1}, ran
+    codes, bs, gs, guide = h.rollout_quant(xv, seg)
+    torch.cuda.synchronize()
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(u16(x), seg)
+    label = f"offset {offset_bytes} cols {cols}"
+    assert_same(f"{label} codes", codes.cpu().numpy(), o_codes)
+    assert_same(f"{label} bs", bs.cpu().numpy(), o_bs)
+    assert_same(f"{label} gs", gs.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    assert_same(f"{label} guide", u32(guide), o_guide)
+    assert h.device_status() == 0
+
+
 def test_rollout_large_segment_takes_two_kernels(h):
     # one segment of 41 MiB of x is more than a fused wave may hold
     rows, cols = 10496, 2048
