@@ -448,12 +448,21 @@ __device__ __forceinline__ uint32_t quad_max2(uint4 v) {
 
 __device__ __forceinline__ uint32_t max2_bits(uint32_t m) { return absmax_lanes_bits(m); }
 
-// Step cursor over the waves.  Contiguous dealing: CTA b owns the steps
-// [b nst / G, (b + 1) nst / G) of each wave of nst steps, so consecutive
-// steps of a CTA mostly stay in one segment (better when a wave holds many
-// small segments: fewer global-scale lookups).  Round-robin dealing: global
-// step base + k goes to CTA (base + k) mod G (better when a wave holds few
-// large segments: all CTAs stream neighbouring steps).  The host picks.
+// Number of CTAs c < bb in the cyclic range [o, o + R) of 0..G-1 (R < G).
+__device__ __forceinline__ uint32_t extras_before(uint32_t bb, uint32_t o, uint32_t R,
+                                                  uint32_t G) {
+  if (o + R <= G) return min(max(bb, o), o + R) - o;
+  return (bb > o ? bb - o : 0u) + min(bb, o + R - G);
+}
+
+// Step cursor over the waves.  Contiguous dealing: CTA b owns one
+// contiguous range of each wave's nst steps, floor(nst / G) or one more, so
+// consecutive steps of a CTA mostly stay in one segment (better when a wave
+// holds many small segments: fewer global-scale lookups); which CTAs take
+// the remainder rotates from wave to wave, since a wave completes only when
+// its last CTA does.  Round-robin dealing: global step base + k goes to CTA
+// (base + k) mod G (better when a wave holds few large segments: all CTAs
+// stream neighbouring steps).  The host picks.
 struct WaveCursor {
   int w;
   uint32_t kend, k, nst, c0, c1, base, contig;
@@ -465,8 +474,13 @@ struct WaveCursor {
       c1 = (uint32_t)seg.off[wv.seg0[w + 1]] * cpr_u;
       nst = (c1 - c0 + kThreads - 1) / kThreads;
       if (contig) {
-        k = (uint32_t)((uint64_t)b * nst / G);
-        kend = (uint32_t)((uint64_t)(b + 1) * nst / G);
+        // q steps each, and one more for the R CTAs of the cyclic range
+        // [o, o + R) with o = w R mod G: the CTAs that take the extra step
+        // change from wave to wave, so none falls a step behind per wave
+        const uint32_t q = nst / G, R = nst - q * G;
+        const uint32_t o = (uint32_t)(((uint64_t)w * R) % G);
+        k = b * q + extras_before(b, o, R, G);
+        kend = (b + 1) * q + extras_before(b + 1, o, R, G);
       } else {
         const uint32_t r = base % G;
         k = b >= r ? b - r : b + G - r;
@@ -493,10 +507,10 @@ struct WaveCursor {
 };
 
 #ifndef TFP4_FUSED_SLOTS_A
-#define TFP4_FUSED_SLOTS_A 6
+#define TFP4_FUSED_SLOTS_A 5
 #endif
 #ifndef TFP4_FUSED_SLOTS_Q
-#define TFP4_FUSED_SLOTS_Q 6
+#define TFP4_FUSED_SLOTS_Q 8
 #endif
 #ifndef TFP4_FUSED_AMAX_WARPS
 #define TFP4_FUSED_AMAX_WARPS 4
