@@ -148,7 +148,7 @@ cudaError_t end_call(trace_ctx* h, cudaStream_t st) { return cudaEventRecord(h->
 
 extern "C" {
 
-int trace_version(void) { return 200; }
+int trace_version(void) { return 300; }
 
 const char* trace_status_string(trace_status_t s) {
   switch (s) {
@@ -403,13 +403,18 @@ trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
   return TRACE_OK;
 }
 
-trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
-                                     int64_t cols, trace_segments_t seg_t,
-                                     trace_guide_kind_t kind, const void* guide,
-                                     const void* bs_r, const float* gs_r,
-                                     trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
-                                     void* codes_t_u8, trace_stats_t* stats_dev,
-                                     trace_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The training-side fake quantiser; gs_t == nullptr: the call first runs the
+// amax pass over x into the handle's training scales.
+trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t rows, int64_t cols,
+                                    trace_segments_t seg_t, const float* gs_t,
+                                    trace_guide_kind_t kind, const void* guide, const void* bs_r,
+                                    const float* gs_r, trace_segments_t seg_r, void* y_bf16,
+                                    uint32_t* ste_mask, void* codes_t_u8,
+                                    trace_stats_t* stats_dev, trace_stream_t stream) {
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
@@ -421,6 +426,7 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
   if (ste_mask && (s = check_tensor(ste_mask)) != TRACE_OK) return s;
   if (codes_t_u8 && (s = check_tensor(codes_t_u8)) != TRACE_OK) return s;
   if (stats_dev && !aligned(stats_dev, 8)) return TRACE_ERR_ALIGNMENT;
+  if (gs_t && !aligned(gs_t, 4)) return TRACE_ERR_ALIGNMENT;
   static thread_local tfp4::SegParam spt, spr;
   if ((s = make_segments(seg_t, rows, &spt)) != TRACE_OK) return s;
   if (kind != TRACE_GUIDE_NONE) {
@@ -442,16 +448,19 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
   cudaError_t e = begin_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   const int32_t cpr = (int32_t)(cols / 32);
-  e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
-    return tfp4::launch_amax(x_bf16, nchunks, cpr, spt, h->scratch, h->scratch.gs_train,
-                             h->sm_count, st);
-  });
+  if (!gs_t) {
+    e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
+      return tfp4::launch_amax(x_bf16, nchunks, cpr, spt, h->scratch, h->scratch.gs_train,
+                               h->sm_count, st);
+    });
+    gs_t = h->scratch.gs_train;
+  }
   if (e == cudaSuccess) {
     tfp4::FakequantArgs a;
     a.x = x_bf16;
     a.nchunks = nchunks;
     a.cpr = cpr;
-    a.gs_t = h->scratch.gs_train;
+    a.gs_t = gs_t;
     a.kind = (int)kind;
     a.guide = guide;
     a.bs_r = bs_r;
@@ -462,6 +471,63 @@ trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64
     a.stats = stats_dev;
     e = timed(h, TRACE_KERNEL_FAKEQUANT, st,
               [&] { return tfp4::launch_fakequant(a, spt, spr, h->sm_count, st); });
+  }
+  const cudaError_t e2 = end_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (e2 != cudaSuccess) return cuda_fail(h, e2);
+  return TRACE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                     int64_t cols, trace_segments_t seg_t,
+                                     trace_guide_kind_t kind, const void* guide,
+                                     const void* bs_r, const float* gs_r,
+                                     trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
+                                     void* codes_t_u8, trace_stats_t* stats_dev,
+                                     trace_stream_t stream) {
+  return train_fakequant_impl(h, x_bf16, rows, cols, seg_t, nullptr, kind, guide, bs_r, gs_r,
+                              seg_r, y_bf16, ste_mask, codes_t_u8, stats_dev, stream);
+}
+
+trace_status_t trace_train_fakequant_gs(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                        int64_t cols, trace_segments_t seg_t, const float* gs_t,
+                                        trace_guide_kind_t kind, const void* guide,
+                                        const void* bs_r, const float* gs_r,
+                                        trace_segments_t seg_r, void* y_bf16,
+                                        uint32_t* ste_mask, void* codes_t_u8,
+                                        trace_stats_t* stats_dev, trace_stream_t stream) {
+  if (!gs_t) return TRACE_ERR_INVALID_ARG;
+  return train_fakequant_impl(h, x_bf16, rows, cols, seg_t, gs_t, kind, guide, bs_r, gs_r,
+                              seg_r, y_bf16, ste_mask, codes_t_u8, stats_dev, stream);
+}
+
+trace_status_t trace_segment_amax(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                  int64_t cols, trace_segments_t seg, float* gs_f32,
+                                  trace_stream_t stream) {
+  if (!h) return TRACE_ERR_INVALID_ARG;
+  trace_status_t s = check_shape(rows, cols);
+  if (s != TRACE_OK) return s;
+  if ((s = check_tensor(x_bf16, rows == 0)) != TRACE_OK) return s;
+  if (!gs_f32) return TRACE_ERR_INVALID_ARG;
+  if (!aligned(gs_f32, 4)) return TRACE_ERR_ALIGNMENT;
+  static thread_local tfp4::SegParam sp;
+  if ((s = make_segments(seg, rows, &sp)) != TRACE_OK) return s;
+  DeviceGuard g(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = begin_call(h, st);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  const int64_t nchunks = rows * (cols / 32);
+  if (nchunks == 0) {
+    e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
+  } else {
+    e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
+      return tfp4::launch_amax(x_bf16, nchunks, (int32_t)(cols / 32), sp, h->scratch, gs_f32,
+                               h->sm_count, st);
+    });
   }
   const cudaError_t e2 = end_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);

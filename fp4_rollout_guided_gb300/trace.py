@@ -66,6 +66,9 @@ SIGNATURES = {
     "trace_guide_unpack": (INT, [P, P, P, P, P, Segments, I64, I64, P, P]),
     "trace_train_fakequant": (INT, [P, P, I64, I64, Segments, INT, P, P, P, Segments, P, P,
                                     P, P, P]),
+    "trace_train_fakequant_gs": (INT, [P, P, I64, I64, Segments, P, INT, P, P, P, Segments, P,
+                                       P, P, P, P]),
+    "trace_segment_amax": (INT, [P, P, I64, I64, Segments, P, P]),
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
     "trace_set_option": (INT, [P, INT, I64]),
     "trace_device_status": (INT, [P, P]),
@@ -234,11 +237,27 @@ class Handle:
         return out
 
     # -- a5 + a6 -----------------------------------------------------------------
+    def segment_amax(self, x: torch.Tensor, seg=None, out: Optional[torch.Tensor] = None):
+        """-> gs float32[n_seg]: per-segment amax / 2688 (one streaming kernel)."""
+        rows, cols = x.shape
+        _need(x, torch.bfloat16, (rows, cols), "x", self.device)
+        keep = []
+        sg = _segments(seg, rows, keep)
+        if out is None:
+            out = torch.empty(sg.n_seg, dtype=torch.float32, device=self.device)
+        _need(out, torch.float32, (sg.n_seg,), "gs", self.device)
+        self._check("trace_segment_amax",
+                    lib().trace_segment_amax(self._h, _ptr(x), rows, cols, sg, _ptr(out),
+                                             _stream()))
+        return out
+
     def train_fakequant(self, x, seg_t=None, kind="none", guide=None, bs_r=None, gs_r=None,
                         seg_r=None, *, mask: bool = True, codes: bool = False,
-                        stats: Optional[torch.Tensor] = None, out=None):
+                        stats: Optional[torch.Tensor] = None, out=None,
+                        gs_t: Optional[torch.Tensor] = None):
         """-> (y bf16[rows, cols], mask int32[rows, cols/32] or None,
-        codes uint8[rows, cols/2] or None, stats)."""
+        codes uint8[rows, cols/2] or None, stats).  With gs_t (the training
+        scales from segment_amax) the amax pass is skipped."""
         k = _KINDS[kind] if isinstance(kind, str) else int(kind)
         rows, cols = x.shape
         if out is None:
@@ -263,11 +282,19 @@ class Handle:
                 _need(guide, torch.int32, (rows, cols // 16), "guide", self.device)
             _need(bs_r, torch.uint8, (rows, cols // 16), "bs_r", self.device)
         keep = []
-        st = lib().trace_train_fakequant(
-            self._h, _ptr(x), rows, cols, _segments(seg_t, rows, keep), k, _ptr(guide),
-            _ptr(bs_r), _ptr(gs_r), _segments(seg_r, rows, keep), _ptr(y), _ptr(m), _ptr(c),
-            _ptr(stats), _stream())
-        self._check("trace_train_fakequant", st)
+        sgt = _segments(seg_t, rows, keep)
+        if gs_t is None:
+            st = lib().trace_train_fakequant(
+                self._h, _ptr(x), rows, cols, sgt, k, _ptr(guide), _ptr(bs_r), _ptr(gs_r),
+                _segments(seg_r, rows, keep), _ptr(y), _ptr(m), _ptr(c), _ptr(stats), _stream())
+            self._check("trace_train_fakequant", st)
+        else:
+            _need(gs_t, torch.float32, (sgt.n_seg,), "gs_t", self.device)
+            st = lib().trace_train_fakequant_gs(
+                self._h, _ptr(x), rows, cols, sgt, _ptr(gs_t), k, _ptr(guide), _ptr(bs_r),
+                _ptr(gs_r), _segments(seg_r, rows, keep), _ptr(y), _ptr(m), _ptr(c), _ptr(stats),
+                _stream())
+            self._check("trace_train_fakequant_gs", st)
         return y, m, c, stats
 
     # -- backward ---------------------------------------------------------------

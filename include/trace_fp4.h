@@ -56,7 +56,9 @@
  *     trace_last_cuda_error.  Nothing aborts and no exception crosses the ABI.
  *   - Threading: one host thread at a time per handle.  Calls through one
  *     handle on different streams are ordered on the handle's scratch with
- *     an internal event, so they run one after another on the GPU.
+ *     an internal event, so they run one after another on the GPU.  Work
+ *     that should run concurrently uses one handle per stream (each has its
+ *     own scratch).
  *   - Inputs must be finite; NaN/Inf inputs give unspecified codes but never
  *     fault.
  *
@@ -245,6 +247,32 @@ TRACE_API trace_status_t trace_train_fakequant(trace_handle_t h, const void* x_b
                                      trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
                                      void* codes_t_u8, trace_stats_t* stats_dev,
                                      trace_stream_t stream);
+
+/* trace_train_fakequant with the training scales supplied: the fake
+ * quantiser alone.  gs_t [n_seg_t] (device) holds one global scale per
+ * training segment, as trace_segment_amax writes them for the same x and
+ * seg_t; with those scales the outputs equal trace_train_fakequant's bit for
+ * bit.  Lets the training-side amax pass run earlier, for instance on another
+ * handle and stream while the rollout-side calls run.  gs_t == NULL is an
+ * argument error. */
+TRACE_API trace_status_t trace_train_fakequant_gs(trace_handle_t h, const void* x_bf16,
+                                                  int64_t rows, int64_t cols,
+                                                  trace_segments_t seg_t, const float* gs_t,
+                                                  trace_guide_kind_t kind, const void* guide,
+                                                  const void* bs_r, const float* gs_r,
+                                                  trace_segments_t seg_r, void* y_bf16,
+                                                  uint32_t* ste_mask, void* codes_t_u8,
+                                                  trace_stats_t* stats_dev,
+                                                  trace_stream_t stream);
+
+/* Per-segment amax and global scale alone ([EN] "TRACE Core Concept": one
+ * FP32 global scale per segment, gs = amax / (448 * 6)); the first pass of
+ * trace_rollout_quant's two-kernel form and of trace_train_fakequant.
+ *   x_bf16 [rows, cols]; gs_f32 [n_seg] out (device); an empty or all-zero
+ *   segment gets 0.  One streaming kernel (no wait on other CTAs). */
+TRACE_API trace_status_t trace_segment_amax(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                            int64_t cols, trace_segments_t seg, float* gs_f32,
+                                            trace_stream_t stream);
 
 /* Backward of the fake quantiser through the straight-through estimator
  * (the article's title names quantization-aware training, which trains

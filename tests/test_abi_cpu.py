@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
         s = lib.trace_status_string(code)
         assert isinstance(s, bytes) and s
     assert lib.trace_status_string(99) == b"unknown status"
-    assert lib.trace_version() == 200
+    assert lib.trace_version() == 300
 
 
 def test_create_rejects_bad_devices(lib):
@@ -74,6 +74,29 @@ def test_null_handle_is_an_argument_error(lib):
     assert lib.trace_profile_collect(None, arr) == 1
     assert lib.trace_destroy(None) == 0
     assert lib.trace_last_cuda_error(None) == 0
+
+
+def test_segment_amax_and_scaled_fakequant_argument_errors(lib):
+    from fp4_rollout_guided_gb300.trace import Segments
+    seg = Segments(None, 1)
+    p = ctypes.c_void_p(256)
+    assert lib.trace_segment_amax(None, p, 1, 32, seg, p, None) == 1
+    assert lib.trace_train_fakequant_gs(None, p, 1, 32, seg, p, 0, None, None, None, seg, p,
+                                        None, None, None, None) == 1
+    if not torch.cuda.is_available():
+        return
+    h = ctypes.c_void_p()
+    assert lib.trace_create(ctypes.byref(h), 0) == 0
+    try:
+        # no scales, misaligned scales, bad shape: rejected before any work
+        assert lib.trace_train_fakequant_gs(h, p, 1, 32, seg, None, 0, None, None, None, seg,
+                                            p, None, None, None, None) == 1
+        assert lib.trace_train_fakequant_gs(h, p, 1, 32, seg, ctypes.c_void_p(258), 0, None,
+                                            None, None, seg, p, None, None, None, None) == 2
+        assert lib.trace_segment_amax(h, p, 1, 48, seg, p, None) == 1
+        assert lib.trace_segment_amax(h, p, 1, 32, seg, None, None) == 1
+    finally:
+        lib.trace_destroy(h)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

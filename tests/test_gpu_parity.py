@@ -478,6 +478,76 @@ def test_rollout_input_16_byte_aligned_only(h, cols, offset_bytes):
     assert h.device_status() == 0
 
 
+@pytest.mark.parametrize("cfg", [1, 3, 5])
+def test_segment_amax_and_scaled_fakequant(h, cfg):
+    # the amax pass on its own, then the fake quantiser with those scales:
+    # the same bytes as the one-call form and as the oracle
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(cfg, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    xg, rg = x.to(DEV), r.to(DEV)
+    gs_t = h.segment_amax(xg, w.seg_t)
+    torch.cuda.synchronize()
+    _, _, o_gs, _ = oracle.rollout_quant(u16(x), w.seg_t)
+    assert_same(f"cfg{cfg} gs_t", gs_t.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    codes, bs, gs, guide = h.rollout_quant(rg, w.seg_r)
+    for kind, g in (("none", None), ("full", codes), ("compact", guide)):
+        st1, st2 = trace.new_stats(DEV), trace.new_stats(DEV)
+        args = (xg, w.seg_t, kind) + (() if kind == "none" else (g, bs, gs, w.seg_r))
+        one = h.train_fakequant(*args, codes=True, stats=st1)
+        two = h.train_fakequant(*args, codes=True, stats=st2, gs_t=gs_t)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("y", "mask", "codes_t", "stats"), one, two):
+            assert torch.equal(a, b), f"cfg{cfg} {kind} {name}"
+
+
+def test_segment_amax_empty_and_zero_segments(h):
+    rows, cols = 300, 64
+    x = rand_bf16((rows, cols), 81)
+    x[100:200] = 0
+    seg = [0, 0, 100, 200, 200, rows]
+    gs = h.segment_amax(x.to(DEV), seg)
+    torch.cuda.synchronize()
+    _, _, o_gs, _ = oracle.rollout_quant(u16(x), seg)
+    assert_same("gs", gs.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    assert gs[0].item() == 0 and gs[2].item() == 0 and gs[3].item() == 0
+    gs0 = h.segment_amax(torch.empty((0, cols), dtype=torch.bfloat16, device=DEV), [0, 0, 0])
+    torch.cuda.synchronize()
+    assert gs0.tolist() == [0.0, 0.0]
+
+
+def test_two_handles_overlap_training_scales(h):
+    # rollout side on one handle and stream, training scales on a second
+    # handle and stream at the same time, then the scaled fake quantiser:
+    # equal to the serial one-call path
+    from fp4_rollout_guided_gb300 import trace
+    w = synth.workload(3, small=True)
+    x, r = synth.make_inputs(w, "cpu")
+    xg, rg = x.to(DEV), r.to(DEV)
+    h2 = trace.Handle(0)
+    try:
+        side = torch.cuda.Stream()
+        start = torch.cuda.Event()
+        start.record()
+        with torch.cuda.stream(side):
+            side.wait_event(start)
+            gs_t = h2.segment_amax(xg, w.seg_t)
+            done = torch.cuda.Event()
+            done.record()
+        codes, bs, gs, guide = h.rollout_quant(rg, w.seg_r)
+        h.guide_pack(codes)
+        h.guide_unpack(rg, guide, bs, gs, w.seg_r)
+        torch.cuda.current_stream().wait_event(done)
+        gs_t.record_stream(torch.cuda.current_stream())
+        y, m, _, _ = h.train_fakequant(xg, w.seg_t, "compact", guide, bs, gs, w.seg_r, gs_t=gs_t)
+        y1, m1, _, _ = h.train_fakequant(xg, w.seg_t, "compact", guide, bs, gs, w.seg_r)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y1) and torch.equal(m, m1)
+        assert h.device_status() == 0 and h2.device_status() == 0
+    finally:
+        h2.close()
+
+
 def test_rollout_large_segment_takes_two_kernels(h):
     # one segment of 41 MiB of x is more than a fused wave may hold
     rows, cols = 10496, 2048
