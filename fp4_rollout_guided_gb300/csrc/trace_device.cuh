@@ -16,8 +16,8 @@
 // step's loads are issued before the current step is computed.  Segments
 // are looked up once per step (uniform across the CTA); only a step that
 // straddles a segment boundary resolves segments per thread.  Two kernels
-// differ: the fused rollout kernel stages steps with TMA bulk copies and
-// splits its CTA into copy, amax and quantiser warps, and the STE backward
+// differ: the fused rollout kernel stages steps with TMA copies and splits
+// its CTA into producer, amax and quantiser warps, and the STE backward
 // gives each thread one 16-byte word of eight elements per instruction.
 //
 // Arithmetic.  All of it is binary32 with round-to-nearest-even (explicit

@@ -279,26 +279,27 @@ __global__ void __launch_bounds__(kThreads)
 //
 // The segments are grouped into waves of whole segments small enough to stay
 // in L2 (host-planned, WaveParam, at most kWaveSegs segments each).  The
-// 256-chunk steps of each wave are split into contiguous ranges, one per
-// CTA, one CTA per SM.  In each CTA one producer thread stages steps into shared memory
-// with TMA bulk copies (cp.async.bulk, completion on mbarriers) on two
-// rings (a second thread watches the cross-CTA wave counters for it):
-//   - the amax ring streams this CTA's steps from HBM; four amax warps fold
-//     per-segment maxima into shared memory and, at the end of each wave,
-//     into amax_bits, then count the CTA done with that wave (wave_cnt);
-//   - the quantiser ring re-reads the same steps of an earlier wave, from
-//     L2, once every CTA has counted that wave; eight quantiser warps turn
-//     each staged chunk into codes, block scales and compact words with
+// 256-chunk steps of each wave are dealt to the CTAs, one CTA per SM, in
+// contiguous ranges or round-robin (WaveCursor).  In each CTA two producer
+// threads stage steps into shared memory with TMA copies (a 2-D tensor map
+// with 128-byte swizzle when rows hold an even number of chunks, else
+// cp.async.bulk; completion on mbarriers) on two rings:
+//   - the amax producer streams this CTA's steps from HBM; four amax warps
+//     fold per-segment maxima into shared memory and, at the end of each
+//     wave, into amax_bits, then count the CTA done with that wave
+//     (wave_cnt);
+//   - the quantiser producer waits until every CTA has counted a wave, then
+//     re-reads the same steps, from L2; two groups of eight quantiser warps
+//     turn each staged chunk into codes, block scales and compact words with
 //     gs = amax/2688.
 // The amax stream leads the quantiser by a bounded number of steps, which
 // bounds what L2 must hold, and otherwise never waits, so HBM streaming and
 // quantisation overlap.
 //
-// The launch is cooperative (all CTAs co-resident).  Every wait is bounded:
-// the producer gives up the cross-CTA waits once nothing has moved for the
-// time limit (setting *err, the outputs are then undefined), every mbarrier
-// wait has the same limit, and the producer waits for its own copies in
-// flight before the CTA exits.
+// The launch is cooperative (all CTAs co-resident).  Every wait is bounded
+// by the same time limit: a wait that runs out sets *err (the outputs are
+// then undefined) and gives up the cross-CTA waits that follow, and each
+// producer waits for its own copies in flight before the CTA exits.
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
