@@ -137,7 +137,9 @@ def drift(x, seed, sigma):
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 32), (3, 96), (7, 160), (1000, 64), (517, 224),
-                                        (2049, 32), (5, 4096)])
+                                        (2049, 32), (5, 4096),
+                                        # smaller than one 128-row tensor-map box
+                                        (1, 64), (3, 128), (100, 64)])
 def test_ragged_shapes(h, rows, cols):
     x = rand_bf16((rows, cols), rows * 7 + cols)
     r = drift(x, rows, 2.0 ** -6)
