@@ -692,9 +692,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   } else if (warp == 1) {
     // ---- quantiser producer: wave by wave, waits until every CTA has
-    // counted the wave's maxima, writes the global scales of the waves w
-    // with w mod G == b, then re-reads the CTA's steps of the wave (now from
-    // L2) into ring Q ----
+    // counted the wave's maxima, then re-reads the CTA's steps of the wave
+    // (now from L2) into ring Q ----
     if (lane == 0) {
       uint64_t evict_first;
       asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
@@ -707,10 +706,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (!broken && !wait_at_least(wave_cnt + w, G + wait_extra, wait_ns)) {
           atomicOr(err, 1u);
           broken = true;
-        }
-        if (b == (uint32_t)w % G) {
-          for (int s = wv.seg0[w]; s < wv.seg0[w + 1]; ++s)
-            gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
         }
         for (; cq.w == w; cq.next(seg, wv, cpr_u, b, G)) {
           const uint32_t slot = nq % kSlotsQ, use = nq / kSlotsQ;
@@ -863,8 +858,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   }
 
-  // The last CTA to finish re-zeroes the maxima and the wave counters for
-  // the next call (every CTA has finished reading them by then).
+  // The last CTA to finish writes the global scales and re-zeroes the
+  // maxima and the wave counters for the next call (every CTA has finished
+  // reading them by then).
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -874,7 +870,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __syncthreads();
   if (is_last) {
     __threadfence();
-    for (int s = threadIdx.x; s < seg.n; s += kFusedThreads) amax_bits[s] = 0u;
+    // the global scales are written here, all at once: a producer that
+    // wrote a wave's scales before streaming the wave would start it late
+    for (int s = threadIdx.x; s < seg.n; s += kFusedThreads) {
+      gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
+      amax_bits[s] = 0u;
+    }
     for (int w = threadIdx.x; w < wv.n; w += kFusedThreads) wave_cnt[w] = 0u;
     if (threadIdx.x == 0) *done = 0u;
   }
