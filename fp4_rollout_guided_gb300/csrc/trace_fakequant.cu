@@ -56,6 +56,15 @@ __device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) 
   k.h_g[3] += d1 >= 3;
 }
 
+// A packed product that an add or subtract consumes goes through this
+// first.  The code generator may fuse a packed multiply into the packed add
+// that follows it (it did so for the distances below, even with explicit
+// round-to-nearest on both instructions), which skips the product's own
+// rounding and changes near-tie decisions.  Multiplying the rounded product
+// by a 1.0 known only at run time (a kernel argument) makes any such fusion
+// harmless: a fused p * 1 + c rounds once, to fl(p + c).
+__device__ __forceinline__ F2 rounded(F2 p, float one) { return mul2_rn(p, splat(one)); }
+
 // Training side of one pair of elements.  ax holds |x|; St holds the
 // training scale carrying each element's sign, vr the rollout's
 // reconstructed values with the rollout's signs, so the candidates
@@ -69,8 +78,8 @@ __device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) 
 // rtn_hi - 1 >= 0 as a signed integer; the select is done on the bit
 // patterns: y = v_hi - lo * (v_hi - v_lo) with lo = 0 or 1.
 template <bool GUIDED, bool WANT_G>
-__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2& ym, F2& gsel,
-                                           F2& grtn) {
+__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, float one, F2& ym,
+                                           F2& gsel, F2& grtn) {
   const F2 t = mul2_rn(ax, splat(inv_t));
   const F2 tc = {fminf(t.x, 6.0f), fminf(t.y, 6.0f)};
   const F2 C = magic_pair(tc);
@@ -84,8 +93,9 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, F2&
   }
   const F2 sz = add2_rz(tc, C), sp = add2_rp(tc, C);
   const F2 glo = sub2_rn(sz, C), ghi = sub2_rn(sp, C);
-  const F2 vlo = mul2_rn(glo, St), vhi = mul2_rn(ghi, St);
-  const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
+  const F2 vlo = rounded(mul2_rn(glo, St), one), vhi = rounded(mul2_rn(ghi, St), one);
+  const F2 vrr = rounded(vr, one);
+  const F2 dlo = sub2_rn(vlo, vrr), dhi = sub2_rn(vhi, vrr);
   const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
   const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
   const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
@@ -108,6 +118,69 @@ __device__ __forceinline__ uint32_t spread16(uint32_t v) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// The guided choice without distances (the fast form)
+// ---------------------------------------------------------------------------
+//
+// Let rho = S_r / S_t.  The method compares d_c = |G[c] S_t - v_r| for the
+// two candidates lo < hi = lo + 1 of t in binary32.  In exact arithmetic,
+// with equal signs, hi is closer exactly when G[m_r] rho > (G[lo] + G[hi])/2.
+// Over every adjacent pair of the E2M1 grid that midpoint lies at least
+// 7/6 G[lo] above G[lo] and at most 7/8 G[hi] below G[hi], so whenever
+// 7/8 < rho < 7/6 the rollout index alone decides: hi if m_r > lo (that is,
+// m_r >= hi), else lo; with opposite signs lo always wins (the smaller
+// magnitude is nearer a value of the other sign); a point bracket has one
+// candidate.  The margins used below (0.876, 1.165) leave at least 2^-9 of
+// relative room between the two distances, far above the few binary32
+// rounding errors of the products and differences, and the scales are kept
+// at or above 2^-100 so that every product is a normal number.  No tie can
+// occur inside that window, so the RTN fallback never applies there.
+//
+// Which side of lo the rollout index lies on needs no rollout-frame bracket.
+// The decoded index is the member of the bracket of t_r = |x| * inv_r whose
+// parity is the stored bit, so with glo = G[lo], ghi = G[hi] of the
+// training side:  t_r < glo or t_r == glo gives m_r <= lo;  t_r >= ghi gives
+// m_r >= hi;  glo < t_r < ghi gives m_r = lo or hi by the stored bit.  All
+// of that is read off t_r rounded down and up to the training side's grid
+// spacing s (the rounding constant C of t):  uz = fl_rz(t_r + C) and
+// up = fl_rp(t_r + C) are C + s floor(t_r / s) and C + s ceil(t_r / s), the
+// member us of {uz, up} whose significand parity equals the stored bit is
+// the decoded point relative to that grid, and the chosen candidate is
+// us clamped to [C + glo, C + ghi].  An opposite rollout sign is carried by
+// t_r itself (x is given the relative sign first): t_r < 0 gives us <= C,
+// which clamps to lo.  For the full record the stored index's value is
+// clamped the same way (rounded toward zero onto the grid of C).
+//
+// The form is exact wherever it is taken; blocks whose ratio lies outside
+// the window (rare: about one block in 10^4 to 10^5 on the workloads) send
+// their warp through the distance comparison.
+constexpr float kRhoLo = 0.876f, kRhoHi = 1.165f, kScaleMin = 0x1p-100f;
+
+__device__ __forceinline__ bool fast_block(float S_t, float S_r) {
+  return S_t >= kScaleMin && S_r > __fmul_rn(kRhoLo, S_t) && S_r < __fmul_rn(kRhoHi, S_t);
+}
+
+// A compact word's sixteen sign bits rearranged so that the signs of
+// elements 2k and 2k + 1 land at bits 15 and 31 after a left shift by
+// 15 - 2k: even elements at bit j, odd elements at bit j + 15.
+__device__ __forceinline__ uint32_t sign_spread(uint32_t gw) {
+  return (gw & 0x5555u) | ((gw & 0xAAAAu) << 15);
+}
+
+// The two bf16 lanes of a word as binary32 (signs kept).
+__device__ __forceinline__ F2 lanes(uint32_t w) {
+  return F2{__uint_as_float(imad(w, 0x10000u, 0u)), __uint_as_float(w & 0xFFFF0000u)};
+}
+
+// Training bracket of a pair in the frame of its rounding constant:
+// C, sz = C + glo, sp = C + ghi (t may carry any sign; |t| is bracketed).
+__device__ __forceinline__ void train_bracket(F2 t, F2& C, F2& sz, F2& sp) {
+  const F2 tc = {fminf(fabsf(t.x), 6.0f), fminf(fabsf(t.y), 6.0f)};
+  C = magic_pair(tc);
+  sz = add2_rz(tc, C);
+  sp = add2_rp(tc, C);
+}
+
 #ifndef TFP4_FQ_MIN_CTAS
 #define TFP4_FQ_MIN_CTAS 4
 #endif
@@ -119,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
                 const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
                 const float* __restrict__ gs_r, uint8_t* __restrict__ y,
                 uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
-                trace_stats_t* __restrict__ stats) {
+                trace_stats_t* __restrict__ stats, float one) {
   constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
   const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
   uint32_t step = blockIdx.x * steps_per_cta;
@@ -139,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
 
   // the next step's inputs are loaded at the end of the current step
-  Chunk cur;
+  Chunk cur = {};
   uint4 gcur = make_uint4(0, 0, 0, 0);
   uint32_t bcur = 0;
   if (step < step_end) {
@@ -180,18 +253,20 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       __syncthreads();
     }
-    if (c < nchunks) {
+    // scales of both blocks (threads past the end compute on stale data
+    // and store nothing)
+    PairScale pt, pr = {};
+    uint32_t thr2[2];
+    {
       int s_t = st.cur, s_r = sr.cur;
       if (!uni_t || !uni_r) {
-        const uint32_t row = cpr.div(c);
+        const uint32_t row = cpr.div(min(c, nchunks - 1));
         if (!uni_t) s_t = seg_advance(seg_t, st.cur, row);
         if (GUIDED && !uni_r) s_r = seg_advance(seg_r, sr.cur, row);
       }
       uint32_t a[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
-      PairScale pt, pr = {};
-      uint32_t thr2[2];
       if (uni_t) {
         pt.codes = pair_codes(block_amax8(a), block_amax8(a + 8), seg_gs, seg_den, seg_rden);
 #pragma unroll
@@ -219,52 +294,110 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           pr = pair_scale_stored(bcur, gs_r[s_r]);
         }
       }
-
+    }
+    // the fast form when every block of the warp's chunks allows it
+    bool fast = false;
+    if (GUIDED && !STATS)
+      fast = __all_sync(0xFFFFFFFFu, c >= nchunks || (fast_block(pt.S[0], pr.S[0]) &&
+                                                       fast_block(pt.S[1], pr.S[1])));
+    if (c < nchunks) {
       uint32_t ybits[4];
       uint32_t cbytes[16];
       uint32_t kept = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int b = i >> 3;        // block of this word
-        const int j0 = (i & 7) * 2;  // index of its low element in the block
-        const uint32_t w = cur.w[i];
-        const F2 ax = {__uint_as_float(imad(a[i], 0x10000u, 0u)), __uint_as_float(a[i] & 0xFFFF0000u)};
-        const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
-        const uint32_t Stb = __float_as_uint(pt.S[b]);
-        const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
-        F2 vr = {0.0f, 0.0f};
-        F2 grs = {0.0f, 0.0f};  // signed rollout magnitudes (statistics)
+      if (fast) {
+        uint32_t U[2] = {0u, 0u};
         if (KIND == TRACE_GUIDE_COMPACT) {
-          const uint32_t gw = b ? gcur.y : gcur.x;
-          const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw, j0);
-          const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
-          const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
-          const uint32_t Sb = __float_as_uint(pr.S[b]);
-          vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
-          if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
-                              __uint_as_float(__float_as_uint(gr.y) | sr1)};
-        } else if (KIND == TRACE_GUIDE_FULL) {
-          const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
-          float g0, g1;
-          e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
-          vr = mul2_rn(F2{g0, g1}, splat(pr.S[b]));
-          if (STATS) grs = F2{g0, g1};
+          U[0] = sign_spread(gcur.x);
+          U[1] = sign_spread(gcur.y);
         }
-        F2 ym, gsel, grtn;
-        train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, ym, gsel, grtn);
-        ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
-        if ((i & 3) == 3)
-          st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-        if (MASK) kept = (kept >> 1) | (imad(a[i], 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
-        if (CODES || STATS) {
-          const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
-          const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
-          if (CODES) cbytes[i] = e2m1x2(g0, g1);
-          if (STATS && GUIDED) {
-            count(cnt, signed_index(grs.x),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.x) | sx0)), signed_index(g0));
-            count(cnt, signed_index(grs.y),
-                  signed_index(__uint_as_float(__float_as_uint(grtn.y) | sx1)), signed_index(g1));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int b = i >> 3;        // block of this word
+          const int j0 = (i & 7) * 2;  // index of its low element in the block
+          const uint32_t w = cur.w[i];
+          F2 C, sz, sp, us;
+          if (KIND == TRACE_GUIDE_COMPACT) {
+            // x with the relative sign (training xor rollout) in both lanes
+            const uint32_t rel = w ^ (imad(U[b], 1u << (15 - j0), 0u) & 0x80008000u);
+            const F2 xl = lanes(rel);
+            train_bracket(mul2_rn(xl, splat(pt.inv[b])), C, sz, sp);
+            const F2 tr = rounded(mul2_rn(xl, splat(pr.inv[b])), one);
+            const F2 uz = add2_rz(tr, C), up = add2_rp(tr, C);
+            const uint32_t gw = b ? gcur.y : gcur.x;
+            const uint32_t b0 = 1u << (16 + j0), b1 = 1u << (17 + j0);
+            const uint32_t m0 = (imad(__float_as_uint(uz.x), b0, 0u) ^ gw) & b0;
+            const uint32_t m1 = (imad(__float_as_uint(uz.y), b1, 0u) ^ gw) & b1;
+            us = F2{m0 ? up.x : uz.x, m1 ? up.y : uz.y};
+          } else {
+            train_bracket(mul2_rn(lanes(w), splat(pt.inv[b])), C, sz, sp);
+            const uint32_t gword =
+                (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
+            uint32_t h;  // the stored pair's values (f16x2), relative sign
+            asm("{ .reg .b8 q; cvt.u8.u32 q, %1; cvt.rn.f16x2.e2m1x2 %0, q; }"
+                : "=r"(h)
+                : "r"((gword >> (8 * (i & 3))) & 0xFFu));
+            h ^= w & 0x80008000u;
+            float g0, g1;
+            asm("cvt.f32.f16 %0, %1;" : "=f"(g0) : "h"((unsigned short)(h & 0xFFFFu)));
+            asm("cvt.f32.f16 %0, %1;" : "=f"(g1) : "h"((unsigned short)(h >> 16)));
+            us = add2_rz(F2{g0, g1}, C);
+          }
+          const F2 yc = {fminf(fmaxf(us.x, sz.x), sp.x), fminf(fmaxf(us.y, sz.y), sp.y)};
+          const F2 g = sub2_rn(yc, C);
+          const F2 ym = mul2_rn(g, splat(pt.S[b]));
+          ybits[i & 3] = bf16x2_rn(ym.x, ym.y) | (w & 0x80008000u);
+          if ((i & 3) == 3)
+            st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
+          if (MASK) kept = (kept >> 1) | (imad(w & kAbs2, 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
+          if (CODES)
+            cbytes[i] = e2m1x2(__uint_as_float(__float_as_uint(g.x) | (imad(w, 0x10000u, 0u) & 0x80000000u)),
+                               __uint_as_float(__float_as_uint(g.y) | (w & 0x80000000u)));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int b = i >> 3;        // block of this word
+          const int j0 = (i & 7) * 2;  // index of its low element in the block
+          const uint32_t w = cur.w[i];
+          const uint32_t a = w & kAbs2;
+          const F2 ax = {__uint_as_float(imad(a, 0x10000u, 0u)), __uint_as_float(a & 0xFFFF0000u)};
+          const uint32_t sx0 = imad(w, 0x10000u, 0u) & 0x80000000u, sx1 = w & 0x80000000u;
+          const uint32_t Stb = __float_as_uint(pt.S[b]);
+          const F2 St = {__uint_as_float(Stb | sx0), __uint_as_float(Stb | sx1)};
+          F2 vr = {0.0f, 0.0f};
+          F2 grs = {0.0f, 0.0f};  // signed rollout magnitudes (statistics)
+          if (KIND == TRACE_GUIDE_COMPACT) {
+            const uint32_t gw = b ? gcur.y : gcur.x;
+            const F2 gr = decode_pair(mul2_rn(ax, splat(pr.inv[b])), gw, j0);
+            const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
+            const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
+            const uint32_t Sb = __float_as_uint(pr.S[b]);
+            vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
+            if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
+                                __uint_as_float(__float_as_uint(gr.y) | sr1)};
+          } else if (KIND == TRACE_GUIDE_FULL) {
+            const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
+            float g0, g1;
+            e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
+            vr = mul2_rn(F2{g0, g1}, splat(pr.S[b]));
+            if (STATS) grs = F2{g0, g1};
+          }
+          F2 ym, gsel, grtn;
+          train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, one, ym, gsel, grtn);
+          ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
+          if ((i & 3) == 3)
+            st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
+          if (MASK) kept = (kept >> 1) | (imad(a, 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
+          if (CODES || STATS) {
+            const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
+            const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
+            if (CODES) cbytes[i] = e2m1x2(g0, g1);
+            if (STATS && GUIDED) {
+              count(cnt, signed_index(grs.x),
+                    signed_index(__uint_as_float(__float_as_uint(grtn.x) | sx0)), signed_index(g0));
+              count(cnt, signed_index(grs.y),
+                    signed_index(__uint_as_float(__float_as_uint(grtn.y) | sx1)), signed_index(g1));
+            }
           }
         }
       }
@@ -319,7 +452,7 @@ cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegPa
                                     FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
                                     seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
                                     a.gs_r, (uint8_t*)a.y, (uint8_t*)a.mask,
-                                    (uint8_t*)a.codes_t, a.stats);
+                                    (uint8_t*)a.codes_t, a.stats, 1.0f);
   return cudaGetLastError();
 }
 

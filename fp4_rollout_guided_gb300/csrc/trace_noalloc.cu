@@ -12,11 +12,21 @@
 // until the process exits.
 //
 // The first call on a device (with that device current) looks up the
-// array's device address with cudaGetSymbolAddress and caches it; make that
-// first call before any stream capture.  Every later call reuses the cached
-// address.  All calls on a device share the one array: each call clears the
-// part it needs with cudaMemsetAsync on its own stream, and calls that
-// overlap on the GPU (for example on two streams at once) race on it.
+// array's device address with cudaGetSymbolAddress and caches it together
+// with the identity of the calling thread's current CUDA context; make that
+// first call before any stream capture.  A later call reuses the cached
+// address while the current context is the same one, and looks it up again
+// when it is not (after cudaDeviceReset, or with another context made
+// current on the device), so an address from a destroyed or foreign context
+// is never used.  All calls on a device share the one array: each call
+// clears the part it needs with cudaMemsetAsync on its own stream, and calls
+// that overlap on the GPU (for example on two streams at once) race on it.
+//
+// The call always runs the two-kernel rollout path (the amax pass, then the
+// quantiser), so x is read twice; the fused single-read kernel needs the
+// per-wave counters and error word of a handle.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,17 +44,45 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kWords];
 constexpr int kMaxDevices = 64;
 
 struct DeviceSlot {
-  bool ready = false;
-  int status = TRACE_OK;
-  uint32_t* scratch = nullptr;
+  bool ready = false;            // device checked, sm_count known
+  uint32_t* scratch = nullptr;   // device address of the array ...
+  unsigned long long ctx = 0;    // ... in this context (0: unknown, look up every call)
   int sm_count = 0;
 };
 
 std::mutex g_mu;
 DeviceSlot g_slots[kMaxDevices];
 
-// Once per device, with that device current: check the device and resolve
-// the scratch array's device address.
+// Identity of the calling thread's current context (driver entry points
+// looked up once through the runtime); 0 when there is none or the driver
+// cannot tell, in which case the address is looked up on every call.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// With the device current: check the device once, and resolve the scratch
+// array's device address whenever the current context is not the one the
+// cached address belongs to.
 trace_status_t setup(int dev, DeviceSlot** out) {
   if (dev < 0 || dev >= kMaxDevices) return TRACE_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -58,14 +96,20 @@ trace_status_t setup(int dev, DeviceSlot** out) {
       return TRACE_ERR_UNSUPPORTED_DEVICE;
     }
     if (major != 10 || minor != 3) return TRACE_ERR_UNSUPPORTED_DEVICE;
+    s.sm_count = sms;
+    s.ready = true;
+  }
+  const unsigned long long ctx = current_context_id();
+  if (s.scratch == nullptr || ctx == 0 || ctx != s.ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      s.scratch = nullptr;
       return TRACE_ERR_CUDA;
     }
     s.scratch = (uint32_t*)p;
-    s.sm_count = sms;
-    s.ready = true;
+    // the lookup above made a context current if there was none
+    s.ctx = ctx != 0 ? ctx : current_context_id();
   }
   *out = &s;
   return TRACE_OK;

@@ -378,7 +378,9 @@ TRACE_API trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes,
 
 /* Rollout-side quantisation without a handle and without any device
  * allocation.  The paper has no counterpart: this is a deployment variant of
- * trace_rollout_quant with the same arguments, layouts and results.
+ * trace_rollout_quant with the same arguments, layouts and results (bit for
+ * bit).  It always runs the two-kernel path (amax pass, then quantiser), so
+ * x is read twice; the handle's fused kernel reads it once.
  *
  * It is for callers that must not call cudaMalloc (code running inside a
  * device allocator or memory pool, runtimes that pre-reserve all device
@@ -391,10 +393,14 @@ TRACE_API trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes,
  * TRACE_ERR_INVALID_ARG before anything is enqueued.
  *
  * It works on the current device.  Its first call on a device resolves the
- * array's device address (cudaGetSymbolAddress) and caches it, so make that
- * first call before any stream capture.  Every call clears the part of the
- * array it uses on `stream`; all calls on one device share the array, so
- * calls that overlap on the GPU (e.g. on two streams at once) race. */
+ * array's device address (cudaGetSymbolAddress) and caches it with the
+ * identity of the current CUDA context, so make that first call before any
+ * stream capture; a call made under another context (after cudaDeviceReset,
+ * or with a different context current) resolves the address again.  rows ==
+ * 0 writes n_seg zero global scales and launches no kernel.  Every call
+ * clears the part of the array it uses on `stream`; all calls on one device
+ * share the array, so calls that overlap on the GPU (e.g. on two streams at
+ * once) race. */
 #define TRACE_NOALLOC_MAX_SEGMENTS 1024
 TRACE_API trace_status_t trace_rollout_quant_noalloc(const void* x_bf16, int64_t rows,
                                                      int64_t cols, trace_segments_t seg,

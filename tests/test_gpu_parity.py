@@ -71,6 +71,14 @@ def run_everything(h, x_cpu, r_cpu, seg_t, seg_r, stats=True):
             y, m, c, _ = h.train_fakequant(xg, seg_t, kind, g, bs, gs, seg_r, codes=True, stats=st)
         out[kind] = (u16(y), u32(m), c.cpu().numpy(),
                      None if st is None else st.cpu().numpy().astype(np.uint64))
+        if kind != "none":
+            # without counters the kernel takes the distance-free form of the
+            # guided choice wherever the scale ratio allows it: once with the
+            # training codes, once with the output and mask only
+            y2, m2, c2, _ = h.train_fakequant(xg, seg_t, kind, g, bs, gs, seg_r, codes=True)
+            y3, m3, _, _ = h.train_fakequant(xg, seg_t, kind, g, bs, gs, seg_r)
+            out[kind + "/codes"] = (u16(y2), u32(m2), c2.cpu().numpy(), None)
+            out[kind + "/mask"] = (u16(y3), u32(m3), None, None)
     torch.cuda.synchronize()
     return dict(codes=codes.cpu().numpy(), bs=bs.cpu().numpy(), gs=gs.cpu().numpy(),
                 guide=u32(guide), packed=u32(packed), unpack_r=unpack_r.cpu().numpy(),
@@ -108,6 +116,12 @@ def check_all(h, x_cpu, r_cpu, seg_t, seg_r, label):
             assert gst[0] == ost[0]
         else:
             assert_same(f"{label} {kind} stats", gst, ost)
+            for variant in ("/codes", "/mask"):
+                vy, vm, vc, _ = g["fq"][kind + variant]
+                assert_same(f"{label} {kind}{variant} y", vy, oy)
+                assert_same(f"{label} {kind}{variant} mask", vm, om)
+                if vc is not None:
+                    assert_same(f"{label} {kind}{variant} codes_t", vc, oc)
     return g, o
 
 
@@ -211,6 +225,57 @@ def test_unrelated_rollout(h):
     seg_r = np.array([0, 50, 51, 299, 300], np.int64)
     g, o = check_all(h, x, r, seg_t, seg_r, "unrelated")
     assert np.all(o["fq"]["full"][3][3:7] > 0)
+
+
+def test_guided_choice_at_scale_ratio_window_edges(h):
+    """The guided choice takes a distance-free form when the rollout/training
+    scale ratio lies strictly inside (7/8, 7/6) (with a small margin) and the
+    binary32 distance comparison elsewhere.  Rollout global scales swept
+    finely across both edges of that window, and far outside it, must give
+    the oracle's bytes either way; rows of one call mix both forms."""
+    rows, cols = 512, 256
+    x = rand_bf16((rows, cols), 51)
+    r = drift(x, 52, 2.0 ** -7)
+    xu, ru = u16(x), u16(r)
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(ru, None)
+    factors = np.concatenate([np.linspace(0.86, 0.89, 13), np.linspace(1.15, 1.18, 13),
+                              [0.5, 0.8, 1.0, 1.25, 2.0, 0.876, 1.165]]).astype(np.float32)
+    n_seg = len(factors)
+    seg = np.linspace(0, rows, n_seg + 1).astype(np.int64)
+    seg[-1] = rows
+    # the same rollout record, read with a different global scale per segment
+    gs_r = (o_gs[0] * factors).astype(np.float32)
+    xg = x.to(DEV)
+    codes_g = torch.from_numpy(o_codes).to(DEV)
+    bs_g = torch.from_numpy(o_bs).to(DEV)
+    guide_g = torch.from_numpy(o_guide.view(np.int32)).to(DEV)
+    gs_g = torch.from_numpy(gs_r).to(DEV)
+    for kind, gd, od in (("compact", guide_g, o_guide), ("full", codes_g, o_codes)):
+        okind = oracle.GUIDE_COMPACT if kind == "compact" else oracle.GUIDE_FULL
+        oy, om, oc, _ = oracle.train_fakequant(xu, None, okind, od, o_bs, gs_r, seg,
+                                               want_stats=False)
+        for want_codes in (False, True):
+            y, m, c, _ = h.train_fakequant(xg, None, kind, gd, bs_g, gs_g, seg, codes=want_codes)
+            torch.cuda.synchronize()
+            assert_same(f"ratio sweep {kind} y", u16(y), oy)
+            assert_same(f"ratio sweep {kind} mask", u32(m), om)
+            if want_codes:
+                assert_same(f"ratio sweep {kind} codes_t", c.cpu().numpy(), oc)
+
+
+def test_mixed_forms_in_one_warp(h):
+    """Rows whose rollout copy is rescaled by 1.3 or 0.75 (outside the ratio
+    window) interleaved with plain drifted rows, so warps hold both kinds of
+    blocks and take the exact form, while neighbouring warps take the fast one."""
+    rows, cols = 2048, 128
+    x = rand_bf16((rows, cols), 61, scale=2.0)
+    r = drift(x, 62, 2.0 ** -8).float()
+    k = torch.arange(rows)
+    r[k % 97 == 3] *= 1.3
+    r[k % 89 == 5] *= 0.75
+    r = r.to(torch.bfloat16)
+    check_all(h, x, r, np.array([0, 700, 2048], np.int64), np.array([0, 1024, 2048], np.int64),
+              "mixed")
 
 
 def test_empty_input(h):
