@@ -161,15 +161,18 @@ __device__ __forceinline__ uint32_t absmax_lanes_bits(uint32_t m) {
   return (absmax_bf16x2(m, m >> 16) << 16) & 0x7FFF0000u;
 }
 
-// Eight words of masked bf16 magnitudes -> binary32 bits of their maximum.
-__device__ __forceinline__ float block_amax8(const uint32_t* a) {
-  uint32_t m0 = max_u16x2(a[0], a[1]);
-  const uint32_t m1 = max_u16x2(a[2], a[3]);
-  const uint32_t m2 = max_u16x2(a[4], a[5]);
-  const uint32_t m3 = max_u16x2(a[6], a[7]);
-  m0 = max_u16x2(max_u16x2(m0, m1), max_u16x2(m2, m3));
-  const uint32_t hi = m0 >> 16, lo = m0 & 0xFFFFu;
-  return __uint_as_float((hi > lo ? hi : lo) << 16);
+// The two block maxima of a chunk (bf16 abs-max on the raw words).
+__device__ __forceinline__ void chunk_bamax(const Chunk& cur, float& b0, float& b1) {
+  uint32_t m[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t* w = cur.w + 8 * b;
+    const uint32_t m01 = absmax_bf16x2(absmax_bf16x2(w[0], w[1]), absmax_bf16x2(w[2], w[3]));
+    const uint32_t m23 = absmax_bf16x2(absmax_bf16x2(w[4], w[5]), absmax_bf16x2(w[6], w[7]));
+    m[b] = absmax_lanes_bits(absmax_bf16x2(m01, m23));
+  }
+  b0 = __uint_as_float(m[0]);
+  b1 = __uint_as_float(m[1]);
 }
 
 // E4M3 code -> binary32: placing the 7 magnitude bits at bit 20 gives the

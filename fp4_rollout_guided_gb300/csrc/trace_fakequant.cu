@@ -109,13 +109,19 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, flo
   }
 }
 
-// Spreads the 16 low bits of v to the even bit positions.
-__device__ __forceinline__ uint32_t spread16(uint32_t v) {
-  v = (v | (v << 8)) & 0x00FF00FFu;
-  v = (v | (v << 4)) & 0x0F0F0F0Fu;
-  v = (v | (v << 2)) & 0x33333333u;
-  v = (v | (v << 1)) & 0x55555555u;
-  return v;
+// STE mask bits of a chunk.  Word i (elements 2i, 2i + 1) yields
+// X = (thr2 - |x|pair) & 0x80008000, its two kept bits at 15 and 31.  One
+// 64-bit multiply-add per word moves them to their interleaved place:
+// X * (2^(2k + 15) + 2^(2k)), k = i mod 8, puts bit 15 at 2k + 30 and bit 31
+// at 2k + 31; the two other partial products land at 2k + 15 (below bit 30)
+// and 2k + 46 (above bit 45), every one at its own position for k = 0..7,
+// so the sum has no carries and bits 30..45 of the two accumulators (words
+// 0..7 and 8..15) are the mask word's two halves in element order.
+__device__ __forceinline__ void mask_gather(uint64_t& acc, uint32_t X, int k) {
+  asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(acc) : "r"(X), "r"((1u << (2 * k + 15)) + (1u << (2 * k))));
+}
+__device__ __forceinline__ uint32_t mask_word(uint64_t acc0, uint64_t acc1) {
+  return ((uint32_t)(acc0 >> 30) & 0xFFFFu) | ((uint32_t)(acc1 >> 30) << 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -264,11 +270,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         if (!uni_t) s_t = seg_advance(seg_t, st.cur, row);
         if (GUIDED && !uni_r) s_r = seg_advance(seg_r, sr.cur, row);
       }
-      uint32_t a[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) a[i] = cur.w[i] & kAbs2;
+      float bam0, bam1;
+      chunk_bamax(cur, bam0, bam1);
       if (uni_t) {
-        pt.codes = pair_codes(block_amax8(a), block_amax8(a + 8), seg_gs, seg_den, seg_rden);
+        pt.codes = pair_codes(bam0, bam1, seg_gs, seg_den, seg_rden);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const uint32_t code = (pt.codes >> (8 * b)) & 0xFFu;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           thr2[b] = tab_t.thr2[code];
         }
       } else {
-        pt = pair_scale(block_amax8(a), block_amax8(a + 8), gs_t[s_t]);
+        pt = pair_scale(bam0, bam1, gs_t[s_t]);
         thr2[0] = ste_threshold2(pt.S[0]);
         thr2[1] = ste_threshold2(pt.S[1]);
       }
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     if (c < nchunks) {
       uint32_t ybits[4];
       uint32_t cbytes[16];
-      uint32_t kept = 0;
+      uint64_t kacc[2] = {0, 0};
       if (fast) {
         uint32_t U[2] = {0u, 0u};
         if (KIND == TRACE_GUIDE_COMPACT) {
@@ -342,13 +347,16 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
             asm("cvt.f32.f16 %0, %1;" : "=f"(g1) : "h"((unsigned short)(h >> 16)));
             us = add2_rz(F2{g0, g1}, C);
           }
+          // us clamped to [sz, sp], on the FMA pipe: us - sz is a multiple of
+          // the grid spacing (>= 0.5) or <= 0, so h = sat(4 (us - sz)) is
+          // exactly 1 or 0, and g = glo + h (ghi - glo) is the chosen point
           const F2 yc = {fminf(fmaxf(us.x, sz.x), sp.x), fminf(fmaxf(us.y, sz.y), sp.y)};
           const F2 g = sub2_rn(yc, C);
           const F2 ym = mul2_rn(g, splat(pt.S[b]));
           ybits[i & 3] = bf16x2_rn(ym.x, ym.y) | (w & 0x80008000u);
           if ((i & 3) == 3)
             st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-          if (MASK) kept = (kept >> 1) | (imad(w & kAbs2, 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
+          if (MASK) mask_gather(kacc[b], imad(w & kAbs2, 0xFFFFFFFFu, thr2[b]) & 0x80008000u, i & 7);
           if (CODES)
             cbytes[i] = e2m1x2(__uint_as_float(__float_as_uint(g.x) | (imad(w, 0x10000u, 0u) & 0x80000000u)),
                                __uint_as_float(__float_as_uint(g.y) | (w & 0x80000000u)));
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
           if ((i & 3) == 3)
             st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
-          if (MASK) kept = (kept >> 1) | (imad(a, 0xFFFFFFFFu, thr2[b]) & 0x80008000u);
+          if (MASK) mask_gather(kacc[b], imad(a, 0xFFFFFFFFu, thr2[b]) & 0x80008000u, i & 7);
           if (CODES || STATS) {
             const float g0 = __uint_as_float(__float_as_uint(gsel.x) | sx0);
             const float g1 = __uint_as_float(__float_as_uint(gsel.y) | sx1);
@@ -401,9 +409,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           }
         }
       }
-      // word i left its two bits at positions i and 16 + i: interleave
-      if (MASK) kept = spread16(kept & 0xFFFFu) | (spread16(kept >> 16) << 1);
-      if (MASK) st_stream1(mask + (uint64_t)c * 4u, kept);
+      if (MASK) st_stream1(mask + (uint64_t)c * 4u, mask_word(kacc[0], kacc[1]));
       if (CODES) {
         uint32_t o[4];
 #pragma unroll

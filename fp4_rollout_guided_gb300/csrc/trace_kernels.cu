@@ -141,20 +141,6 @@ __device__ __forceinline__ uint32_t compact_word(uint32_t c0, uint32_t c1) {
 // a2: rollout quantisation
 // ---------------------------------------------------------------------------
 
-// The two block maxima of a chunk (bf16 abs-max on the raw words).
-__device__ __forceinline__ void chunk_bamax(const Chunk& cur, float& b0, float& b1) {
-  uint32_t m[2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    const uint32_t* w = cur.w + 8 * b;
-    const uint32_t m01 = absmax_bf16x2(absmax_bf16x2(w[0], w[1]), absmax_bf16x2(w[2], w[3]));
-    const uint32_t m23 = absmax_bf16x2(absmax_bf16x2(w[4], w[5]), absmax_bf16x2(w[6], w[7]));
-    m[b] = absmax_lanes_bits(absmax_bf16x2(m01, m23));
-  }
-  b0 = __uint_as_float(m[0]);
-  b1 = __uint_as_float(m[1]);
-}
-
 // Per-segment table of 1/S for every E4M3 code (S = dec(code) * gs), built
 // by the n threads tid = 0..n-1 of a CTA or warp group.
 __device__ __forceinline__ void build_inv_tab(float* inv, float gs, int tid, int n) {
