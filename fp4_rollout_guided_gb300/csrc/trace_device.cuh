@@ -320,6 +320,15 @@ __device__ __forceinline__ F2 fma2_rn(F2 a, F2 b, F2 c) {
   return d;
 }
 
+__device__ __forceinline__ F2 fma2_rz(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("{ .reg .b64 A, B, C, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; "
+      "mov.b64 C, {%6, %7}; fma.rz.f32x2 D, A, B, C; mov.b64 {%0, %1}, D; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
 
 // Multiply-add on the FMA pipe (IMAD): a * b + c, wrapping.
@@ -329,11 +338,6 @@ __device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-__device__ __forceinline__ float fma_sat(float a, float b, float c) {
-  float d;
-  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 // ---------------------------------------------------------------------------
 // E2M1
@@ -366,18 +370,17 @@ __device__ __forceinline__ uint32_t e2m1x8(F2 p0, F2 p1, F2 p2, F2 p3) {
 }
 
 // The rounding constant for a pair of clamped values t in [0, 6]:
-// C = 1.5 * 2^(22 + e) with 2^e the binade of max(t, 1), built on the FMA
-// pipe from two saturating indicators, b1 = [t > 2] and b2 = [t > 4]
-// (sat(t * 2^30 - 2^31) is 0 for t <= 2 and 1 otherwise: the next binary32
-// above 2 is 2 + 2^-22), then C = K * (1 + b1) * (1 + b2), K = 1.5 * 2^22.
-// At t = 2 or 4 either constant puts the (on-grid) value on the grid, so
-// the boundary side does not matter.
+// C = 1.5 * 2^(22 + e) with 2^e the binade of max(t, 1), on the FMA pipe in
+// three instructions.  u = fl_rz(t * m + 2^23) with m = 0.5 - 2^-25 holds
+// F = floor(t * m) in its low significand bits (t * m < 3 stays below one
+// ulp of 2^23 times 3), and F is e: t * m < 1 for t < 2, < 2 for t < 4, and
+// 6 * m < 3; only t = 2 and t = 4 exactly fall one binade low, where either
+// constant puts the on-grid value on the grid.  bits(u) * 2^23 adds F to the
+// exponent field of K = 1.5 * 2^22 (bits(2^23) * 2^23 vanishes mod 2^32).
 __device__ __forceinline__ F2 magic_pair(F2 tc) {
-  const float k = 0x1.8p22f;
-  const F2 b1 = {fma_sat(tc.x, 0x1p30f, -0x1p31f), fma_sat(tc.y, 0x1p30f, -0x1p31f)};
-  const F2 b2 = {fma_sat(tc.x, 0x1p30f, -0x1p32f), fma_sat(tc.y, 0x1p30f, -0x1p32f)};
-  const F2 m1 = fma2_rn(b1, splat(k), splat(k));
-  return fma2_rn(b2, m1, m1);
+  const F2 u = fma2_rz(tc, splat(0x1.fffffep-2f), splat(0x1p23f));
+  return F2{__uint_as_float(imad(__float_as_uint(u.x), 1u << 23, 0x4AC00000u)),
+            __uint_as_float(imad(__float_as_uint(u.y), 1u << 23, 0x4AC00000u))};
 }
 
 // Rollout-frame decode of a pair from the compact record: for each element
