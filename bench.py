@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of the guided-NVFP4 hot path of TRACE on GB300.
 
-One step = one pass of the whole path over one batch of the workload:
+One step = one pass of the whole hot path over one batch of the workload:
   rollout side:  segment amax + NVFP4 quantisation with the compact record
   record:        guide pack (codes -> compact words), guide unpack (round trip)
   training side: segment amax + rollout-guided fake quantisation (bf16 out,
@@ -11,16 +11,21 @@ tokens x 4 heads x 128, 6.44 G elements per tensor, guide in 4096-token
 chunks).  Inputs are synthetic (seeded generators), resident in HBM, and far
 larger than L2, so no flush is needed between steps.
 
-Metric: algorithmic bytes in + out of every kernel of the step per second
-(GB/s = 1e9 B/s); per-kernel GB/s and the HBM-roofline fraction of the
-dominant kernel come from CUDA events recorded by the library around each
-launch on its own stream.
+Metric: the guided fake quantiser's GB/s (its algorithmic bytes in + out,
+4.4375 B per element with the compact record, 4.6875 with the full one,
+1 GB/s = 1e9 B/s) from CUDA events the library records around each launch
+on the launch's own stream, and its fraction of the measured HBM copy peak.
+The whole step's row bytes per second are reported beside it (step_gbs), and
+so are the other four workloads (per-kernel GB/s, elements/s, roofline
+fraction, mismatch rates before and after guidance; compact-vs-full
+agreement on the 262144 x 4096 expert activations).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
                   [--guide compact|full] [--impl ours|reference]
 
 ``--impl reference`` times the CPU oracle (the plain single-threaded
-definition) on bounded samples of the same workload.
+definition, run segment-parallel on every host core) on bounded samples of
+the same workload, with the same metric.
 """
 from __future__ import annotations
 
@@ -199,18 +204,79 @@ def oracle_sample(w, rows):
     return synth.to_u16(x[:rows]), synth.to_u16(r[:rows]), seg_r
 
 
-def oracle_step(xu, ru, seg_r, guide_kind):
+def oracle_step(xu, ru, seg_r, guide_kind, amax_t=None):
+    """One step of the oracle on a sample (rows of one training segment)."""
     import oracle
     codes, bs, gs, guide = oracle.rollout_quant(ru, seg_r)
     oracle.guide_pack(codes)
     oracle.guide_unpack(ru, guide, bs, gs, seg_r)
     kind = oracle.GUIDE_COMPACT if guide_kind == "compact" else oracle.GUIDE_FULL
     oracle.train_fakequant(xu, None, kind, guide if guide_kind == "compact" else codes, bs, gs,
-                           seg_r, want_codes=False, want_stats=False)
+                           seg_r, want_codes=False, want_stats=False,
+                           amax_t=None if amax_t is None else [amax_t])
+
+
+def row_pieces(seg_r, piece_rows=512):
+    """(first row, end row, rollout segment) pieces of at most piece_rows
+    rows that never cross a rollout segment boundary."""
+    out = []
+    for k, (a, b) in enumerate(zip(seg_r[:-1], seg_r[1:])):
+        for p in range(int(a), int(b), piece_rows):
+            out.append((p, min(p + piece_rows, int(b)), k))
+    return out
+
+
+def parallel_maxima(u, seg, n_threads):
+    """Per-segment maxima of |u| on a thread pool (exact: a max of maxima)."""
+    import oracle
+    pieces = row_pieces(seg)
+    part = oracle.parallel_map(lambda q: (q[2], float(oracle.segment_amax(u[q[0]:q[1]])[0])),
+                               pieces, n_threads)
+    m = np.zeros(len(seg) - 1, dtype=np.float32)
+    for k, v in part:
+        m[k] = max(m[k], v)
+    return m
+
+
+def oracle_step_parallel(xu, ru, seg_r, guide_kind, n_threads=None):
+    """The same step on every host core.  The sample's training maximum and
+    each rollout segment's maximum come first (maxima of row pieces); then
+    every piece of rows is quantised, packed, unpacked and fake-quantised on
+    its own with those maxima given, which is the whole step's result
+    (segments are independent once their maxima are known)."""
+    import oracle
+    seg = [0, xu.shape[0]]
+    amax_t = float(parallel_maxima(xu, seg, n_threads)[0])
+    amax_r = parallel_maxima(ru, seg_r, n_threads)
+    kind = oracle.GUIDE_COMPACT if guide_kind == "compact" else oracle.GUIDE_FULL
+
+    def piece(q):
+        a, b, k = q
+        codes, bs, gs, guide = oracle.rollout_quant(ru[a:b], None, amax=amax_r[k:k + 1])
+        oracle.guide_pack(codes)
+        oracle.guide_unpack(ru[a:b], guide, bs, gs, None)
+        oracle.train_fakequant(xu[a:b], None, kind, guide if guide_kind == "compact" else codes,
+                               bs, gs, None, want_codes=False, want_stats=False,
+                               amax_t=[amax_t])
+    oracle.parallel_map(piece, row_pieces(seg_r), n_threads)
+
+
+def oracle_fakequant_parallel(xu, gd, bs, gs, seg_r, guide_kind, n_threads=None):
+    """The oracle's guided fake quantiser alone (the metric's kernel) on
+    every host core: the training maximum first, then pieces of rows."""
+    import oracle
+    amax_t = float(parallel_maxima(xu, [0, xu.shape[0]], n_threads)[0])
+    kind = oracle.GUIDE_COMPACT if guide_kind == "compact" else oracle.GUIDE_FULL
+    oracle.parallel_map(
+        lambda q: oracle.train_fakequant(xu[q[0]:q[1]], None, kind, gd[q[0]:q[1]], bs[q[0]:q[1]],
+                                         gs[q[2]:q[2] + 1], None, want_codes=False,
+                                         want_stats=False, amax_t=[amax_t]),
+        row_pieces(seg_r), n_threads)
 
 
 def oracle_rows_for(w, seconds, guide_kind):
-    """Rows of a sample that takes about `seconds` of oracle time."""
+    """Rows of a sample that takes about `seconds` of single-threaded oracle
+    time, in whole rollout segments."""
     probe = max(w.seg_r[1] - w.seg_r[0], 1) if w.n_seg_r > 1 else 256
     probe = int(min(probe, 4096 if w.cols <= 256 else 256))
     xu, ru, sr = oracle_sample(w, probe)
@@ -225,43 +291,63 @@ def oracle_rows_for(w, seconds, guide_kind):
 
 
 def cpu_baseline(w, guide_kind, seconds=12.0):
+    """The oracle timed on a bounded sample of the workload, single-threaded
+    and segment-parallel on every host core; GB/s of the step's bytes."""
     import oracle
     oracle.build()
     rows = oracle_rows_for(w, seconds, guide_kind)
     xu, ru, sr = oracle_sample(w, rows)
+    elems = xu.size
     t = time.perf_counter()
     oracle_step(xu, ru, sr, guide_kind)
-    dt = time.perf_counter() - t
-    elems = xu.size
-    gbs = step_bytes_per_elem(guide_kind) * elems / dt / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"rows 0..{rows} of training segment 0 ({elems} elements, "
-                      f"{len(sr) - 1} rollout segments), one full step, {dt:.2f} s"}
+    dt1 = time.perf_counter() - t
+    n = oracle.threads()
+    t = time.perf_counter()
+    oracle_step_parallel(xu, ru, sr, guide_kind, n)
+    dtn = time.perf_counter() - t
+    bpe = step_bytes_per_elem(guide_kind)
+    sample = (f"rows 0..{rows} of training segment 0 ({elems} elements, {len(sr) - 1} rollout "
+              f"segments), one full step")
+    return {"value": bpe * elems / dtn / 1e9, "unit": "GB/s", "cores": n, "threads": n,
+            "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": sample + f", segment-parallel on {n} threads, {dtn:.2f} s",
+            "single_thread": {"value": bpe * elems / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": sample + f", one thread, {dt1:.2f} s"}}
 
 
 def run_reference(args, w):
+    """The reference arm: the CPU oracle's guided fake quantiser (the metric's
+    kernel), segment-parallel on every host core, on a sample of the same
+    workload; rollout record from the oracle's own rollout quantiser."""
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return 0
     import oracle
     oracle.build()
-    rows = oracle_rows_for(w, 1.5, args.guide)
+    rows = oracle_rows_for(w, 6.0, args.guide)
     xu, ru, sr = oracle_sample(w, rows)
+    codes, bs, gs, guide = oracle.rollout_quant(ru, sr)
+    gd = guide if args.guide == "compact" else codes
+    n = oracle.threads()
     for _ in range(args.warmup):
-        oracle_step(xu, ru, sr, args.guide)
+        oracle_fakequant_parallel(xu, gd, bs, gs, sr, args.guide, n)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(xu, ru, sr, args.guide)
+        oracle_fakequant_parallel(xu, gd, bs, gs, sr, args.guide, n)
     dt = (time.perf_counter() - t) / max(args.steps, 1)
-    value = step_bytes_per_elem(args.guide) * xu.size / dt / 1e9
+    value = KERNEL_BYTES["fakequant_" + args.guide] * xu.size / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "sample_rows": rows, "sample_elements": int(xu.size)},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: rows 0..{rows} of training segment 0 "
-                                       f"({xu.size} elements)"},
+            "config": {"workload": w.name, "guide": args.guide, "sample_rows": rows,
+                       "sample_elements": int(xu.size)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "threads": n,
+                             "nproc": os.cpu_count(), "kind": "oracle",
+                             "sample": f"each step: the guided fake quantiser over rows "
+                                       f"0..{rows} of training segment 0 ({xu.size} elements, "
+                                       f"{len(sr) - 1} rollout segments), segment-parallel on "
+                                       f"{n} threads"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -283,6 +369,139 @@ def mem_available_bytes():
     return 0
 
 
+class StepRunner:
+    """Device buffers and the step of one workload through the public API."""
+
+    def __init__(self, h, w, x, r, kind, dev):
+        from fp4_rollout_guided_gb300 import trace
+        self.h, self.w, self.x, self.r, self.kind, self.dev = h, w, x, r, kind, dev
+        rows, cols = w.rows, w.cols
+        self.codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        self.bs = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+        self.gs = torch.empty((w.n_seg_r,), dtype=torch.float32, device=dev)
+        self.guide = torch.empty((rows, cols // 16), dtype=torch.int32, device=dev)
+        self.packed = torch.empty_like(self.guide)
+        self.unpacked = torch.empty_like(self.codes)
+        self.y = torch.empty_like(x)
+        self.mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
+        self.trace = trace
+
+    def step(self, xd=None, rd=None, stats=None, kind=None):
+        xd = self.x if xd is None else xd
+        rd = self.r if rd is None else rd
+        kind = kind or self.kind
+        w, h = self.w, self.h
+        h.rollout_quant(rd, w.seg_r, out=(self.codes, self.bs, self.gs, self.guide))
+        h.guide_pack(self.codes, out=self.packed)
+        h.guide_unpack(rd, self.guide, self.bs, self.gs, w.seg_r, out=self.unpacked)
+        h.train_fakequant(xd, w.seg_t, kind, self.guide if kind == "compact" else self.codes,
+                          self.bs, self.gs, w.seg_r, out=(self.y, self.mask, None), stats=stats)
+
+    def check(self):
+        """One step with the counters: the record's round trip and the
+        train/rollout mismatch statistics."""
+        st = self.trace.new_stats(self.dev)
+        self.step(stats=st)
+        torch.cuda.synchronize()
+        ok = bool(torch.equal(self.packed, self.guide) and torch.equal(self.unpacked, self.codes))
+        return ok, self.trace.stats_dict(st)
+
+    def timed(self, steps, warmup, dist=None, kind=None):
+        """(ms per step from events around the K steps, per-kernel
+        (launches, total ms) from the library's launch events over the
+        same number of steps again)."""
+        for _ in range(warmup):
+            self.step(kind=kind)
+        torch.cuda.synchronize()
+        barrier(dist)
+        stream = torch.cuda.current_stream()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            self.step(kind=kind)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        ms = ev0.elapsed_time(ev1) / max(steps, 1)
+        self.h.profile(True)
+        for _ in range(steps):
+            self.step(kind=kind)
+        times = self.h.collect()
+        self.h.profile(False)
+        torch.cuda.synchronize()
+        return ms, times
+
+
+def kernel_table(times, kind, elems, peak):
+    kernels = {}
+    for name, (n, tot) in times.items():
+        if n == 0:
+            continue
+        b = kernel_bytes(name, kind)
+        avg = tot / n
+        gbs = b * elems / (avg * 1e-3) / 1e9
+        kernels[name] = {"launches": n, "avg_ms": round(avg, 4), "bytes_per_elem": b,
+                         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+                         "elements_per_s": round(elems / (avg * 1e-3), 1)}
+    return kernels
+
+
+def mismatch_of(stats):
+    n = max(stats["n_elems"], 1)
+    return {"rtn_rate": stats["mismatch_rtn"] / n, "guided_rate": stats["mismatch_guided"] / n,
+            "hist_rtn": stats["hist_rtn"], "hist_guided": stats["hist_guided"]}
+
+
+def agreement_compact_full(h, w, run):
+    """Fraction of elements whose guided code from the compact record equals
+    the one from the full record (same training values, same rollout record)."""
+    _, _, ct, _ = h.train_fakequant(run.x, w.seg_t, "compact", run.guide, run.bs, run.gs, w.seg_r,
+                                    mask=False, codes=True)
+    _, _, cf, _ = h.train_fakequant(run.x, w.seg_t, "full", run.codes, run.bs, run.gs, w.seg_r,
+                                    mask=False, codes=True)
+    d = torch.bitwise_xor(ct, cf)
+    same = ((d & 0x0F) == 0).sum(dtype=torch.int64) + ((d >> 4) == 0).sum(dtype=torch.int64)
+    return float(same.item()) / w.elems
+
+
+def other_configs(args, h, dev, peak, skip):
+    """The other workloads, one after another: per-kernel GB/s, elements/s,
+    roofline fraction, mismatch before/after guidance, L2 flag; the expert
+    activations 262144 x 4096 add the full-vs-compact comparison."""
+    from fp4_rollout_guided_gb300 import synth
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for cfg in (1, 2, 3, 4, 5):
+        if cfg == skip:
+            continue
+        w = synth.workload(cfg, seed=args.seed)
+        x, r = synth.make_inputs(w, dev)
+        run = StepRunner(h, w, x, r, "compact", dev)
+        ok, stats = run.check()
+        steps = max(args.steps, 5)
+        ms, times = run.timed(steps, args.warmup)
+        kernels = kernel_table(times, "compact", w.elems, peak)
+        fq = kernels["fakequant"]
+        ws = int(KERNEL_BYTES["fakequant_compact"] * w.elems)
+        entry = {"workload": w.name, "elements": w.elems, "segments_train": w.n_seg_t,
+                 "segments_rollout": w.n_seg_r, "guide": "compact",
+                 "fakequant_gbs": fq["gbs"], "fakequant_frac_of_hbm": fq["frac_of_hbm"],
+                 "elements_per_s": fq["elements_per_s"], "ms_per_step": round(ms, 4),
+                 "step_gbs": round(step_bytes_per_elem("compact") * w.elems / (ms * 1e-3) / 1e9, 1),
+                 "kernels": kernels, "mismatch": mismatch_of(stats), "record_round_trip_ok": ok,
+                 "fakequant_bytes": ws, "l2_bytes": l2, "l2_resident": ws <= l2}
+        if cfg == 4:
+            _, tf = run.timed(steps, args.warmup, kind="full")
+            kf = kernel_table(tf, "full", w.elems, peak)["fakequant"]
+            entry["full_guide"] = {"fakequant_gbs": kf["gbs"], "fakequant_frac_of_hbm":
+                                   kf["frac_of_hbm"], "elements_per_s": kf["elements_per_s"]}
+            entry["agreement_compact_vs_full"] = agreement_compact_full(h, w, run)
+        out[str(cfg)] = entry
+        del run, x, r
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w0):
     from fp4_rollout_guided_gb300 import build, shard, synth, trace
     world, rank, local = dist_env()
@@ -299,88 +518,49 @@ def run_ours(args, w0):
 
     t_gen = time.perf_counter()
     x, r = synth.make_inputs(w, dev)
-    rows, cols = w.rows, w.cols
-    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
-    bs = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
-    gs = torch.empty((w.n_seg_r,), dtype=torch.float32, device=dev)
-    guide = torch.empty((rows, cols // 16), dtype=torch.int32, device=dev)
-    packed = torch.empty_like(guide)
-    unpacked = torch.empty_like(codes)
-    y = torch.empty_like(x)
-    mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
+    kind = args.guide
+    run = StepRunner(h, w, x, r, kind, dev)
     torch.cuda.synchronize()
     t_gen = time.perf_counter() - t_gen
-    kind = args.guide
-
-    def step(xd, rd, stats=None):
-        h.rollout_quant(rd, w.seg_r, out=(codes, bs, gs, guide))
-        h.guide_pack(codes, out=packed)
-        h.guide_unpack(rd, guide, bs, gs, w.seg_r, out=unpacked)
-        h.train_fakequant(xd, w.seg_t, kind, guide if kind == "compact" else codes, bs, gs,
-                          w.seg_r, out=(y, mask, None), stats=stats)
 
     # correctness guard: the round trip of the record and stats of one step
-    st = trace.new_stats(dev)
-    step(x, r, st)
-    torch.cuda.synchronize()
-    stats = trace.stats_dict(st)
-    record_ok = bool(torch.equal(packed, guide) and torch.equal(unpacked, codes))
+    record_ok, stats = run.check()
 
     clocks = ClockSampler(local) if rank == 0 else None
-    for _ in range(args.warmup):
-        step(x, r)
-    torch.cuda.synchronize()
-    barrier(dist)
-    stream = torch.cuda.current_stream()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step(x, r)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    ms = ev0.elapsed_time(ev1) / max(args.steps, 1)
+    ms, times = run.timed(args.steps, args.warmup, dist)
     ms = max_over_ranks(dist, ms, dev)
-
-    # per-kernel times from the library's own events, same steps again
-    h.profile(True)
-    for _ in range(args.steps):
-        step(x, r)
-    times = h.collect()
-    h.profile(False)
-    torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
 
     waits = h.device_status()           # 0, or 6 if an in-kernel wait ran out
     if waits != 0:
         raise SystemExit("an in-kernel wait ran out during the timed steps")
     launches = sum(n for n, _ in times.values())
-    bpe = step_bytes_per_elem(kind)
-    value = bpe * elems * world / (ms * 1e-3) / 1e9
-    fused = times.get("rollout_fused", (0, 0.0))[0] > 0
     peak, peak_src = load_peaks()
-    kernels = {}
-    for name, (n, tot) in times.items():
-        if n == 0:
-            continue
-        b = kernel_bytes(name, kind)
-        avg = tot / n
-        gbs = b * elems / (avg * 1e-3) / 1e9
-        kernels[name] = {"launches": n, "avg_ms": round(avg, 4), "bytes_per_elem": b,
-                         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
-    dom = max(kernels, key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
-    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
-            "unit": "GB/s", "frac": round(kernels[dom]["gbs"] / peak, 4),
-            "traffic": measured_traffic(kind, elems) if dom == "fakequant" else None,
-            "traffic_unit": "GB per launch", "peak_source": peak_src}
+    kernels = kernel_table(times, kind, elems, peak)
+    # the metric: the guided fake quantiser's bytes over its own launch time
+    fq_ms = max_over_ranks(dist, kernels["fakequant"]["avg_ms"], dev)
+    value = KERNEL_BYTES["fakequant_" + kind] * elems * world / (fq_ms * 1e-3) / 1e9
+    bpe = step_bytes_per_elem(kind)
+    step_gbs = bpe * elems * world / (ms * 1e-3) / 1e9
+    fused = times.get("rollout_fused", (0, 0.0))[0] > 0
+    roof = {"bound": "hbm", "kernel": "fakequant", "achieved": round(value / world, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(value / world / peak, 4),
+            "traffic": measured_traffic(kind, elems), "traffic_unit": "GB per launch",
+            "peak_source": peak_src,
+            "bytes_per_launch": round(KERNEL_BYTES["fakequant_" + kind] * elems / 1e9, 3)}
 
-    e2e = measure_e2e(args, h, w, x, r, step, dev, bpe, (y, mask, guide, bs, gs)) \
-        if not args.no_e2e else None
+    e2e = measure_e2e(args, h, w, x, r, run.step, dev, bpe,
+                      (run.y, run.mask, run.guide, run.bs, run.gs)) if not args.no_e2e else None
     e2e_v = None if e2e is None else max_over_ranks(dist, e2e["ms"], dev)
+    del run, x, r
+    torch.cuda.empty_cache()
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(w, kind)
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = other_configs(args, h, dev, peak, skip=w0.cfg)
 
     if rank == 0:
         line = {
@@ -393,22 +573,30 @@ def run_ours(args, w0):
                        "guide": kind,
                        "step": ("rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
                        + ", guide_pack, guide_unpack, amax+guided_fakequant",
+                       "value_bytes_per_elem": KERNEL_BYTES["fakequant_" + kind],
                        "step_bytes_per_elem": bpe,
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replica-per-gpu x{world}"},
             "percent_of_hbm_peak": round(100 * value / world / peak, 2),
+            "elements_per_s": round(elems * world / (fq_ms * 1e-3), 1),
+            "step_gbs": round(step_gbs, 1),
+            "step_percent_of_hbm_peak": round(100 * step_gbs / world / peak, 2),
             "kernels": kernels, "roofline": roof, "gpu_launches": launches,
             "clocks": clk, "cpu_baseline": base,
             "e2e": None if e2e is None else {
-                "value": round(bpe * e2e["elems"] * world / (e2e_v * 1e-3) / 1e9, 1),
+                "value": round(KERNEL_BYTES["fakequant_" + kind] * e2e["elems"] * world
+                               / (e2e_v * 1e-3) / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_v, 3), "scope": e2e["scope"],
+                "measures": "the fake quantiser's bytes per element over the time of the whole "
+                            "step through the public API, inputs from and outputs to pinned "
+                            "host memory",
+                "step_gbs": round(bpe * e2e["elems"] * world / (e2e_v * 1e-3) / 1e9, 1),
                 "pipeline": "per training segment: H2D (x, r on two streams), kernels, D2H overlap",
                 "matches_device_step": e2e["matches_device_step"]},
-            "mismatch": {"rtn_rate": stats["mismatch_rtn"] / max(stats["n_elems"], 1),
-                         "guided_rate": stats["mismatch_guided"] / max(stats["n_elems"], 1),
-                         "hist_rtn": stats["hist_rtn"], "hist_guided": stats["hist_guided"]},
+            "mismatch": mismatch_of(stats),
             "record_round_trip_ok": record_ok,
+            "configs": configs,
             "generation_s": round(t_gen, 2),
         }
         print(json.dumps(line), flush=True)
@@ -669,6 +857,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload report of the other four workloads")
     ap.add_argument("--no-fuse", action="store_true",
                     help="rollout side as two kernels (amax, then quantiser)")
     ap.add_argument("--backward", action="store_true",

@@ -95,6 +95,27 @@ def _load():
         return lib
 
 
+def threads() -> int:
+    """Host threads the segment-parallel helpers use: every core."""
+    return max(1, os.cpu_count() or 1)
+
+
+def parallel_map(fn, items, n_threads=None):
+    """``[fn(item) for item in items]`` on a pool of host threads.
+
+    The oracle's C functions are single-threaded and independent per call;
+    ctypes releases the interpreter lock while one runs, so calls on
+    disjoint segments proceed on all cores at once.  Results keep the
+    order of ``items``."""
+    from concurrent.futures import ThreadPoolExecutor
+    items = list(items)
+    n = min(n_threads or threads(), max(1, len(items)))
+    if n == 1:
+        return [fn(it) for it in items]
+    with ThreadPoolExecutor(n) as ex:
+        return list(ex.map(fn, items))
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
