@@ -187,6 +187,12 @@ __device__ __forceinline__ void train_bracket(F2 t, F2& C, F2& sz, F2& sp) {
   sp = add2_rp(tc, C);
 }
 
+// sat(4 a): 0 for a <= 0, 1 for a >= 1/4.
+__device__ __forceinline__ float sat4(float a) {
+  float d;
+  asm("mul.rn.sat.f32 %0, %1, 0f40800000;" : "=f"(d) : "f"(a));
+  return d;
+}
 #ifndef TFP4_FQ_MIN_CTAS
 #define TFP4_FQ_MIN_CTAS 4
 #endif
@@ -350,8 +356,20 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           // us clamped to [sz, sp], on the FMA pipe: us - sz is a multiple of
           // the grid spacing (>= 0.5) or <= 0, so h = sat(4 (us - sz)) is
           // exactly 1 or 0, and g = glo + h (ghi - glo) is the chosen point
-          const F2 yc = {fminf(fmaxf(us.x, sz.x), sp.x), fminf(fmaxf(us.y, sz.y), sp.y)};
-          const F2 g = sub2_rn(yc, C);
+          // the chosen point g: us clamped to [sz, sp], minus C.  With the
+          // compact record the ALU pipe is lighter than the FMA pipe, so the
+          // clamp is two min/max; with the full record the other way round,
+          // so it is done on the FMA pipe: us - sz is a multiple of the grid
+          // spacing (>= 0.5) or <= 0, h = sat(4 (us - sz)) is exactly 1 or 0,
+          // and g = glo + h (ghi - glo).
+          F2 g;
+          if (KIND == TRACE_GUIDE_COMPACT) {
+            const F2 yc = {fminf(fmaxf(us.x, sz.x), sp.x), fminf(fmaxf(us.y, sz.y), sp.y)};
+            g = sub2_rn(yc, C);
+          } else {
+            const F2 dl = sub2_rn(us, sz);
+            g = fma2_rn(F2{sat4(dl.x), sat4(dl.y)}, sub2_rn(sp, sz), sub2_rn(sz, C));
+          }
           const F2 ym = mul2_rn(g, splat(pt.S[b]));
           ybits[i & 3] = bf16x2_rn(ym.x, ym.y) | (w & 0x80008000u);
           if ((i & 3) == 3)
