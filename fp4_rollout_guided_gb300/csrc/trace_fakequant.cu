@@ -56,14 +56,16 @@ __device__ __forceinline__ void count(Counters& k, int k_r, int k_rtn, int k_g) 
   k.h_g[3] += d1 >= 3;
 }
 
-// A packed product that an add or subtract consumes goes through this
-// first.  The code generator may fuse a packed multiply into the packed add
-// that follows it (it did so for the distances below, even with explicit
-// round-to-nearest on both instructions), which skips the product's own
-// rounding and changes near-tie decisions.  Multiplying the rounded product
-// by a 1.0 known only at run time (a kernel argument) makes any such fusion
-// harmless: a fused p * 1 + c rounds once, to fl(p + c).
-__device__ __forceinline__ F2 rounded(F2 p, float one) { return mul2_rn(p, splat(one)); }
+// A packed product that an add or subtract consumes is formed by this.  The
+// code generator may fuse a packed multiply into the packed add that follows
+// it (it did so for the distances below, even with explicit round-to-nearest
+// on both instructions), which skips the product's own rounding and changes
+// near-tie decisions.  An explicit FMA with a -0 addend known only at run
+// time (a kernel argument) is the rounded product itself (adding -0 changes
+// no value, +0 included) and cannot be fused into anything further.
+__device__ __forceinline__ F2 mul2_kept(F2 a, F2 b, float nzero) {
+  return fma2_rn(a, b, splat(nzero));
+}
 
 // Training side of one pair of elements.  ax holds |x|; St holds the
 // training scale carrying each element's sign, vr the rollout's
@@ -78,7 +80,7 @@ __device__ __forceinline__ F2 rounded(F2 p, float one) { return mul2_rn(p, splat
 // rtn_hi - 1 >= 0 as a signed integer; the select is done on the bit
 // patterns: y = v_hi - lo * (v_hi - v_lo) with lo = 0 or 1.
 template <bool GUIDED, bool WANT_G>
-__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, float one, F2& ym,
+__device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, float nzero, F2& ym,
                                            F2& gsel, F2& grtn) {
   const F2 t = mul2_rn(ax, splat(inv_t));
   const F2 tc = {fminf(t.x, 6.0f), fminf(t.y, 6.0f)};
@@ -93,9 +95,8 @@ __device__ __forceinline__ void train_pair(F2 ax, float inv_t, F2 St, F2 vr, flo
   }
   const F2 sz = add2_rz(tc, C), sp = add2_rp(tc, C);
   const F2 glo = sub2_rn(sz, C), ghi = sub2_rn(sp, C);
-  const F2 vlo = rounded(mul2_rn(glo, St), one), vhi = rounded(mul2_rn(ghi, St), one);
-  const F2 vrr = rounded(vr, one);
-  const F2 dlo = sub2_rn(vlo, vrr), dhi = sub2_rn(vhi, vrr);
+  const F2 vlo = mul2_kept(glo, St, nzero), vhi = mul2_kept(ghi, St, nzero);
+  const F2 dlo = sub2_rn(vlo, vr), dhi = sub2_rn(vhi, vr);
   const float diff0 = __fsub_rn(fabsf(dlo.x), fabsf(dhi.x));
   const float diff1 = __fsub_rn(fabsf(dlo.y), fabsf(dhi.y));
   const uint32_t lo0 = (__float_as_uint(diff0) + __float_as_uint(sn.x) + ~__float_as_uint(sz.x)) >> 31;
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
                 const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
                 const float* __restrict__ gs_r, uint8_t* __restrict__ y,
                 uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
-                trace_stats_t* __restrict__ stats, float one) {
+                trace_stats_t* __restrict__ stats, float nzero) {
   constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
   const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
   uint32_t step = blockIdx.x * steps_per_cta;
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
             const uint32_t rel = w ^ (imad(U[b], 1u << (15 - j0), 0u) & 0x80008000u);
             const F2 xl = lanes(rel);
             train_bracket(mul2_rn(xl, splat(pt.inv[b])), C, sz, sp);
-            const F2 tr = rounded(mul2_rn(xl, splat(pr.inv[b])), one);
+            const F2 tr = mul2_kept(xl, splat(pr.inv[b]), nzero);
             const F2 uz = add2_rz(tr, C), up = add2_rp(tr, C);
             const uint32_t gw = b ? gcur.y : gcur.x;
             const uint32_t b0 = 1u << (16 + j0), b1 = 1u << (17 + j0);
@@ -398,18 +399,18 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
             const uint32_t sr0 = imad(gw, 1u << (31 - j0), 0u) & 0x80000000u;
             const uint32_t sr1 = imad(gw, 1u << (30 - j0), 0u) & 0x80000000u;
             const uint32_t Sb = __float_as_uint(pr.S[b]);
-            vr = mul2_rn(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)});
+            vr = mul2_kept(gr, F2{__uint_as_float(Sb | sr0), __uint_as_float(Sb | sr1)}, nzero);
             if (STATS) grs = F2{__uint_as_float(__float_as_uint(gr.x) | sr0),
                                 __uint_as_float(__float_as_uint(gr.y) | sr1)};
           } else if (KIND == TRACE_GUIDE_FULL) {
             const uint32_t gword = (i < 4) ? gcur.x : (i < 8) ? gcur.y : (i < 12) ? gcur.z : gcur.w;
             float g0, g1;
             e2m1x2_values((gword >> (8 * (i & 3))) & 0xFFu, g0, g1);
-            vr = mul2_rn(F2{g0, g1}, splat(pr.S[b]));
+            vr = mul2_kept(F2{g0, g1}, splat(pr.S[b]), nzero);
             if (STATS) grs = F2{g0, g1};
           }
           F2 ym, gsel, grtn;
-          train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, one, ym, gsel, grtn);
+          train_pair<GUIDED, CODES || STATS>(ax, pt.inv[b], St, vr, nzero, ym, gsel, grtn);
           ybits[i & 3] = bf16x2_rn(ym.x, ym.y);
           if ((i & 3) == 3)
             st_stream(y + (uint64_t)c * 64u + 16 * (i >> 2), ybits[0], ybits[1], ybits[2], ybits[3]);
@@ -476,7 +477,7 @@ cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegPa
                                     FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
                                     seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
                                     a.gs_r, (uint8_t*)a.y, (uint8_t*)a.mask,
-                                    (uint8_t*)a.codes_t, a.stats, 1.0f);
+                                    (uint8_t*)a.codes_t, a.stats, -0.0f);
   return cudaGetLastError();
 }
 
