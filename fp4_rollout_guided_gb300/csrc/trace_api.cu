@@ -10,6 +10,7 @@
 
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -45,9 +46,46 @@ struct trace_ctx {
   size_t gemm_ws_bytes = 0;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> spare;  // recycled timing events
+  const void* scratch_base = nullptr;  // the one scratch allocation
+  size_t scratch_bytes = 0;
+  bool dbg_shrink = false;  // debug builds: register outputs 16 bytes short
 };
 
 namespace {
+
+// Debug builds: registers the byte ranges the call's launches may touch
+// (its buffers, and the handle's scratch), stream-ordered before them.
+// Outputs are registered 16 bytes short while the test option asks for it.
+struct DbgBuf {
+  const void* p;
+  int64_t bytes;
+  bool out;
+};
+cudaError_t dbg_register(const trace_ctx* h, cudaStream_t st, std::initializer_list<DbgBuf> bufs,
+                         const void* extra = nullptr, int64_t extra_bytes = 0) {
+#ifdef TRACE_DEBUG_BOUNDS
+  tfp4::DbgRanges r;
+  memset(&r, 0, sizeof(r));
+  auto add = [&](const void* p, int64_t n) {
+    if (p && n > 0 && r.n < (uint32_t)tfp4::kDbgRanges) {
+      r.lo[r.n] = (uint64_t)p;
+      r.hi[r.n] = (uint64_t)p + (uint64_t)n;
+      ++r.n;
+    }
+  };
+  for (const DbgBuf& b : bufs) add(b.p, b.bytes - ((b.out && h && h->dbg_shrink) ? 16 : 0));
+  if (h) add(h->scratch_base, (int64_t)h->scratch_bytes);
+  add(extra, extra_bytes);
+  return tfp4::dbg_set_ranges(r, st);
+#else
+  (void)h;
+  (void)st;
+  (void)bufs;
+  (void)extra;
+  (void)extra_bytes;
+  return cudaSuccess;
+#endif
+}
 
 // Makes the handle's device current for the duration of a call.
 class DeviceGuard {
@@ -202,6 +240,8 @@ trace_status_t trace_create(trace_handle_t* out, int device) {
     delete h;
     return TRACE_ERR_CUDA;
   }
+  h->scratch_base = base;
+  h->scratch_bytes = bytes;
   h->scratch.amax_bits = (uint32_t*)base;
   h->scratch.done = (uint32_t*)(base + seg_bytes);
   h->scratch.gs_train = (float*)(base + seg_bytes + 256);
@@ -248,6 +288,14 @@ trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t va
       if (value != 0 && value != 1) return TRACE_ERR_INVALID_ARG;
       h->wait_extra = (uint32_t)value;
       return TRACE_OK;
+    case TRACE_OPT_DEBUG_SHRINK:
+#ifdef TRACE_DEBUG_BOUNDS
+      if (value != 0 && value != 1) return TRACE_ERR_INVALID_ARG;
+      h->dbg_shrink = value != 0;
+      return TRACE_OK;
+#else
+      return TRACE_ERR_INVALID_ARG;
+#endif
   }
   return TRACE_ERR_INVALID_ARG;
 }
@@ -298,6 +346,12 @@ trace_status_t rollout_quant_impl(trace_handle_t h, const void* x_bf16, int64_t 
   const int64_t nchunks = rows * (cols / 32);
   const int32_t cpr = (int32_t)(cols / 32);
   const tfp4::MmaOut mma{(uint8_t*)bs_mma, (uint32_t)((cols / 16 + 3) / 4)};
+  if (e == cudaSuccess)
+    e = dbg_register(h, st, {{x_bf16, rows * cols * 2, false}, {codes_u8, rows * cols / 2, true},
+                             {bs_e4m3, rows * cols / 16, true},
+                             {bs_mma, bs_mma ? tfp4::mma_scales_bytes(rows, cols) : 0, true},
+                             {gs_f32, (int64_t)sizeof(float) * sp.n, true},
+                             {guide_bits, rows * cols / 4, true}});
   // the tile layout's padding (rows past a multiple of 128, scale columns
   // past a multiple of 4) is zero
   if (bs_mma && (rows % 128 != 0 || (cols / 16) % 4 != 0))
@@ -370,9 +424,12 @@ trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t 
   if (nchunks == 0) return TRACE_OK;
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const cudaError_t e = timed(h, TRACE_KERNEL_GUIDE_PACK, st, [&] {
-    return tfp4::launch_guide_pack(codes_u8, nchunks, guide_bits, h->sm_count, st);
-  });
+  cudaError_t e = dbg_register(h, st, {{codes_u8, rows * cols / 2, false},
+                                       {guide_bits, rows * cols / 4, true}});
+  if (e == cudaSuccess)
+    e = timed(h, TRACE_KERNEL_GUIDE_PACK, st, [&] {
+      return tfp4::launch_guide_pack(codes_u8, nchunks, guide_bits, h->sm_count, st);
+    });
   if (e != cudaSuccess) return cuda_fail(h, e);
   return TRACE_OK;
 }
@@ -395,10 +452,16 @@ trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
   if (nchunks == 0) return TRACE_OK;
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const cudaError_t e = timed(h, TRACE_KERNEL_GUIDE_UNPACK, st, [&] {
-    return tfp4::launch_guide_unpack(x_ref_bf16, guide_bits, bs_r, gs_r, nchunks,
-                                     (int32_t)(cols / 32), sp, codes_u8, h->sm_count, st);
-  });
+  cudaError_t e = dbg_register(h, st, {{x_ref_bf16, rows * cols * 2, false},
+                                       {guide_bits, rows * cols / 4, false},
+                                       {bs_r, rows * cols / 16, false},
+                                       {gs_r, (int64_t)sizeof(float) * sp.n, false},
+                                       {codes_u8, rows * cols / 2, true}});
+  if (e == cudaSuccess)
+    e = timed(h, TRACE_KERNEL_GUIDE_UNPACK, st, [&] {
+      return tfp4::launch_guide_unpack(x_ref_bf16, guide_bits, bs_r, gs_r, nchunks,
+                                       (int32_t)(cols / 32), sp, codes_u8, h->sm_count, st);
+    });
   if (e != cudaSuccess) return cuda_fail(h, e);
   return TRACE_OK;
 }
@@ -448,7 +511,16 @@ trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t ro
   cudaError_t e = begin_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   const int32_t cpr = (int32_t)(cols / 32);
-  if (!gs_t) {
+  if (e == cudaSuccess)
+    e = dbg_register(h, st, {{x_bf16, rows * cols * 2, false}, {y_bf16, rows * cols * 2, true},
+                             {ste_mask, rows * cols / 8, true}, {codes_t_u8, rows * cols / 2, true},
+                             {stats_dev, (int64_t)sizeof(trace_stats_t), true},
+                             {guide, kind == TRACE_GUIDE_FULL ? rows * cols / 2 : rows * cols / 4,
+                              false},
+                             {bs_r, rows * cols / 16, false},
+                             {gs_r, (int64_t)sizeof(float) * spr.n, false},
+                             {gs_t, (int64_t)sizeof(float) * spt.n, false}});
+  if (e == cudaSuccess && !gs_t) {
     e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
       return tfp4::launch_amax(x_bf16, nchunks, cpr, spt, h->scratch, h->scratch.gs_train,
                                h->sm_count, st);
@@ -521,7 +593,11 @@ trace_status_t trace_segment_amax(trace_handle_t h, const void* x_bf16, int64_t 
   cudaError_t e = begin_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   const int64_t nchunks = rows * (cols / 32);
-  if (nchunks == 0) {
+  if (e == cudaSuccess)
+    e = dbg_register(h, st, {{x_bf16, rows * cols * 2, false},
+                             {gs_f32, (int64_t)sizeof(float) * sp.n, true}});
+  if (e != cudaSuccess) {
+  } else if (nchunks == 0) {
     e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
   } else {
     e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
@@ -548,10 +624,14 @@ trace_status_t trace_ste_backward(trace_handle_t h, const void* grad_out_bf16,
   if (nchunks == 0) return TRACE_OK;
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const cudaError_t e = timed(h, TRACE_KERNEL_STE_BACKWARD, st, [&] {
-    return tfp4::launch_ste_backward(grad_out_bf16, ste_mask, nchunks, grad_in_bf16, h->sm_count,
-                                     st);
-  });
+  cudaError_t e = dbg_register(h, st, {{grad_out_bf16, rows * cols * 2, false},
+                                       {ste_mask, rows * cols / 8, false},
+                                       {grad_in_bf16, rows * cols * 2, true}});
+  if (e == cudaSuccess)
+    e = timed(h, TRACE_KERNEL_STE_BACKWARD, st, [&] {
+      return tfp4::launch_ste_backward(grad_out_bf16, ste_mask, nchunks, grad_in_bf16,
+                                       h->sm_count, st);
+    });
   if (e != cudaSuccess) return cuda_fail(h, e);
   return TRACE_OK;
 }
@@ -789,3 +869,36 @@ trace_status_t trace_profile_collect(trace_handle_t h, trace_kernel_time_t* out)
 }
 
 }  // extern "C"
+
+namespace tfp4 {
+
+cudaError_t dbg_set_ranges(const DbgRanges& r, cudaStream_t st) {
+  cudaError_t e = dbg_set_ranges_kernels(r, st);
+  if (e == cudaSuccess) e = dbg_set_ranges_fakequant(r, st);
+  return e;
+}
+
+unsigned long long dbg_take_violations() {
+  const unsigned long long a = dbg_take_kernels(), b = dbg_take_fakequant();
+  return (a == ~0ull || b == ~0ull) ? ~0ull : a + b;
+}
+
+}  // namespace tfp4
+
+extern "C" trace_status_t trace_debug_bounds(trace_handle_t h, int* checked,
+                                             uint64_t* violations) {
+  if (!h || !checked || !violations) return TRACE_ERR_INVALID_ARG;
+#ifdef TRACE_DEBUG_BOUNDS
+  DeviceGuard g(h->device);
+  *checked = 1;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  const unsigned long long v = tfp4::dbg_take_violations();
+  if (v == ~0ull) return cuda_fail(h, cudaGetLastError());
+  *violations = v;
+#else
+  *checked = 0;
+  *violations = 0;
+#endif
+  return TRACE_OK;
+}

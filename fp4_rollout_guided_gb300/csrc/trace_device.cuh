@@ -52,8 +52,30 @@ constexpr uint32_t kAbs2 = 0x7FFF7FFFu;
 // memory access
 // ---------------------------------------------------------------------------
 
+// Debug builds: every global access of the helpers below (and the direct
+// accesses marked TFP4_OK in the kernels) is checked against the ranges the
+// API registered for the call; one outside them is counted and skipped.
+#ifdef TRACE_DEBUG_BOUNDS
+__device__ DbgRanges g_dbg_ranges;
+__device__ unsigned long long g_dbg_violations;
+__device__ __noinline__ bool dbg_ok(const void* p, uint32_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  for (uint32_t i = 0; i < g_dbg_ranges.n && i < (uint32_t)kDbgRanges; ++i)
+    if (a >= g_dbg_ranges.lo[i] && a + bytes <= g_dbg_ranges.hi[i]) return true;
+  atomicAdd(&g_dbg_violations, 1ull);
+  return false;
+}
+#define TFP4_OK(p, bytes) dbg_ok((const void*)(p), (bytes))
+#else
+#define TFP4_OK(p, bytes) true
+#endif
+
+// A float from global memory (0 if a debug build finds it out of range).
+__device__ __forceinline__ float ldf(const float* p) { return TFP4_OK(p, 4) ? *p : 0.0f; }
+
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (!TFP4_OK(p, 16)) return v;
   asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(p));
@@ -61,33 +83,39 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 }
 
 __device__ __forceinline__ uint2 ld_stream2(const void* p) {
-  uint2 v;
+  uint2 v = make_uint2(0, 0);
+  if (!TFP4_OK(p, 8)) return v;
   asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 
 __device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
-  unsigned short v;
+  unsigned short v = 0;
+  if (!TFP4_OK(p, 2)) return v;
   asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
 
 __device__ __forceinline__ void st_stream(void* p, uint32_t a, uint32_t b, uint32_t c,
                                           uint32_t d) {
+  if (!TFP4_OK(p, 16)) return;
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
 }
 
 __device__ __forceinline__ void st_stream2(void* p, uint32_t a, uint32_t b) {
+  if (!TFP4_OK(p, 8)) return;
   asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void st_stream1(void* p, uint32_t a) {
+  if (!TFP4_OK(p, 4)) return;
   asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
 }
 
 __device__ __forceinline__ void st_stream_u16(void* p, uint32_t a) {
+  if (!TFP4_OK(p, 2)) return;
   asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)a) : "memory");
 }
 
@@ -410,6 +438,31 @@ struct Plan {
   int grid;
   uint32_t steps_per_cta;
 };
+
+// Host side of this translation unit's debug table.
+inline cudaError_t dbg_set_here(const DbgRanges& r, cudaStream_t st) {
+#ifdef TRACE_DEBUG_BOUNDS
+  return cudaMemcpyToSymbolAsync(g_dbg_ranges, &r, sizeof(r), 0, cudaMemcpyHostToDevice, st);
+#else
+  (void)r;
+  (void)st;
+  return cudaSuccess;
+#endif
+}
+
+inline unsigned long long dbg_take_here() {
+#ifdef TRACE_DEBUG_BOUNDS
+  unsigned long long v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dbg_violations, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_dbg_violations, &zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return ~0ull;
+  }
+  return v;
+#else
+  return 0;
+#endif
+}
 
 int occupancy_of(const void* kernel) {
   static std::mutex mu;

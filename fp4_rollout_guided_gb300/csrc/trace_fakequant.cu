@@ -255,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       __syncthreads();
       if (new_t) {
         tseg = st.cur;
-        seg_gs = gs_t[tseg];
+        seg_gs = ldf(gs_t + tseg);
         seg_den = __fmul_rn(seg_gs, 6.0f);
         seg_rden = seg_gs > 0.0f ? __frcp_rn(seg_den) : 0.0f;
         build_tab(tab_t, seg_gs);
       }
       if (new_r) {
         rseg = sr.cur;
-        build_tab(tab_r, gs_r[rseg]);
+        build_tab(tab_r, ldf(gs_r + rseg));
       }
       __syncthreads();
     }
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
           thr2[b] = tab_t.thr2[code];
         }
       } else {
-        pt = pair_scale(bam0, bam1, gs_t[s_t]);
+        pt = pair_scale(bam0, bam1, ldf(gs_t + s_t));
         thr2[0] = ste_threshold2(pt.S[0]);
         thr2[1] = ste_threshold2(pt.S[1]);
       }
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
             pr.inv[b] = e.y;
           }
         } else {
-          pr = pair_scale_stored(bcur, gs_r[s_r]);
+          pr = pair_scale_stored(bcur, ldf(gs_r + s_r));
         }
       }
     }
@@ -463,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     for (int k = 0; k < 11; ++k) {
       if (!GUIDED && k > 0) break;
       const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, v[k]);
-      if ((threadIdx.x & 31) == 0 && tot) atomicAdd(dst + k, (unsigned long long)tot);
+      if ((threadIdx.x & 31) == 0 && tot && TFP4_OK(dst + k, 8))
+        atomicAdd(dst + k, (unsigned long long)tot);
     }
   }
 }
@@ -508,5 +509,10 @@ cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
     default: return fq_dispatch<TRACE_GUIDE_NONE>(a, seg_t, seg_r, sm_count, st);
   }
 }
+
+cudaError_t dbg_set_ranges_fakequant(const DbgRanges& r, cudaStream_t st) {
+  return dbg_set_here(r, st);
+}
+unsigned long long dbg_take_fakequant() { return dbg_take_here(); }
 
 }  // namespace tfp4

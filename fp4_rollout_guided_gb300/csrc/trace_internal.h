@@ -48,6 +48,27 @@ struct FastDivU {
   }
 };
 
+// Debug builds (TRACE_DEBUG_BOUNDS): the byte ranges of global memory the
+// next launches on a stream may touch.  Each API call registers its buffers
+// and its scratch before it launches (stream-ordered); the kernels' memory
+// helpers check every access against the table, count one that falls
+// outside, and skip it.  Release builds register nothing and check nothing.
+constexpr int kDbgRanges = 24;
+struct DbgRanges {
+  uint32_t n;
+  uint64_t lo[kDbgRanges];
+  uint64_t hi[kDbgRanges];
+};
+// Register the ranges in every translation unit's table (on st); read and
+// clear the accesses counted outside the ranges since the last call.
+cudaError_t dbg_set_ranges(const DbgRanges& r, cudaStream_t st);
+unsigned long long dbg_take_violations();
+// per translation unit
+cudaError_t dbg_set_ranges_kernels(const DbgRanges& r, cudaStream_t st);
+unsigned long long dbg_take_kernels();
+cudaError_t dbg_set_ranges_fakequant(const DbgRanges& r, cudaStream_t st);
+unsigned long long dbg_take_fakequant();
+
 // Device scratch owned by a handle.  amax_bits holds per-segment maxima as
 // binary32 bit patterns (non-negative floats order like unsigned integers);
 // the amax kernel's last CTA converts them to global scales and re-zeroes

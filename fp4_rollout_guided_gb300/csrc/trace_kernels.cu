@@ -39,7 +39,7 @@ __device__ __forceinline__ void cta_flush_max(uint32_t v, uint32_t* dst, uint32_
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < kThreads / 32; ++i) m = red[i] > m ? red[i] : m;
-    if (m) atomicMax(dst, m);
+    if (m && TFP4_OK(dst, 4)) atomicMax(dst, m);
   }
   __syncthreads();
 }
@@ -86,7 +86,10 @@ __global__ void __launch_bounds__(kThreads)
       if (open >= 0) cta_flush_max(run, amax_bits + open, red);
       open = -1;
       run = 0;
-      if (c < nchunks && m) atomicMax(amax_bits + seg_advance(seg, ss.cur, cpr.div(c)), m);
+      if (c < nchunks && m) {
+        uint32_t* dst = amax_bits + seg_advance(seg, ss.cur, cpr.div(c));
+        if (TFP4_OK(dst, 4)) atomicMax(dst, m);
+      }
     }
     cur = nxt;
   }
@@ -97,17 +100,17 @@ __global__ void __launch_bounds__(kThreads)
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t ticket = atomicAdd(done, 1u);
+    const uint32_t ticket = TFP4_OK(done, 4) ? atomicAdd(done, 1u) : 0u;
     is_last = (ticket == gridDim.x - 1);
   }
   __syncthreads();
   if (is_last) {
     __threadfence();
     for (int s = threadIdx.x; s < seg.n; s += kThreads) {
-      const uint32_t a = atomicExch(amax_bits + s, 0u);
-      gs_out[s] = global_scale_of(a);
+      const uint32_t a = TFP4_OK(amax_bits + s, 4) ? atomicExch(amax_bits + s, 0u) : 0u;
+      if (TFP4_OK(gs_out + s, 4)) gs_out[s] = global_scale_of(a);
     }
-    if (threadIdx.x == 0) atomicExch(done, 0u);
+    if (threadIdx.x == 0 && TFP4_OK(done, 4)) atomicExch(done, 0u);
   }
 }
 
@@ -245,14 +248,14 @@ __global__ void __launch_bounds__(kThreads)
     if (uniform && ss.cur != tseg) {
       __syncthreads();
       tseg = ss.cur;
-      sc.set(gs[tseg]);
+      sc.set(ldf(gs + tseg));
       build_inv_tab(inv_tab, sc.gs, threadIdx.x, kThreads);
       __syncthreads();
     }
     if (c < nchunks) {
       const PairScale ps =
           uniform ? chunk_scale_tab(cur, sc.gs, sc.den, sc.rden, inv_tab)
-                  : chunk_scale(cur, gs[seg_advance(seg, ss.cur, cpr.div(c))]);
+                  : chunk_scale(cur, ldf(gs + seg_advance(seg, ss.cur, cpr.div(c))));
       quant_chunk(cur, ps, c, codes, bs, mma, cpr, guide);
     }
     cur = nxt;
@@ -661,11 +664,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         fence_proxy_async();
         if (swz) {
           mbar_expect_tx(&sm.full_a[slot], kStepBytes);
-          tensor_load_2d(sm.a[slot], &xmap, 0u, ca.step_chunk() >> 1, &sm.full_a[slot]);
+          if (TFP4_OK(x + (uint64_t)(ca.step_chunk() >> 1) * 128u, 128))
+            tensor_load_2d(sm.a[slot], &xmap, 0u, ca.step_chunk() >> 1, &sm.full_a[slot]);
         } else {
           const uint32_t bytes = ca.step_chunks() * 64u;
           mbar_expect_tx(&sm.full_a[slot], bytes);
-          bulk_load(sm.a[slot], x + (uint64_t)ca.step_chunk() * 64u, bytes, &sm.full_a[slot]);
+          if (TFP4_OK(x + (uint64_t)ca.step_chunk() * 64u, bytes))
+            bulk_load(sm.a[slot], x + (uint64_t)ca.step_chunk() * 64u, bytes, &sm.full_a[slot]);
         }
         ++na;
         ca.next(seg, wv, cpr_u, b, G);
@@ -702,11 +707,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           fence_proxy_async();
           if (swz) {
             mbar_expect_tx(&sm.full_q[slot], kStepBytes);
+            if (TFP4_OK(x + (uint64_t)(cq.step_chunk() >> 1) * 128u, 128))
             tensor_load_2d_hint(sm.q[slot], &xmap, 0u, cq.step_chunk() >> 1, &sm.full_q[slot],
                                 evict_first);
           } else {
             const uint32_t bytes = cq.step_chunks() * 64u;
             mbar_expect_tx(&sm.full_q[slot], bytes);
+            if (TFP4_OK(x + (uint64_t)cq.step_chunk() * 64u, bytes))
             bulk_load_hint(sm.q[slot], x + (uint64_t)cq.step_chunk() * 64u, bytes,
                            &sm.full_q[slot], evict_first);
           }
@@ -734,7 +741,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // no step are counted as soon as the cursor passes them
     int counted = 0;
     if (t == 0)
-      for (; counted < c.w; ++counted) red_release_add(wave_cnt + counted, 1u);
+      for (; counted < c.w; ++counted)
+        if (TFP4_OK(wave_cnt + counted, 4)) red_release_add(wave_cnt + counted, 1u);
     while (c.w < wv.n) {
       const int w = c.w;
       const int s0 = wv.seg0[w];
@@ -793,13 +801,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int i = t; i < wv.seg0[w + 1] - s0; i += 32 * kAmaxWarps) {
           const uint32_t m = sm.smax[i];
           if (m) {
-            atomicMax(amax_bits + s0 + i, m);
+            if (TFP4_OK(amax_bits + s0 + i, 4)) atomicMax(amax_bits + s0 + i, m);
             sm.smax[i] = 0u;
           }
         }
         amax_warps_sync();
         if (t == 0)
-          for (; counted < c.w; ++counted) red_release_add(wave_cnt + counted, 1u);
+          for (; counted < c.w; ++counted)
+        if (TFP4_OK(wave_cnt + counted, 4)) red_release_add(wave_cnt + counted, 1u);
       }
     }
   } else {
@@ -830,7 +839,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int s = uniform ? ss.cur : seg_advance(seg, ss.cur, cpr.div(cidx));
         if (s != gseg) {
           gseg = s;
-          g = global_scale_of(ld_acquire(amax_bits + s));
+          g = TFP4_OK(amax_bits + s, 4) ? global_scale_of(ld_acquire(amax_bits + s)) : 0.0f;
         }
         quant_chunk(ch, chunk_scale(ch, g), cidx, codes, bs, mma, cpr, guide);
       }
@@ -850,7 +859,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const uint32_t ticket = atomicAdd(done, 1u);
+    const uint32_t ticket = TFP4_OK(done, 4) ? atomicAdd(done, 1u) : 0u;
     is_last = (ticket == G - 1);
   }
   __syncthreads();
@@ -859,11 +868,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // the global scales are written here, all at once: a producer that
     // wrote a wave's scales before streaming the wave would start it late
     for (int s = threadIdx.x; s < seg.n; s += kFusedThreads) {
-      gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
-      amax_bits[s] = 0u;
+      if (TFP4_OK(gs_out + s, 4) && TFP4_OK(amax_bits + s, 4)) {
+        gs_out[s] = global_scale_of(ld_l2(amax_bits + s));
+        amax_bits[s] = 0u;
+      }
     }
-    for (int w = threadIdx.x; w < wv.n; w += kFusedThreads) wave_cnt[w] = 0u;
-    if (threadIdx.x == 0) *done = 0u;
+    for (int w = threadIdx.x; w < wv.n; w += kFusedThreads)
+      if (TFP4_OK(wave_cnt + w, 4)) wave_cnt[w] = 0u;
+    if (threadIdx.x == 0 && TFP4_OK(done, 4)) *done = 0u;
   }
 }
 
@@ -963,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
     if (uniform && ss.cur != tseg) {
       __syncthreads();
       tseg = ss.cur;
-      build_tab(tab, gs_r[tseg]);
+      build_tab(tab, ldf(gs_r + tseg));
       __syncthreads();
     }
     if (c < nchunks) {
@@ -973,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_UNPACK_MIN_CTAS)
         inv[0] = tab.sinv[bcur & 0x7Fu].y;
         inv[1] = tab.sinv[(bcur >> 8) & 0x7Fu].y;
       } else {
-        const PairScale ps = pair_scale_stored(bcur, gs_r[s]);
+        const PairScale ps = pair_scale_stored(bcur, ldf(gs_r + s));
         inv[0] = ps.inv[0];
         inv[1] = ps.inv[1];
       }
@@ -1229,5 +1241,10 @@ cudaError_t launch_ste_backward(const void* g, const uint32_t* mask, int64_t nch
                                               (uint32_t)nchunks, p.steps_per_cta, (uint8_t*)out);
   return cudaGetLastError();
 }
+
+cudaError_t dbg_set_ranges_kernels(const DbgRanges& r, cudaStream_t st) {
+  return dbg_set_here(r, st);
+}
+unsigned long long dbg_take_kernels() { return dbg_take_here(); }
 
 }  // namespace tfp4

@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "trace_fp4.h"
@@ -176,6 +178,23 @@ trace_status_t trace_rollout_quant_noalloc(const void* x_bf16, int64_t rows, int
     sc.gs_train = nullptr;
     // the maxima start at zero and the ticket at zero for this call
     e = cudaMemsetAsync(slot->scratch, 0, sizeof(uint32_t) * kWords, s);
+#ifdef TRACE_DEBUG_BOUNDS
+    if (e == cudaSuccess) {
+      tfp4::DbgRanges r;
+      memset(&r, 0, sizeof(r));
+      const void* p[6] = {x_bf16, codes_u8, bs_e4m3, gs_f32, guide_bits, slot->scratch};
+      const int64_t n[6] = {rows * cols * 2, rows * cols / 2, rows * cols / 16,
+                            (int64_t)sizeof(float) * sp.n, rows * cols / 4,
+                            (int64_t)sizeof(uint32_t) * kWords};
+      for (int i = 0; i < 6; ++i)
+        if (p[i]) {
+          r.lo[r.n] = (uint64_t)p[i];
+          r.hi[r.n] = (uint64_t)p[i] + (uint64_t)n[i];
+          ++r.n;
+        }
+      e = tfp4::dbg_set_ranges(r, s);
+    }
+#endif
     const int32_t cpr = (int32_t)(cols / 32);
     if (e == cudaSuccess)
       e = tfp4::launch_amax(x_bf16, nchunks, cpr, sp, sc, gs_f32, slot->sm_count, s);

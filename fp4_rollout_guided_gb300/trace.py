@@ -26,7 +26,8 @@ GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
 KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward",
            "rollout_fused", "mma_scales", "nvfp4_gemm")
-OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3}
+OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3,
+           "debug_shrink": 4}
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
           4: "CUDA error", 5: "out of memory", 6: "timeout", 7: "cuBLASLt missing or refused"}
@@ -72,6 +73,8 @@ SIGNATURES = {
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
     "trace_set_option": (INT, [P, INT, I64]),
     "trace_device_status": (INT, [P, P]),
+    "trace_debug_bounds": (INT, [P, ctypes.POINTER(ctypes.c_int),
+                                 ctypes.POINTER(ctypes.c_uint64)]),
     "trace_rollout_quant_mma": (INT, [P, P, I64, I64, Segments, P, P, P, P, P, P]),
     "trace_block_scales_mma_bytes": (ctypes.c_size_t, [I64, I64]),
     "trace_block_scales_mma": (INT, [P, P, I64, I64, P, P]),
@@ -449,6 +452,15 @@ class Handle:
         if st not in (0, 6):
             self._check("trace_device_status", st)
         return st
+
+    def debug_bounds(self):
+        """-> (checked, violations): whether this build checks global accesses
+        against the calls' registered buffers (TRACE_DEBUG_BOUNDS), and the
+        out-of-range accesses counted since the last query (waits for the device)."""
+        c, v = ctypes.c_int(0), ctypes.c_uint64(0)
+        self._check("trace_debug_bounds",
+                    lib().trace_debug_bounds(self._h, ctypes.byref(c), ctypes.byref(v)))
+        return bool(c.value), int(v.value)
 
     # -- profiler ---------------------------------------------------------------
     def profile(self, enable: bool = True):

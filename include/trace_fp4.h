@@ -174,9 +174,15 @@ typedef enum {
                                   4 KiB .. 40 MiB (default 32 MiB)            */
   TRACE_OPT_WAIT_LIMIT_NS = 2, /* limit of each in-kernel wait, 1 ms .. 10 s
                                   (default 1 s)                               */
-  TRACE_OPT_WAIT_EXTRA = 3     /* test hook, 0 (default) or 1: each wait also
+  TRACE_OPT_WAIT_EXTRA = 3,    /* test hook, 0 (default) or 1: each wait also
                                   expects an arrival that never comes, so every
                                   wait runs out at its limit                  */
+  TRACE_OPT_DEBUG_SHRINK = 4   /* test hook of builds with TRACE_DEBUG_BOUNDS
+                                  (see trace_debug_bounds), 0 (default) or 1:
+                                  every output buffer is registered 16 bytes
+                                  short, so the kernels' last stores into it
+                                  are counted as out of range and skipped.
+                                  Other builds return TRACE_ERR_INVALID_ARG. */
 } trace_option_t;
 TRACE_API trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t value);
 
@@ -407,6 +413,17 @@ TRACE_API trace_status_t trace_rollout_quant_noalloc(const void* x_bf16, int64_t
                                                      void* codes_u8, void* bs_e4m3,
                                                      float* gs_f32, uint32_t* guide_bits,
                                                      trace_stream_t stream);
+
+/* Bounds checking of debug builds.  A library compiled with
+ * -DTRACE_DEBUG_BOUNDS registers, before every launch of a call, the byte
+ * ranges of the call's buffers and of the handle's scratch (stream-ordered),
+ * and its hot-path kernels check every global access against them: an access
+ * outside them is counted and skipped (never a trap).  This call waits for
+ * the device (cudaDeviceSynchronize), sets *checked to 1 and *violations to
+ * the accesses counted since the previous call, and clears the count.  In
+ * other builds it sets *checked = 0, *violations = 0.  No counterpart in the
+ * paper: it stands in for a device-side memory checker. */
+TRACE_API trace_status_t trace_debug_bounds(trace_handle_t h, int* checked, uint64_t* violations);
 
 /* Built-in profiler.  While enabled, every kernel launch through the handle
  * is bracketed by CUDA events on its own stream.  trace_profile_collect
