@@ -283,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
         pt.codes = pair_codes(bam0, bam1, seg_gs, seg_den, seg_rden);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-          const uint32_t code = (pt.codes >> (8 * b)) & 0xFFu;
+          // codes of non-negative block maxima are at most 0x7F (NaN); the
+          // mask keeps the table index in range whatever the input holds
+          const uint32_t code = (pt.codes >> (8 * b)) & 0x7Fu;
           const float2 e = tab_t.sinv[code];
           pt.S[b] = e.x;
           pt.inv[b] = e.y;

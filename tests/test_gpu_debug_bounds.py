@@ -76,6 +76,28 @@ for rows, cols, seg in [(1, 32, None), (3, 96, [0, 0, 2, 3]), (257, 64, [0, 100,
     res["violations"] = v
     res["bit_exact"] = ok
     out["cases"].append(res)
+# non-finite inputs (unspecified results, but every access stays in range)
+rows, cols = 300, 96
+xn = rand((rows, cols), 5, 2.0).float()
+xn[3, 5] = float("nan"); xn[7, 0] = float("inf"); xn[7, 1] = -float("inf")
+xn[100:110, :] = float("nan"); xn[200, 17] = 3.0e38; xn[250, :32] = float("inf")
+xn = xn.to(torch.bfloat16).to(dev)
+segn = np.array([0, 150, 150, 300], np.int64)
+for fused in (1, 0):
+    h.set_option("fused_amax", fused)
+    codes, bs, gs, guide = h.rollout_quant(xn, segn)
+h.set_option("fused_amax", 1)
+h.guide_pack(codes)
+h.guide_unpack(xn, guide, bs, gs, segn)
+for kind, gd in (("none", None), ("compact", guide), ("full", codes)):
+    args = (xn, segn, kind) + (() if kind == "none" else (gd, bs, gs, segn))
+    y, m, c, _ = h.train_fakequant(*args, codes=True, stats=trace.new_stats(dev))
+    h.train_fakequant(*args)
+h.ste_backward(xn, m)
+h.segment_amax(xn, segn)
+_, v = h.debug_bounds()
+out["nonfinite_violations"] = v
+out["nonfinite_status"] = h.device_status()
 # outputs registered 16 bytes short: the kernels' last stores are counted and skipped
 h.set_option("debug_shrink", 1)
 rows, cols = 257, 64
@@ -111,6 +133,7 @@ def test_debug_build_counts_no_violation_and_detects_one(tmp_path):
     for case in res["cases"]:
         assert case["violations"] == 0, case
         assert case["bit_exact"], case
+    assert res["nonfinite_violations"] == 0 and res["nonfinite_status"] == 0
     shrink = res["shrink"]
     assert shrink["violations"] > 0
     # the last 16 bytes of each output kept their fill pattern

@@ -278,6 +278,48 @@ def test_mixed_forms_in_one_warp(h):
               "mixed")
 
 
+def test_non_finite_inputs_leave_other_segments_exact(h):
+    """NaN and infinities give unspecified results in their own segment but
+    never fault, and the segments without them keep the oracle's bytes."""
+    from fp4_rollout_guided_gb300 import trace
+    rows, cols = 384, 128
+    x = rand_bf16((rows, cols), 71, scale=2.0).float()
+    x[200, 3] = float("nan")
+    x[250, 0] = float("inf")
+    x[300:310, :] = -float("inf")
+    x[350, 64:96] = float("nan")
+    x = x.to(torch.bfloat16)
+    r = x.clone()
+    r[:192] = drift(x[:192], 72, 2.0 ** -7)
+    seg = np.array([0, 192, 384], np.int64)
+    xg, rg = x.to(DEV), r.to(DEV)
+    codes, bs, gs, guide = h.rollout_quant(rg, seg)
+    outs = {}
+    for kind, g in (("none", None), ("compact", guide), ("full", codes)):
+        args = (xg, seg, kind) + (() if kind == "none" else (g, bs, gs, seg))
+        outs[kind] = h.train_fakequant(*args, codes=True, stats=trace.new_stats(DEV))
+        outs[kind + "/mask"] = h.train_fakequant(*args)
+    unpacked = h.guide_unpack(xg, guide, bs, gs, seg)
+    torch.cuda.synchronize()
+    assert h.device_status() == 0
+    # the finite segment against the oracle
+    xu, ru = u16(x[:192]), u16(r[:192])
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(ru, None)
+    assert_same("codes", codes[:192].cpu().numpy(), o_codes)
+    assert_same("guide", u32(guide[:192]), o_guide)
+    assert_same("unpack", unpacked[:192].cpu().numpy(),
+                oracle.guide_unpack(xu, o_guide, o_bs, o_gs, None))
+    for kind, okind, og in (("none", oracle.GUIDE_NONE, None),
+                            ("compact", oracle.GUIDE_COMPACT, o_guide),
+                            ("full", oracle.GUIDE_FULL, o_codes)):
+        oargs = (xu, None, okind) + (() if kind == "none" else (og, o_bs, o_gs, None))
+        oy, om, oc, _ = oracle.train_fakequant(*oargs)
+        assert_same(f"{kind} y", u16(outs[kind][0][:192]), oy)
+        assert_same(f"{kind} mask", u32(outs[kind][1][:192]), om)
+        assert_same(f"{kind} codes_t", outs[kind][2][:192].cpu().numpy(), oc)
+        assert_same(f"{kind} y (mask only)", u16(outs[kind + "/mask"][0][:192]), oy)
+
+
 def test_empty_input(h):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
     codes, bs, gs, guide = h.rollout_quant(x, np.array([0, 0, 0], np.int64))
