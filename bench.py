@@ -785,13 +785,15 @@ def run_gemm(args):
     """The f4 consumer: NVFP4 GEMM over rollout codes on one GPU.  Weights W
     [N, K] are quantised once; each step quantises the activations X [M, K]
     (rollout quantiser writing the scales in the tensor-core tile layout) and runs
-    Y = X W^T (cuBLASLt block-scaled E2M1 GEMM, bf16 out).  Prints one JSON
-    line with the GEMM's TFLOP/s against the FP4 tensor peak."""
+    Y = X W^T (block-scaled E2M1 GEMM, bf16 out: the hand-written tcgen05
+    kernel with 128 x 256 or 128 x 128 tiles, or cuBLASLt, --gemm-form).
+    Prints one JSON line with the GEMM's TFLOP/s against the FP4 tensor peak."""
     from fp4_rollout_guided_gb300 import build, trace
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     build.build()
     h = trace.Handle(0)
+    h.set_option("gemm", args.gemm_form)
     M, N, K = args.gemm_shape
     g = torch.Generator(device=dev).manual_seed(args.seed)
     x = (torch.randn((M, K), generator=g, device=dev) * 2.0).to(torch.bfloat16)
@@ -835,7 +837,7 @@ def run_gemm(args):
             "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "e2m1",
             "data": "synthetic",
             "config": {"workload": f"Y[{M},{N}] = X[{M},{K}] W[{N},{K}]^T, X quantised each step",
-                       "out": "bf16"},
+                       "out": "bf16", "gemm": args.gemm_form},
             "gemm_ms": round(gemm_ms, 4), "quantise_ms": quant,
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
                          "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
@@ -867,6 +869,8 @@ def main():
                     help="time the NVFP4 GEMM over rollout codes instead")
     ap.add_argument("--gemm-shape", type=int, nargs=3, default=[16384, 8192, 8192],
                     metavar=("M", "N", "K"))
+    ap.add_argument("--gemm-form", default="tc256", choices=["tc256", "tc128", "cublaslt"],
+                    help="GEMM form: hand-written tcgen05 kernel (tile N 256 / 128) or cuBLASLt")
     ap.add_argument("--transport", action="store_true",
                     help="time the guide record's device/host/disk round trip instead")
     args = ap.parse_args()

@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtrace_fp4.so")
-SOURCES = ["trace_kernels.cu", "trace_fakequant.cu", "trace_gemm.cu", "trace_api.cu",
-           "trace_noalloc.cu"]
+SOURCES = ["trace_kernels.cu", "trace_fakequant.cu", "trace_gemm.cu", "trace_gemm_tc.cu",
+           "trace_api.cu", "trace_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-prec-div=true",
               "-prec-sqrt=true", "-ftz=false", "-Xcompiler", "-fPIC",
@@ -35,8 +35,9 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "trace_internal.h"), os.path.join(CSRC, "trace_device.cuh"),
-              os.path.join(INCLUDE, "trace_fp4.h")]
+    files += [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
+              if f.endswith((".h", ".cuh"))]
+    files.append(os.path.join(INCLUDE, "trace_fp4.h"))
     return files
 
 

@@ -49,6 +49,7 @@ struct trace_ctx {
   const void* scratch_base = nullptr;  // the one scratch allocation
   size_t scratch_bytes = 0;
   bool dbg_shrink = false;  // debug builds: register outputs 16 bytes short
+  int gemm = TRACE_GEMM_CUBLASLT;  // form of trace_nvfp4_gemm
 };
 
 namespace {
@@ -287,6 +288,11 @@ trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t va
     case TRACE_OPT_WAIT_EXTRA:
       if (value != 0 && value != 1) return TRACE_ERR_INVALID_ARG;
       h->wait_extra = (uint32_t)value;
+      return TRACE_OK;
+    case TRACE_OPT_GEMM:
+      if (value != TRACE_GEMM_TC256 && value != TRACE_GEMM_CUBLASLT && value != TRACE_GEMM_TC128)
+        return TRACE_ERR_INVALID_ARG;
+      h->gemm = (int)value;
       return TRACE_OK;
     case TRACE_OPT_DEBUG_SHRINK:
 #ifdef TRACE_DEBUG_BOUNDS
@@ -804,9 +810,24 @@ extern "C" trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes
   for (const void* p : {a_codes, a_scales_mma, b_codes, b_scales_mma, (const void*)d})
     if ((s = check_tensor(p)) != TRACE_OK) return s;
   if (!a_gs || !b_gs) return TRACE_ERR_INVALID_ARG;
-  if (!tfp4::lt_available()) return TRACE_ERR_LIBRARY;
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
+  if (h->gemm != TRACE_GEMM_CUBLASLT) {
+    if (m > 65535LL * 128) return TRACE_ERR_INVALID_ARG;  // output tile rows on grid y
+    cudaError_t e = begin_call(h, st);
+    if (e == cudaSuccess)
+      e = timed(h, TRACE_KERNEL_NVFP4_GEMM, st, [&] {
+        return tfp4::launch_nvfp4_gemm_tc(a_codes, a_scales_mma, a_gs, b_codes, b_scales_mma,
+                                          b_gs, m, n, k, d, d_type == TRACE_OUT_BF16,
+                                          h->gemm == TRACE_GEMM_TC128 ? 128 : 256, h->scratch.err,
+                                          h->wait_ns, st);
+      });
+    const cudaError_t e2 = end_call(h, st);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    if (e2 != cudaSuccess) return cuda_fail(h, e2);
+    return TRACE_OK;
+  }
+  if (!tfp4::lt_available()) return TRACE_ERR_LIBRARY;
   if (!h->gemm_ws) {
     const size_t ws = size_t(32) << 20;
     if (cudaMalloc(&h->gemm_ws, ws) != cudaSuccess) {

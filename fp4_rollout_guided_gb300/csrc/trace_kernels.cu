@@ -12,6 +12,7 @@
 
 #include <cstring>
 
+#include "trace_async.cuh"
 #include "trace_device.cuh"
 
 namespace tfp4 {
@@ -290,11 +291,6 @@ __global__ void __launch_bounds__(kThreads)
 // then undefined) and gives up the cross-CTA waits that follow, and each
 // producer waits for its own copies in flight before the CTA exits.
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
@@ -312,9 +308,6 @@ __device__ __forceinline__ uint32_t ld_l2(const uint32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // One thread: true once *p >= target; false after limit_ns (or a fixed
 // number of polls, whichever comes first).
@@ -346,67 +339,7 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
 }
 
 
-// ---- TMA bulk copies and mbarriers -------------------------------------------
-
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// Non-blocking: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for a phase; false (and *err set) once limit_ns has passed.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                            uint32_t* err) {
-  for (uint32_t it = 0; it < 16; ++it)
-    if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 15u) == 15u && global_ns() - t0 > limit_ns) break;
-  }
-  atomicOr(err, 2u);
-  return false;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                          uint32_t* err) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, limit_ns, err);
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// bytes (a multiple of 16) from global src to shared dst, completing on bar
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
+// ---- TMA copies with an L2 policy -------------------------------------------
 
 __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
                                                uint64_t* bar, uint64_t policy) {
@@ -570,15 +503,6 @@ __device__ __forceinline__ uint32_t swz_unit_chunk(uint32_t u) {
   return 2u * row + ((((u & 7u) ^ (row & 7u))) >> 2);
 }
 
-__device__ __forceinline__ void tensor_load_2d(void* dst, const CUtensorMap* map, uint32_t c0,
-                                               uint32_t c1, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
-      "r"(smem_addr(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ void tensor_load_2d_hint(void* dst, const CUtensorMap* map,
                                                     uint32_t c0, uint32_t c1, uint64_t* bar,

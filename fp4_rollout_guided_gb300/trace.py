@@ -27,7 +27,9 @@ _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
 KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward",
            "rollout_fused", "mma_scales", "nvfp4_gemm")
 OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3,
-           "debug_shrink": 4}
+           "debug_shrink": 4, "gemm": 5}
+# values of the "gemm" option: the form of nvfp4_gemm
+GEMM_FORMS = {"tc256": 0, "cublaslt": 1, "tc128": 2}
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
           4: "CUDA error", 5: "out of memory", 6: "timeout", 7: "cuBLASLt missing or refused"}
@@ -442,7 +444,10 @@ class Handle:
 
     # -- options and device status -----------------------------------------------
     def set_option(self, name: str, value: int):
-        """fused_amax (0/1), wave_bytes, wait_limit_ns, wait_extra (test hook)."""
+        """fused_amax (0/1), wave_bytes, wait_limit_ns, gemm (a GEMM_FORMS
+        name or value), wait_extra and debug_shrink (test hooks)."""
+        if name == "gemm" and isinstance(value, str):
+            value = GEMM_FORMS[value]
         self._check("trace_set_option", lib().trace_set_option(self._h, OPTIONS[name], int(value)))
 
     def device_status(self) -> int:
@@ -537,7 +542,7 @@ __all__: Sequence[str] = ["Handle", "TraceError", "lib", "library_path", "new_st
                           "stats_dict", "GUIDE_NONE", "GUIDE_FULL", "GUIDE_COMPACT",
                           "KERNELS", "SIGNATURES", "MAX_SEGMENTS", "RecordHeader",
                           "record_size", "record_info", "save_record", "load_record",
-                          "guided_fake_quant", "GuidedFakeQuant", "OPTIONS"]
+                          "guided_fake_quant", "GuidedFakeQuant", "OPTIONS", "GEMM_FORMS"]
 
 
 class GuidedFakeQuant(torch.autograd.Function):

@@ -177,13 +177,23 @@ typedef enum {
   TRACE_OPT_WAIT_EXTRA = 3,    /* test hook, 0 (default) or 1: each wait also
                                   expects an arrival that never comes, so every
                                   wait runs out at its limit                  */
-  TRACE_OPT_DEBUG_SHRINK = 4   /* test hook of builds with TRACE_DEBUG_BOUNDS
+  TRACE_OPT_DEBUG_SHRINK = 4,  /* test hook of builds with TRACE_DEBUG_BOUNDS
                                   (see trace_debug_bounds), 0 (default) or 1:
                                   every output buffer is registered 16 bytes
                                   short, so the kernels' last stores into it
                                   are counted as out of range and skipped.
                                   Other builds return TRACE_ERR_INVALID_ARG. */
+  TRACE_OPT_GEMM = 5           /* form of trace_nvfp4_gemm: TRACE_GEMM_CUBLASLT
+                                  (default), TRACE_GEMM_TC256 or
+                                  TRACE_GEMM_TC128                            */
 } trace_option_t;
+
+/* Values of TRACE_OPT_GEMM. */
+enum {
+  TRACE_GEMM_TC256 = 0,    /* hand-written tcgen05 kernel, 128 x 256 output tiles */
+  TRACE_GEMM_CUBLASLT = 1, /* cuBLASLt's block-scaled GEMM                        */
+  TRACE_GEMM_TC128 = 2     /* hand-written tcgen05 kernel, 128 x 128 output tiles */
+};
 TRACE_API trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t value);
 
 /* Synchronises `stream`, then reports and clears the handle's device-side

@@ -736,8 +736,25 @@ def _student_t(shape, seed):
     return (2.0 * z / chi.sqrt()).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("m,n,k", [(256, 256, 512), (128, 384, 1024), (512, 128, 256)])
-def test_nvfp4_gemm_against_oracle(h, m, n, k):
+GEMM_SHAPES = [(256, 256, 512), (128, 384, 1024), (512, 128, 256)]
+# ragged: k not a multiple of the 256-element stage or of 64, n not a multiple
+# of the tile (a B tile with one scale band), n % 8 != 0 (element stores),
+# single rows and columns, one k-step
+GEMM_RAGGED = [(1, 32, 32), (130, 200, 96), (300, 36, 320), (257, 520, 544), (64, 1000, 2048),
+               (128, 1, 64), (7, 264, 4128)]
+
+
+@pytest.fixture(params=["cublaslt", "tc256", "tc128"])
+def gemm_form(h, request):
+    h.set_option("gemm", request.param)
+    yield request.param
+    h.set_option("gemm", "cublaslt")
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES + GEMM_RAGGED)
+def test_nvfp4_gemm_against_oracle(h, gemm_form, m, n, k):
+    if gemm_form == "cublaslt" and (m, n, k) in GEMM_RAGGED:
+        pytest.skip("the library GEMM is checked on the aligned shapes")
     x = _student_t((m, k), 11 + m)
     w = _student_t((n, k), 13 + n)
     a = h.nvfp4_operand(x.to(DEV))
@@ -745,6 +762,7 @@ def test_nvfp4_gemm_against_oracle(h, m, n, k):
     d = h.nvfp4_gemm(a, b)
     d16 = h.nvfp4_gemm(a, b, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
+    assert h.device_status() == 0
     # the operands are the oracle's, bit for bit
     a_codes, a_bs, a_gs, _ = oracle.rollout_quant(u16(x), None)
     b_codes, b_bs, b_gs, _ = oracle.rollout_quant(u16(w), None)
@@ -763,7 +781,7 @@ def test_nvfp4_gemm_against_oracle(h, m, n, k):
     assert np.all(err16 <= bound + 2.0 ** -8 * np.abs(ref)), float(err16.max())
 
 
-def test_nvfp4_gemm_closed_form(h):
+def test_nvfp4_gemm_closed_form(h, gemm_form):
     m, n, k = 128, 128, 256
     x = torch.full((m, k), 1.5, dtype=torch.bfloat16, device=DEV)
     w = torch.full((n, k), -2.0, dtype=torch.bfloat16, device=DEV)
