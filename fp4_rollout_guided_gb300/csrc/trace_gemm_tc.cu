@@ -6,8 +6,9 @@
 // section "TRACE Core Concept": rollout runs weights and activations in
 // NVFP4, so the rollout codes and their block scales are the operands of its
 // GEMMs.  The operand, scale and descriptor formats are NVIDIA's documented
-// interfaces (PTX ISA, tcgen05 shared-memory and instruction descriptors and
-// block scaling; cuBLAS, "1D block scaling factors layout").
+// interfaces (PTX ISA, tcgen05 shared-memory and instruction descriptors,
+// tensor-memory operands and block scaling; cuBLAS, "1D block scaling factors
+// layout").
 //
 // d [m, n] = fl32(gs_a * gs_b) * sum_k A[i, k] B[j, k], A and B as codes
 // [rows, k/2] (element 2i in the low nibble: the packed E2M1 operand format)
@@ -20,31 +21,39 @@
 //     2-D tensor-map copies in 128-byte swizzle, and the block-scale tiles
 //     (512 bytes per 128 rows and 64 elements of k) with bulk copies, into a
 //     ring of stages completing on mbarriers;
-//   - warp 1: allocates the tensor memory; one lane copies each stage's scale
-//     tiles into tensor memory (tcgen05.cp, 32 lines x 128 bits to all four
-//     lane quarters) and issues the block-scaled MMAs (128 x BN x 64 each),
-//     then commits the stage back to the producer;
-//   - warps 2-5: epilogue.  Once the last MMA has completed each thread reads
-//     its accumulator row from tensor memory (its warp's lane quarter),
-//     multiplies by fl32(gs_a * gs_b) and stores fp32 or bf16.
+//   - warps 2-5: stagers, then epilogue.  Per stage each warp moves its
+//     quarter of the A rows and the stage's scale lines from shared into
+//     tensor memory (tcgen05.st, warp w owning lane quarter w mod 4), so
+//     that the MMAs read only B from shared memory and no scale copy
+//     occupies the tensor pipe.  After the last stage each thread reads its
+//     accumulator row, multiplies by fl32(gs_a * gs_b), and the warp stores
+//     its 32 rows through shared memory with tensor-map stores (fp32 or
+//     bf16);
+//   - warp 1: allocates the tensor memory; one lane issues the block-scaled
+//     MMAs (128 x BN x 64 each, A and the scales in tensor memory, B in
+//     shared memory) and commits each stage back to the producer.
 // Rows and columns past m, n and k are zero-filled by the tensor-map copies
 // (zero codes contribute nothing whatever their scales); scale tiles past the
-// end of a scale tensor are not read, and only the output rows and columns
-// inside d are stored.
+// end of a scale tensor are not read (their lanes hold stale scales that
+// only reach output columns past n, never stored), and only rows and
+// columns inside d are stored.
 //
-// Tensor memory (512 columns of 32-bit lanes): the accumulator in columns
-// [0, BN); per stage, the A scales of its four k-steps (four columns each) and
-// the B scales (BN / 32 columns per k-step).  In a 512-byte scale tile, line
-// L holds rows L, L + 32, L + 64, L + 96; copied to lane L of every quarter,
-// column c of lane L holds the four scales of row L + 32 c for the k-step.
+// Tensor memory (512 columns of 32-bit lanes, lane = tile row): the
+// accumulator in columns [0, BN); per stage, the A scales (four columns per
+// k-step), the B scales (BN / 32 columns per k-step), then A (eight columns
+// of packed codes per k-step).  Scales follow the tile layout: line L of a
+// 512-byte tile holds rows L, L + 32, L + 64, L + 96, and lane L of every
+// quarter holds line L, so column c of lane L holds the four scales of row
+// L + 32 c for the k-step.
 //
 // Every wait is bounded (wait_ns): one that runs out sets *err, the role
-// stops issuing, the producer still waits (bounded) for its own copies in
-// flight, and the tensor memory is freed before the CTA exits.
+// stops, the producer still waits (bounded) for its own copies in flight,
+// and the tensor memory is freed before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "trace_async.cuh"
@@ -58,6 +67,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBK = 256;            // k elements per stage (128 bytes of codes a row)
 constexpr uint32_t kSfTile = 512;        // bytes of one scale tile: 128 rows x 64 k
 constexpr uint32_t kStepsPerStage = 4;   // 64-element MMA k-steps per stage
+constexpr uint32_t kBoxBytes = 4096;     // one output box: 32 rows x 128 bytes
 
 template <int BN>
 struct GemmShape {
@@ -67,17 +77,22 @@ struct GemmShape {
   static constexpr uint32_t kSfaBytes = kStepsPerStage * kSfTile;
   static constexpr uint32_t kSfbBytes = kBands * kStepsPerStage * kSfTile;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr uint32_t kStages = BN == 256 ? 4 : 6;
+  static constexpr uint32_t kStages = BN == 256 ? 3 : 5;
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-  // tensor-memory columns
-  static constexpr uint32_t kSfaCols = 4;                 // per k-step
-  static constexpr uint32_t kSfbCols = (uint32_t)BN / 32; // per k-step
+  // tensor-memory columns per k-step and their regions
+  static constexpr uint32_t kSfaCols = 4;
+  static constexpr uint32_t kSfbCols = 4 * kBands;
+  static constexpr uint32_t kACols = 8;  // 64 packed E2M1 codes
   static constexpr uint32_t kSfaBase = BN;
   static constexpr uint32_t kSfbBase = kSfaBase + kStages * kStepsPerStage * kSfaCols;
-  static constexpr uint32_t kColsUsed = kSfbBase + kStages * kStepsPerStage * kSfbCols;
+  static constexpr uint32_t kABase = kSfbBase + kStages * kStepsPerStage * kSfbCols;
+  static constexpr uint32_t kColsUsed = kABase + kStages * kStepsPerStage * kACols;
+  // epilogue staging per warp: 32 rows of BN fp32 values at most
+  static constexpr uint32_t kEpiWarpBytes = (uint32_t)BN * 32 * 4;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
-  static_assert(kColsUsed <= kTmemCols, "tensor-memory columns");
+  static_assert(kColsUsed + 8 <= kTmemCols, "tensor-memory columns");
+  static_assert(4 * kEpiWarpBytes <= kStages * kStageBytes, "epilogue staging fits the stages");
 };
 
 // ---- tcgen05 ----------------------------------------------------------------
@@ -121,12 +136,6 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t saddr) {
   return smem_desc(saddr, 16, 1024, 2);
 }
 
-// One 512-byte scale tile: 32 lines of 16 bytes, no swizzle, 8-line groups
-// 128 bytes apart (a single 16-byte column, so no leading offset).
-__device__ __forceinline__ uint64_t scale_desc(uint32_t saddr) {
-  return smem_desc(saddr, 0, 128, 0);
-}
-
 // Instruction descriptor of the block-scaled MMA: A and B E2M1 (format 1 of
 // the FP4 kinds, bits 7-9 and 10-11), both K-major, no negation, dense,
 // UE4M3 scales (bit 23 = 0), scale-factor ids 0, N / 8 at bits 17-22,
@@ -135,23 +144,17 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t m, uint32_t n) {
   return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-// 32 lines x 128 bits of shared memory into four columns of tensor memory,
-// the same lines in each of the four lane quarters.
-__device__ __forceinline__ void tmem_copy_scales(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-
-// d (tensor memory) (+)= A B^T over one 64-element k-step, A and B scaled
-// per 16-element block by the UE4M3 scales in tensor memory at sfa / sfb.
-__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+// d (tensor memory) (+)= A B^T over one 64-element k-step, A in tensor
+// memory at a_tmem, B in shared memory, both scaled per 16-element block by
+// the UE4M3 scales in tensor memory at sfa / sfb.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
       " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-      " [%0], %1, %2, %3, [%4], [%5], p;\n}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
       "r"(accumulate)
       : "memory");
 }
@@ -182,18 +185,89 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16 / 32 consecutive 32-bit columns of this thread's lane from registers.
+__device__ __forceinline__ void tmem_store16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+      "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+      "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+      "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+      "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_store_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t e) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
+               "r"(e)
+               : "memory");
+}
+
+// One box (32 rows x 128 bytes, 128-byte swizzle) from shared to global memory.
+__device__ __forceinline__ void tensor_store_2d(const CUtensorMap* map, uint32_t src, uint32_t c0,
+                                                uint32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_commit_and_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
 // ---- the kernel ---------------------------------------------------------------
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_nvfp4_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
-                 const float* __restrict__ gs_a, const float* __restrict__ gs_b, uint32_t m,
-                 uint32_t n, uint32_t k, void* __restrict__ d, uint32_t d_bf16,
+                 const __grid_constant__ CUtensorMap map_d, const uint8_t* __restrict__ sfa,
+                 const uint8_t* __restrict__ sfb, const float* __restrict__ gs_a,
+                 const float* __restrict__ gs_b, uint32_t m, uint32_t n, uint32_t k,
+                 void* __restrict__ d, uint32_t d_bf16, uint32_t tma_out,
                  uint32_t* __restrict__ err, uint64_t wait_ns) {
   using S = GemmShape<BN>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[S::kStages], empty[S::kStages], acc_full;
+  // full: the stage's copies landed; staged: its A and scales are in tensor
+  // memory; empty: its MMAs completed; acc_full: the last MMA completed
+  __shared__ __align__(8) uint64_t full[S::kStages], staged[S::kStages], empty[S::kStages],
+      acc_full;
   __shared__ uint32_t tmem_base;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
@@ -206,6 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&staged[s], 4);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&acc_full, 1);
@@ -249,11 +324,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (uint32_t j = first; j < kb; ++j)
       mbar_wait(&full[j % S::kStages], (j / S::kStages) & 1u, wait_ns, err);
   } else if (warp == 1 && lane == 0) {
-    // ---- scale copies and MMAs ----
+    // ---- MMAs ----
     constexpr uint32_t idesc = mma_idesc(128, BN);
-    const uint32_t bands_b = (n + 127u) / 128u, band_b0 = n0 / 128u;
     bool ok = true;
     for (uint32_t kb = 0; kb < nkb; ++kb) {
+      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
+      if (!mbar_wait(&staged[s], ph, wait_ns, err) || !mbar_wait(&full[s], ph, wait_ns, err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t b_smem = smem_addr(smem + s * S::kStageBytes + S::kABytes);
+      const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
+      const uint32_t step0 = s * kStepsPerStage;
+      for (uint32_t j = 0; j < steps; ++j) {
+        // k-step j sits 32 bytes further along each 128-byte row of B
+        mma_nvf4(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
+                 operand_desc(b_smem + 32u * j), idesc,
+                 tmem + S::kSfaBase + (step0 + j) * S::kSfaCols,
+                 tmem + S::kSfbBase + (step0 + j) * S::kSfbCols, (kb | j) != 0u ? 1u : 0u);
+      }
+      tc_commit(&empty[s]);
+    }
+    if (ok) tc_commit(&acc_full);
+  } else if (warp >= 2) {
+    // ---- stagers: warp w owns lane quarter q = w mod 4 (tile rows 32 q ..) ----
+    const uint32_t q = warp & 3u;
+    const uint32_t row = 32u * q + lane;                 // row inside the tile
+    const uint32_t lane_base = tmem + ((32u * q) << 16);
+    bool ok = true;
+    for (uint32_t kb = 0; kb < nkb && ok; ++kb) {
       const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
       if (!mbar_wait(&full[s], ph, wait_ns, err)) {
         ok = false;
@@ -262,67 +362,135 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t st = smem_addr(smem + s * S::kStageBytes);
       const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
-      const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
-      for (uint32_t j = 0; j < steps; ++j) {
-        const uint32_t ta = tmem + S::kSfaBase + (s * kStepsPerStage + j) * S::kSfaCols;
-        const uint32_t tb = tmem + S::kSfbBase + (s * kStepsPerStage + j) * S::kSfbCols;
-        tmem_copy_scales(ta, scale_desc(sf_a + j * kSfTile));
-        for (uint32_t b = 0; b < S::kBands; ++b)
-          if (band_b0 + b < bands_b)
-            tmem_copy_scales(tb + 4u * b, scale_desc(sf_b + (b * kStepsPerStage + j) * kSfTile));
-        // k-step j sits 32 bytes further along each 128-byte row
-        mma_nvf4(tmem, operand_desc(st + 32u * j), operand_desc(st + S::kABytes + 32u * j), idesc,
-                 ta, tb, (kb | j) != 0u ? 1u : 0u);
+      const uint32_t step0 = s * kStepsPerStage;
+      {
+        // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
+        uint32_t w[32];
+#pragma unroll
+        for (uint32_t c = 0; c < 8; ++c) {
+          const uint4 v = lds128(st + swz128(row, c));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tmem_store32(lane_base + S::kABase + step0 * S::kACols, w);
       }
-      tc_commit(&empty[s]);
+      {
+        // A scales: line `lane` of each k-step's tile
+        uint32_t w[16];
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j) {
+          const uint4 v = lds128(sf_a + j * kSfTile + lane * 16u);
+          w[4 * j] = v.x;
+          w[4 * j + 1] = v.y;
+          w[4 * j + 2] = v.z;
+          w[4 * j + 3] = v.w;
+        }
+        tmem_store16(lane_base + S::kSfaBase + step0 * S::kSfaCols, w);
+      }
+      if constexpr (S::kBands == 2) {
+        // B scales, k-step j: band 0 then band 1
+        uint32_t w[32];
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j)
+#pragma unroll
+          for (uint32_t b = 0; b < 2; ++b) {
+            const uint4 v = lds128(sf_b + (b * kStepsPerStage + j) * kSfTile + lane * 16u);
+            w[8 * j + 4 * b] = v.x;
+            w[8 * j + 4 * b + 1] = v.y;
+            w[8 * j + 4 * b + 2] = v.z;
+            w[8 * j + 4 * b + 3] = v.w;
+          }
+        tmem_store32(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
+      } else {
+        uint32_t w[16];
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j) {
+          const uint4 v = lds128(sf_b + j * kSfTile + lane * 16u);
+          w[4 * j] = v.x;
+          w[4 * j + 1] = v.y;
+          w[4 * j + 2] = v.z;
+          w[4 * j + 3] = v.w;
+        }
+        tmem_store16(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&staged[s]);
     }
-    if (ok) tc_commit(&acc_full);
-  } else if (warp >= 2) {
-    // ---- epilogue: warp w reads lane quarter w mod 4 ----
-    const uint32_t q = warp & 3u;
-    const bool ok = mbar_wait(&acc_full, 0, wait_ns, err);
+    // ---- epilogue ----
+    if (ok) ok = mbar_wait(&acc_full, 0, wait_ns, err);
     tc_fence_after();
     if (ok) {
       const float alpha = __fmul_rn(gs_a[0], gs_b[0]);
-      const uint32_t row = m0 + 32u * q + lane;
-      const bool row_in = row < m;
-      for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
-        uint32_t v[32];
-        tmem_load32(tmem + ((32u * q) << 16) + c, v);
-        const uint32_t col = n0 + c;
-        if (!row_in || col >= n) continue;
-        const uint32_t cnt = min(32u, n - col);
-        if (d_bf16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(d) + (uint64_t)row * n + col;
-          if (cnt == 32 && (n & 7u) == 0) {
+      if (tma_out) {
+        // stage the warp's 32 rows in 128-byte-swizzled boxes, then store
+        const uint32_t stg = smem_addr(smem) + q * S::kEpiWarpBytes;
+        for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
+          uint32_t v[32];
+          tmem_load32(lane_base + c, v);
+          if (d_bf16) {
+            const uint32_t box = stg + (c / 64) * kBoxBytes, c0 = (c % 64) / 8;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t w[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(
-                    __fmul_rn(alpha, __uint_as_float(v[8 * i + 2 * t])),
-                    __fmul_rn(alpha, __uint_as_float(v[8 * i + 2 * t + 1])));
-                w[t] = *reinterpret_cast<const uint32_t*>(&pr);
-              }
-              reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (uint32_t i = 0; i < 4; ++i) {
+              const uint32_t* u = v + 8 * i;
+              sts128(box + swz128(lane, c0 + i),
+                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[0])),
+                            __fmul_rn(alpha, __uint_as_float(u[1]))),
+                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[2])),
+                            __fmul_rn(alpha, __uint_as_float(u[3]))),
+                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[4])),
+                            __fmul_rn(alpha, __uint_as_float(u[5]))),
+                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[6])),
+                            __fmul_rn(alpha, __uint_as_float(u[7]))));
             }
           } else {
-            for (uint32_t i = 0; i < cnt; ++i)
-              out[i] = __float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(v[i])));
-          }
-        } else {
-          float* out = static_cast<float*>(d) + (uint64_t)row * n + col;
-          if (cnt == 32 && (n & 3u) == 0) {
+            const uint32_t box = stg + (c / 32) * kBoxBytes;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              reinterpret_cast<float4*>(out)[i] =
-                  make_float4(__fmul_rn(alpha, __uint_as_float(v[4 * i])),
-                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 1])),
-                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 2])),
-                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 3])));
-          } else {
-            for (uint32_t i = 0; i < cnt; ++i) out[i] = __fmul_rn(alpha, __uint_as_float(v[i]));
+            for (uint32_t i = 0; i < 8; ++i) {
+              const uint32_t* u = v + 4 * i;
+              sts128(box + swz128(lane, i),
+                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[0]))),
+                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[1]))),
+                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[2]))),
+                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[3]))));
+            }
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t cols_per_box = d_bf16 ? 64u : 32u;
+          const uint32_t y = m0 + 32u * q;
+          if (y < m)
+            for (uint32_t b = 0; b < (uint32_t)BN / cols_per_box; ++b) {
+              const uint32_t x = n0 + b * cols_per_box;
+              if (x < n) tensor_store_2d(&map_d, stg + b * kBoxBytes, x, y);
+            }
+          bulk_store_commit_and_drain();
+        }
+        __syncwarp();
+      } else {
+        // element stores (rows whose pitch is not a multiple of 16 bytes)
+        const uint32_t grow = m0 + row;
+        for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
+          uint32_t v[32];
+          tmem_load32(lane_base + c, v);
+          const uint32_t col = n0 + c;
+          if (grow >= m || col >= n) continue;
+          const uint32_t cnt = min(32u, n - col);
+#pragma unroll
+          for (uint32_t i = 0; i < 32; ++i) {
+            if (i < cnt) {
+              const float y = __fmul_rn(alpha, __uint_as_float(v[i]));
+              if (d_bf16)
+                static_cast<__nv_bfloat16*>(d)[(uint64_t)grow * n + col + i] =
+                    __float2bfloat16_rn(y);
+              else
+                static_cast<float*>(d)[(uint64_t)grow * n + col + i] = y;
+            }
           }
         }
       }
@@ -348,6 +516,23 @@ bool encode_operand_map(const void* codes, int64_t rows, int64_t k, uint32_t box
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// d [m, n] in boxes of 32 rows x 128 bytes, 128-byte swizzle (stores past m
+// or n are dropped); false when a row is not a multiple of 16 bytes.
+bool encode_output_map(void* d, int64_t m, int64_t n, int d_bf16, CUtensorMap* map) {
+  const int64_t esize = d_bf16 ? 2 : 4;
+  if ((n * esize) % 16 != 0) return false;
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dim[2] = {(cuuint64_t)n, (cuuint64_t)m};
+  const cuuint64_t stride[1] = {(cuuint64_t)(n * esize)};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), 32};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, d_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+             d, dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN>
 cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                       const void* b_codes, const void* b_sf, const float* b_gs, int64_t m,
@@ -369,13 +554,15 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
       set_for[dev] = true;
     }
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, md;
   if (!encode_operand_map(a_codes, m, k, 128, &ma) || !encode_operand_map(b_codes, n, k, BN, &mb))
     return cudaErrorInvalidValue;
+  const bool tma_out = encode_output_map(d, m, n, d_bf16, &md);
+  if (!tma_out) std::memset(&md, 0, sizeof(md));
   const dim3 grid((unsigned)((n + BN - 1) / BN), (unsigned)((m + 127) / 128));
   k_nvfp4_gemm<BN><<<grid, kGemmThreads, S::kSmemBytes, st>>>(
-      ma, mb, (const uint8_t*)a_sf, (const uint8_t*)b_sf, a_gs, b_gs, (uint32_t)m, (uint32_t)n,
-      (uint32_t)k, d, d_bf16 ? 1u : 0u, err, wait_ns);
+      ma, mb, md, (const uint8_t*)a_sf, (const uint8_t*)b_sf, a_gs, b_gs, (uint32_t)m,
+      (uint32_t)n, (uint32_t)k, d, d_bf16 ? 1u : 0u, tma_out ? 1u : 0u, err, wait_ns);
   return cudaGetLastError();
 }
 
