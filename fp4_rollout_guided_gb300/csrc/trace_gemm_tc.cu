@@ -39,9 +39,11 @@
 // columns inside d are stored.
 //
 // Tensor memory (512 columns of 32-bit lanes, lane = tile row): the
-// accumulator in columns [0, BN); per stage, the A scales (four columns per
-// k-step), the B scales (BN / 32 columns per k-step), then A (eight columns
-// of packed codes per k-step).  Scales follow the tile layout: line L of a
+// accumulator in columns [0, BN), then a ring of slots (one stage each,
+// fewer slots than shared-memory stages so that the loads run a stage
+// further ahead) holding the A scales (four columns per k-step), the B
+// scales (BN / 32 columns per k-step) and A (eight columns of packed codes
+// per k-step).  Scales follow the tile layout: line L of a
 // 512-byte tile holds rows L, L + 32, L + 64, L + 96, and lane L of every
 // quarter holds line L, so column c of lane L holds the four scales of row
 // L + 32 c for the k-step.
@@ -77,22 +79,24 @@ struct GemmShape {
   static constexpr uint32_t kSfaBytes = kStepsPerStage * kSfTile;
   static constexpr uint32_t kSfbBytes = kBands * kStepsPerStage * kSfTile;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr uint32_t kStages = BN == 256 ? 3 : 5;
+  static constexpr uint32_t kStages = BN == 256 ? 4 : 6;  // shared-memory ring
+  static constexpr uint32_t kSlots = BN == 256 ? 3 : 5;   // tensor-memory ring
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   // tensor-memory columns per k-step and their regions
   static constexpr uint32_t kSfaCols = 4;
   static constexpr uint32_t kSfbCols = 4 * kBands;
   static constexpr uint32_t kACols = 8;  // 64 packed E2M1 codes
   static constexpr uint32_t kSfaBase = BN;
-  static constexpr uint32_t kSfbBase = kSfaBase + kStages * kStepsPerStage * kSfaCols;
-  static constexpr uint32_t kABase = kSfbBase + kStages * kStepsPerStage * kSfbCols;
-  static constexpr uint32_t kColsUsed = kABase + kStages * kStepsPerStage * kACols;
+  static constexpr uint32_t kSfbBase = kSfaBase + kSlots * kStepsPerStage * kSfaCols;
+  static constexpr uint32_t kABase = kSfbBase + kSlots * kStepsPerStage * kSfbCols;
+  static constexpr uint32_t kColsUsed = kABase + kSlots * kStepsPerStage * kACols;
   // epilogue staging per warp: 32 rows of BN fp32 values at most
   static constexpr uint32_t kEpiWarpBytes = (uint32_t)BN * 32 * 4;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(kColsUsed + 8 <= kTmemCols, "tensor-memory columns");
   static_assert(4 * kEpiWarpBytes <= kStages * kStageBytes, "epilogue staging fits the stages");
+  static_assert(kSlots <= kStages, "a slot is refilled only after its stage's MMAs");
 };
 
 // ---- tcgen05 ----------------------------------------------------------------
@@ -264,9 +268,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                  uint32_t* __restrict__ err, uint64_t wait_ns) {
   using S = GemmShape<BN>;
   extern __shared__ uint8_t smem_raw[];
-  // full: the stage's copies landed; staged: its A and scales are in tensor
-  // memory; empty: its MMAs completed; acc_full: the last MMA completed
-  __shared__ __align__(8) uint64_t full[S::kStages], staged[S::kStages], empty[S::kStages],
+  // full: a stage's copies landed; empty: its MMAs completed (its shared
+  // memory and its tensor-memory slot are free again); staged: a slot holds
+  // its stage's A and scales; acc_full: the last MMA completed
+  __shared__ __align__(8) uint64_t full[S::kStages], empty[S::kStages], staged[S::kSlots],
       acc_full;
   __shared__ uint32_t tmem_base;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -280,9 +285,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&staged[s], 4);
       mbar_init(&empty[s], 1);
     }
+    for (uint32_t t = 0; t < S::kSlots; ++t) mbar_init(&staged[t], 4);
     mbar_init(&acc_full, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -329,14 +334,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (uint32_t kb = 0; kb < nkb; ++kb) {
       const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      if (!mbar_wait(&staged[s], ph, wait_ns, err) || !mbar_wait(&full[s], ph, wait_ns, err)) {
+      const uint32_t t = kb % S::kSlots, pt = (kb / S::kSlots) & 1u;
+      if (!mbar_wait(&staged[t], pt, wait_ns, err) || !mbar_wait(&full[s], ph, wait_ns, err)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t b_smem = smem_addr(smem + s * S::kStageBytes + S::kABytes);
       const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
-      const uint32_t step0 = s * kStepsPerStage;
+      const uint32_t step0 = t * kStepsPerStage;
       for (uint32_t j = 0; j < steps; ++j) {
         // k-step j sits 32 bytes further along each 128-byte row of B
         mma_nvf4(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
@@ -355,14 +361,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (uint32_t kb = 0; kb < nkb && ok; ++kb) {
       const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      if (!mbar_wait(&full[s], ph, wait_ns, err)) {
+      const uint32_t t = kb % S::kSlots;
+      // slot t last held k-block kb - kSlots: its MMAs completed once that
+      // k-block's stage was released
+      const uint32_t prev = kb - S::kSlots;
+      if (!mbar_wait(&full[s], ph, wait_ns, err) ||
+          (kb >= S::kSlots && !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u,
+                                         wait_ns, err))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t st = smem_addr(smem + s * S::kStageBytes);
       const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
-      const uint32_t step0 = s * kStepsPerStage;
+      const uint32_t step0 = t * kStepsPerStage;
       {
         // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
         uint32_t w[32];
@@ -418,7 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tmem_store_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&staged[s]);
+      if (lane == 0) mbar_arrive(&staged[t]);
     }
     // ---- epilogue ----
     if (ok) ok = mbar_wait(&acc_full, 0, wait_ns, err);
