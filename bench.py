@@ -869,7 +869,7 @@ def main():
                     help="time the NVFP4 GEMM over rollout codes instead")
     ap.add_argument("--gemm-shape", type=int, nargs=3, default=[16384, 8192, 8192],
                     metavar=("M", "N", "K"))
-    ap.add_argument("--gemm-form", default="tc256", choices=["tc256", "tc128", "cublaslt"],
+    ap.add_argument("--gemm-form", default="tc256", choices=["tc256", "tc128", "tc_pair", "cublaslt"],
                     help="GEMM form: hand-written tcgen05 kernel (tile N 256 / 128) or cuBLASLt")
     ap.add_argument("--transport", action="store_true",
                     help="time the guide record's device/host/disk round trip instead")

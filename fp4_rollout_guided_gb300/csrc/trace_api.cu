@@ -290,7 +290,8 @@ trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t va
       h->wait_extra = (uint32_t)value;
       return TRACE_OK;
     case TRACE_OPT_GEMM:
-      if (value != TRACE_GEMM_TC256 && value != TRACE_GEMM_CUBLASLT && value != TRACE_GEMM_TC128)
+      if (value != TRACE_GEMM_TC256 && value != TRACE_GEMM_CUBLASLT && value != TRACE_GEMM_TC128 &&
+          value != TRACE_GEMM_TC_PAIR)
         return TRACE_ERR_INVALID_ARG;
       h->gemm = (int)value;
       return TRACE_OK;
@@ -813,14 +814,16 @@ extern "C" trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   if (h->gemm != TRACE_GEMM_CUBLASLT) {
-    if (m > 65535LL * 128) return TRACE_ERR_INVALID_ARG;  // output tile rows on grid y
+    if (m > 65535LL * 128) return TRACE_ERR_INVALID_ARG;  // 128-row tiles on grid y
     cudaError_t e = begin_call(h, st);
     if (e == cudaSuccess)
       e = timed(h, TRACE_KERNEL_NVFP4_GEMM, st, [&] {
         return tfp4::launch_nvfp4_gemm_tc(a_codes, a_scales_mma, a_gs, b_codes, b_scales_mma,
                                           b_gs, m, n, k, d, d_type == TRACE_OUT_BF16,
-                                          h->gemm == TRACE_GEMM_TC128 ? 128 : 256, h->scratch.err,
-                                          h->wait_ns, st);
+                                          h->gemm == TRACE_GEMM_TC128    ? tfp4::kGemmTile128
+                                          : h->gemm == TRACE_GEMM_TC_PAIR ? tfp4::kGemmTilePair
+                                                                          : tfp4::kGemmTile256,
+                                          h->scratch.err, h->wait_ns, st);
       });
     const cudaError_t e2 = end_call(h, st);
     if (e != cudaSuccess) return cuda_fail(h, e);

@@ -71,21 +71,28 @@ constexpr uint32_t kSfTile = 512;        // bytes of one scale tile: 128 rows x 
 constexpr uint32_t kStepsPerStage = 4;   // 64-element MMA k-steps per stage
 constexpr uint32_t kBoxBytes = 4096;     // one output box: 32 rows x 128 bytes
 
-template <int BN>
+// PAIR: one tile of 256 x BN on an SM pair (tcgen05 cta_group::2): each CTA
+// holds 128 rows of A and of the accumulator and BN / 2 rows of B.
+template <int BN, bool PAIR>
 struct GemmShape {
+  static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
+  static constexpr uint32_t kBRows = PAIR ? (uint32_t)BN / 2 : (uint32_t)BN;  // B rows per CTA
   static constexpr uint32_t kABytes = 128u * kBK / 2;
-  static constexpr uint32_t kBBytes = (uint32_t)BN * kBK / 2;
+  static constexpr uint32_t kBBytes = kBRows * kBK / 2;
   static constexpr uint32_t kBands = (uint32_t)BN / 128;  // 128-row scale bands of a B tile
   static constexpr uint32_t kSfaBytes = kStepsPerStage * kSfTile;
   static constexpr uint32_t kSfbBytes = kBands * kStepsPerStage * kSfTile;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr uint32_t kStages = BN == 256 ? 4 : 6;  // shared-memory ring
-  static constexpr uint32_t kSlots = BN == 256 ? 3 : 5;   // tensor-memory ring
+  static constexpr uint32_t kStages = PAIR ? 5 : BN == 256 ? 4 : 6;  // shared-memory ring
+  // A in tensor memory (single CTA) or read from shared memory by the MMAs
+  // (pair: the stagers then move only scales, and every stage has a slot)
+  static constexpr bool kATmem = !PAIR;
+  static constexpr uint32_t kSlots = PAIR ? kStages : BN == 256 ? 3 : 5;  // tensor-memory ring
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   // tensor-memory columns per k-step and their regions
   static constexpr uint32_t kSfaCols = 4;
   static constexpr uint32_t kSfbCols = 4 * kBands;
-  static constexpr uint32_t kACols = 8;  // 64 packed E2M1 codes
+  static constexpr uint32_t kACols = kATmem ? 8 : 0;  // 64 packed E2M1 codes
   static constexpr uint32_t kSfaBase = BN;
   static constexpr uint32_t kSfbBase = kSfaBase + kSlots * kStepsPerStage * kSfaCols;
   static constexpr uint32_t kABase = kSfbBase + kSlots * kStepsPerStage * kSfbCols;
@@ -101,19 +108,93 @@ struct GemmShape {
 
 // ---- tcgen05 ----------------------------------------------------------------
 
+// Allocation, MMAs and commits name the CTA group: 1 (this CTA) or 2 (the
+// SM pair of a two-CTA cluster, where both CTAs allocate the same columns
+// together and the even CTA issues the MMAs for both).
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               ::"r"(smem_addr(dst_smem)), "r"(cols)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(dst_smem)), "r"(cols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(dst_smem)), "r"(cols)
+                 : "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+}
+
+// ---- clusters -----------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  return a;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// Bounded wait that also acquires what other CTAs of the cluster released.
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity,
+                                                    uint64_t limit_ns, uint32_t* err) {
+  for (uint32_t it = 0; it < 16; ++it)
+    if (mbar_try_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if ((it & 15u) == 15u && global_ns() - t0 > limit_ns) break;
+  }
+  atomicOr(err, 2u);
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns, uint32_t* err) {
+  return mbar_try_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, limit_ns, err);
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -150,25 +231,91 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t m, uint32_t n) {
 
 // d (tensor memory) (+)= A B^T over one 64-element k-step, A in tensor
 // memory at a_tmem, B in shared memory, both scaled per 16-element block by
-// the UE4M3 scales in tensor memory at sfa / sfb.
+// the UE4M3 scales in tensor memory at sfa / sfb.  For a pair, the same
+// addresses name both CTAs' tensor and shared memory.
+template <bool PAIR>
 __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-      " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-      "r"(accumulate)
-      : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
 }
 
-// Arrive on bar once every tcgen05 operation this thread issued so far has
-// completed.
+// The same with A in shared memory (descriptor adesc).
+template <bool PAIR>
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
+// 32 lines x 128 bits of shared memory into four columns of tensor memory,
+// the same lines in each of the four lane quarters; for a pair, each CTA's
+// lines at this address into its own tensor memory.
+template <bool PAIR>
+__device__ __forceinline__ void tmem_copy_scales(uint32_t taddr, uint32_t saddr) {
+  const uint64_t desc = smem_desc(saddr, 0, 128, 0);  // 8-line groups 128 bytes apart
+  if constexpr (PAIR)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
+}
+
+// Arrive on bar (in this CTA, or for a pair in both CTAs) once every tcgen05
+// operation this thread issued so far has completed.
+template <bool PAIR>
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_addr(bar))
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)), "h"((uint16_t)3)
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Arrive on bar in this CTA only once this thread's tcgen05 operations completed.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_local(uint64_t* bar) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_addr(bar))
+                 : "memory");
+  else
+    tc_commit<false>(bar);
 }
 
 // 32 consecutive 32-bit columns of this thread's lane.
@@ -258,7 +405,7 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 // ---- the kernel ---------------------------------------------------------------
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_nvfp4_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const __grid_constant__ CUtensorMap map_d, const uint8_t* __restrict__ sfa,
@@ -266,19 +413,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                  const float* __restrict__ gs_b, uint32_t m, uint32_t n, uint32_t k,
                  void* __restrict__ d, uint32_t d_bf16, uint32_t tma_out,
                  uint32_t* __restrict__ err, uint64_t wait_ns) {
-  using S = GemmShape<BN>;
+  using S = GemmShape<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   // full: a stage's copies landed; empty: its MMAs completed (its shared
   // memory and its tensor-memory slot are free again); staged: a slot holds
   // its stage's A and scales; acc_full: the last MMA completed
+  // (pair: staged, in the even CTA, is the odd CTA's stage landing; empty
+  // and acc_full arrive in both CTAs; drain: this CTA's MMAs retired)
   __shared__ __align__(8) uint64_t full[S::kStages], empty[S::kStages], staged[S::kSlots],
-      acc_full;
+      acc_full, drain;
   __shared__ uint32_t tmem_base;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-  const uint32_t m0 = blockIdx.y * 128u, n0 = blockIdx.x * (uint32_t)BN;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  // this CTA's A and accumulator rows, the tile's columns, this CTA's B rows
+  const uint32_t m0 = blockIdx.y * (PAIR ? 256u : 128u) + 128u * rank;
+  const uint32_t n0 = (PAIR ? blockIdx.x >> 1 : blockIdx.x) * (uint32_t)BN;
+  const uint32_t nb0 = n0 + S::kBRows * rank;
   const uint32_t nkb = (k + kBK - 1) / kBK;
   const uint32_t tiles_per_row = (k + 63) / 64;  // scale tiles along k (64 elements each)
 
@@ -287,22 +440,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (uint32_t t = 0; t < S::kSlots; ++t) mbar_init(&staged[t], 4);
+    for (uint32_t t = 0; t < S::kSlots; ++t) mbar_init(&staged[t], PAIR ? 1 : 4);
     mbar_init(&acc_full, 1);
+    mbar_init(&drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(&tmem_base, kTmemCols);
+    tmem_relinquish<PAIR>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and columns exist
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
   if (warp == 0 && lane == 0) {
     // ---- producer ----
     const uint32_t band_a = m0 / 128u, band_b0 = n0 / 128u;
+    const uint32_t na = band_a < (m + 127u) / 128u ? 1u : 0u;  // (a pair's odd CTA may lie past m)
     const uint32_t bands_b = (n + 127u) / 128u;
     uint32_t kb = 0;
     for (; kb < nkb; ++kb) {
@@ -312,13 +468,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
       uint32_t nb = 0;
       for (uint32_t b = 0; b < S::kBands; ++b) nb += band_b0 + b < bands_b ? 1u : 0u;
-      mbar_expect_tx(&full[s], S::kABytes + S::kBBytes + (1u + nb) * steps * kSfTile);
+      mbar_expect_tx(&full[s], S::kABytes + S::kBBytes + (na + nb) * steps * kSfTile);
       tensor_load_2d(st, &map_a, kb * (kBK / 2), m0, &full[s]);
-      tensor_load_2d(st + S::kABytes, &map_b, kb * (kBK / 2), n0, &full[s]);
+      tensor_load_2d(st + S::kABytes, &map_b, kb * (kBK / 2), nb0, &full[s]);
       const uint64_t tile0 = kStepsPerStage * kb;
-      bulk_load(st + S::kABytes + S::kBBytes,
-                sfa + ((uint64_t)band_a * tiles_per_row + tile0) * kSfTile, steps * kSfTile,
-                &full[s]);
+      if (na)
+        bulk_load(st + S::kABytes + S::kBBytes,
+                  sfa + ((uint64_t)band_a * tiles_per_row + tile0) * kSfTile, steps * kSfTile,
+                  &full[s]);
       for (uint32_t b = 0; b < nb; ++b)
         bulk_load(st + S::kABytes + S::kBBytes + S::kSfaBytes + b * kStepsPerStage * kSfTile,
                   sfb + ((uint64_t)(band_b0 + b) * tiles_per_row + tile0) * kSfTile,
@@ -328,46 +485,78 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t first = kb > S::kStages ? kb - S::kStages : 0u;
     for (uint32_t j = first; j < kb; ++j)
       mbar_wait(&full[j % S::kStages], (j / S::kStages) & 1u, wait_ns, err);
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMAs ----
-    constexpr uint32_t idesc = mma_idesc(128, BN);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---- MMAs (for a pair: the even CTA, for both) ----
+    constexpr uint32_t idesc = mma_idesc(PAIR ? 256 : 128, BN);
     bool ok = true;
     for (uint32_t kb = 0; kb < nkb; ++kb) {
       const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
       const uint32_t t = kb % S::kSlots, pt = (kb / S::kSlots) & 1u;
-      if (!mbar_wait(&staged[t], pt, wait_ns, err) || !mbar_wait(&full[s], ph, wait_ns, err)) {
+      const bool staged_ok = PAIR ? mbar_wait_cluster(&staged[t], pt, wait_ns, err)
+                                  : mbar_wait(&staged[t], pt, wait_ns, err);
+      if (!staged_ok || !mbar_wait(&full[s], ph, wait_ns, err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t b_smem = smem_addr(smem + s * S::kStageBytes + S::kABytes);
+      const uint32_t a_smem = smem_addr(smem + s * S::kStageBytes);
+      const uint32_t b_smem = a_smem + S::kABytes;
       const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
       const uint32_t step0 = t * kStepsPerStage;
-      for (uint32_t j = 0; j < steps; ++j) {
-        // k-step j sits 32 bytes further along each 128-byte row of B
-        mma_nvf4(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
-                 operand_desc(b_smem + 32u * j), idesc,
-                 tmem + S::kSfaBase + (step0 + j) * S::kSfaCols,
-                 tmem + S::kSfbBase + (step0 + j) * S::kSfbCols, (kb | j) != 0u ? 1u : 0u);
+      if constexpr (PAIR) {
+        // scales of both CTAs, each from its own shared memory (paired copies)
+        const uint32_t sf_a = b_smem + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
+        for (uint32_t j = 0; j < steps; ++j) {
+          tmem_copy_scales<true>(tmem + S::kSfaBase + (step0 + j) * S::kSfaCols,
+                                 sf_a + j * kSfTile);
+          for (uint32_t b = 0; b < S::kBands; ++b)
+            tmem_copy_scales<true>(tmem + S::kSfbBase + (step0 + j) * S::kSfbCols + 4u * b,
+                                   sf_b + (b * kStepsPerStage + j) * kSfTile);
+        }
       }
-      tc_commit(&empty[s]);
+      for (uint32_t j = 0; j < steps; ++j) {
+        // k-step j sits 32 bytes further along each 128-byte row of A and B
+        const uint32_t sfa_t = tmem + S::kSfaBase + (step0 + j) * S::kSfaCols;
+        const uint32_t sfb_t = tmem + S::kSfbBase + (step0 + j) * S::kSfbCols;
+        const uint32_t acc = (kb | j) != 0u ? 1u : 0u;
+        if constexpr (S::kATmem)
+          mma_nvf4<PAIR>(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
+                         operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
+        else
+          mma_nvf4_ss<PAIR>(tmem, operand_desc(a_smem + 32u * j), operand_desc(b_smem + 32u * j),
+                            idesc, sfa_t, sfb_t, acc);
+      }
+      tc_commit<PAIR>(&empty[s]);
     }
-    if (ok) tc_commit(&acc_full);
+    if (ok) tc_commit<PAIR>(&acc_full);
+    // every MMA issued here has retired before the columns are freed
+    tc_commit_local<PAIR>(&drain);
+    mbar_wait(&drain, 0, wait_ns, err);
+  } else if (PAIR && warp == 1 && lane == 0) {
+    // ---- the odd CTA's relay: its stage landed -> the even CTA's staged ----
+    const uint32_t remote = peer_addr(&staged[0], 0);
+    for (uint32_t kb = 0; kb < nkb; ++kb) {
+      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
+      if (!mbar_wait(&full[s], ph, wait_ns, err)) break;
+      mbar_arrive_remote(remote + (kb % S::kSlots) * (uint32_t)sizeof(uint64_t));
+    }
   } else if (warp >= 2) {
     // ---- stagers: warp w owns lane quarter q = w mod 4 (tile rows 32 q ..) ----
     const uint32_t q = warp & 3u;
     const uint32_t row = 32u * q + lane;                 // row inside the tile
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     bool ok = true;
-    for (uint32_t kb = 0; kb < nkb && ok; ++kb) {
+    // (a pair's scales are copied by the MMA thread: no staging)
+    const uint32_t nstage = PAIR ? 0u : nkb;
+    for (uint32_t kb = 0; kb != nstage && ok; ++kb) {
       const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
       const uint32_t t = kb % S::kSlots;
       // slot t last held k-block kb - kSlots: its MMAs completed once that
       // k-block's stage was released
       const uint32_t prev = kb - S::kSlots;
       if (!mbar_wait(&full[s], ph, wait_ns, err) ||
-          (kb >= S::kSlots && !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u,
-                                         wait_ns, err))) {
+          (S::kSlots < S::kStages && kb >= S::kSlots &&
+           !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u, wait_ns, err))) {
         ok = false;
         break;
       }
@@ -375,7 +564,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t st = smem_addr(smem + s * S::kStageBytes);
       const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
       const uint32_t step0 = t * kStepsPerStage;
-      {
+      if constexpr (S::kATmem) {
         // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
         uint32_t w[32];
 #pragma unroll
@@ -430,7 +619,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tmem_store_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&staged[t]);
+      if (lane == 0) {
+        if (PAIR && rank != 0)
+          mbar_arrive_remote(peer_addr(&staged[t], 0));
+        else
+          mbar_arrive(&staged[t]);
+      }
     }
     // ---- epilogue ----
     if (ok) ok = mbar_wait(&acc_full, 0, wait_ns, err);
@@ -510,7 +704,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if constexpr (PAIR) cluster_sync();  // the pair's MMAs and reads are done in both CTAs
+  if (warp == 1) tmem_dealloc<PAIR>(tmem, kTmemCols);
 }
 
 // Codes [rows, k/2] as a 2-D byte tensor, boxes of box_rows rows x 128 bytes
@@ -545,12 +740,12 @@ bool encode_output_map(void* d, int64_t m, int64_t n, int d_bf16, CUtensorMap* m
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                       const void* b_codes, const void* b_sf, const float* b_gs, int64_t m,
                       int64_t n, int64_t k, void* d, int d_bf16, uint32_t* err, uint64_t wait_ns,
                       cudaStream_t st) {
-  using S = GemmShape<BN>;
+  using S = GemmShape<BN, PAIR>;
   static std::mutex mu;
   static bool set_for[64];
   int dev = 0;
@@ -560,22 +755,34 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!set_for[dev]) {
-      e = cudaFuncSetAttribute(k_nvfp4_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)S::kSmemBytes);
+      e = cudaFuncSetAttribute(k_nvfp4_gemm<BN, PAIR>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmemBytes);
       if (e != cudaSuccess) return e;
       set_for[dev] = true;
     }
   }
   CUtensorMap ma, mb, md;
-  if (!encode_operand_map(a_codes, m, k, 128, &ma) || !encode_operand_map(b_codes, n, k, BN, &mb))
+  if (!encode_operand_map(a_codes, m, k, 128, &ma) ||
+      !encode_operand_map(b_codes, n, k, S::kBRows, &mb))
     return cudaErrorInvalidValue;
   const bool tma_out = encode_output_map(d, m, n, d_bf16, &md);
   if (!tma_out) std::memset(&md, 0, sizeof(md));
-  const dim3 grid((unsigned)((n + BN - 1) / BN), (unsigned)((m + 127) / 128));
-  k_nvfp4_gemm<BN><<<grid, kGemmThreads, S::kSmemBytes, st>>>(
-      ma, mb, md, (const uint8_t*)a_sf, (const uint8_t*)b_sf, a_gs, b_gs, (uint32_t)m,
-      (uint32_t)n, (uint32_t)k, d, d_bf16 ? 1u : 0u, tma_out ? 1u : 0u, err, wait_ns);
-  return cudaGetLastError();
+  const int64_t tm = PAIR ? 256 : 128;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + BN - 1) / BN * (PAIR ? 2 : 1)), (unsigned)((m + tm - 1) / tm));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_nvfp4_gemm<BN, PAIR>, ma, mb, md, (const uint8_t*)a_sf,
+                            (const uint8_t*)b_sf, a_gs, b_gs, (uint32_t)m, (uint32_t)n,
+                            (uint32_t)k, d, d_bf16 ? 1u : 0u, tma_out ? 1u : 0u, err, wait_ns);
 }
 
 }  // namespace
@@ -583,15 +790,18 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
 cudaError_t launch_nvfp4_gemm_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                                  const void* b_codes, const void* b_sf, const float* b_gs,
                                  int64_t m, int64_t n, int64_t k, void* d, int d_bf16,
-                                 int tile_n, uint32_t* err, uint64_t wait_ns, cudaStream_t st) {
+                                 int tile, uint32_t* err, uint64_t wait_ns, cudaStream_t st) {
   if (m <= 0 || n <= 0 || k <= 0 || k % 32 || m > 65535LL * 128 || m > UINT32_MAX ||
       n > UINT32_MAX || k > UINT32_MAX)
     return cudaErrorInvalidValue;
-  return tile_n == 128
-             ? launch_tc<128>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d, d_bf16, err,
-                              wait_ns, st)
-             : launch_tc<256>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d, d_bf16, err,
-                              wait_ns, st);
+  if (tile == kGemmTilePair)
+    return launch_tc<256, true>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d, d_bf16,
+                                err, wait_ns, st);
+  return tile == kGemmTile128
+             ? launch_tc<128, false>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d,
+                                     d_bf16, err, wait_ns, st)
+             : launch_tc<256, false>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d,
+                                     d_bf16, err, wait_ns, st);
 }
 
 }  // namespace tfp4

@@ -150,11 +150,13 @@ cudaError_t launch_mma_scales(const void* bs, int64_t rows, int64_t cols, void* 
 cudaError_t launch_gemm_scalars(const float* gs_a, const float* gs_b, float* out,
                                 cudaStream_t st);
 // The hand-written tcgen05 form (trace_gemm_tc.cu): output tiles of
-// 128 x tile_n (128 or 256); a wait that runs out sets *err.
+// 128 x 256, 128 x 128, or 256 x 256 on an SM pair; a wait that runs out
+// sets *err.
+enum { kGemmTile256 = 0, kGemmTile128 = 1, kGemmTilePair = 2 };
 cudaError_t launch_nvfp4_gemm_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                                  const void* b_codes, const void* b_sf, const float* b_gs,
                                  int64_t m, int64_t n, int64_t k, void* d, int d_bf16,
-                                 int tile_n, uint32_t* err, uint64_t wait_ns, cudaStream_t st);
+                                 int tile, uint32_t* err, uint64_t wait_ns, cudaStream_t st);
 // The driver's tensor-map encoder (null if the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool lt_available();

@@ -29,7 +29,7 @@ KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "
 OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3,
            "debug_shrink": 4, "gemm": 5}
 # values of the "gemm" option: the form of nvfp4_gemm
-GEMM_FORMS = {"tc256": 0, "cublaslt": 1, "tc128": 2}
+GEMM_FORMS = {"tc256": 0, "cublaslt": 1, "tc128": 2, "tc_pair": 3}
 MAX_SEGMENTS = 4000
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported device",
           4: "CUDA error", 5: "out of memory", 6: "timeout", 7: "cuBLASLt missing or refused"}

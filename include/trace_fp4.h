@@ -184,15 +184,17 @@ typedef enum {
                                   are counted as out of range and skipped.
                                   Other builds return TRACE_ERR_INVALID_ARG. */
   TRACE_OPT_GEMM = 5           /* form of trace_nvfp4_gemm: TRACE_GEMM_CUBLASLT
-                                  (default), TRACE_GEMM_TC256 or
-                                  TRACE_GEMM_TC128                            */
+                                  (default), TRACE_GEMM_TC256, TRACE_GEMM_TC128
+                                  or TRACE_GEMM_TC_PAIR                       */
 } trace_option_t;
 
 /* Values of TRACE_OPT_GEMM. */
 enum {
   TRACE_GEMM_TC256 = 0,    /* hand-written tcgen05 kernel, 128 x 256 output tiles */
   TRACE_GEMM_CUBLASLT = 1, /* cuBLASLt's block-scaled GEMM                        */
-  TRACE_GEMM_TC128 = 2     /* hand-written tcgen05 kernel, 128 x 128 output tiles */
+  TRACE_GEMM_TC128 = 2,    /* hand-written tcgen05 kernel, 128 x 128 output tiles */
+  TRACE_GEMM_TC_PAIR = 3   /* hand-written tcgen05 kernel, 256 x 256 output tiles
+                              on SM pairs (two-CTA clusters)                      */
 };
 TRACE_API trace_status_t trace_set_option(trace_handle_t h, trace_option_t opt, int64_t value);
 

@@ -744,7 +744,7 @@ GEMM_RAGGED = [(1, 32, 32), (130, 200, 96), (300, 36, 320), (257, 520, 544), (64
                (128, 1, 64), (7, 264, 4128)]
 
 
-@pytest.fixture(params=["cublaslt", "tc256", "tc128"])
+@pytest.fixture(params=["cublaslt", "tc256", "tc128", "tc_pair"])
 def gemm_form(h, request):
     h.set_option("gemm", request.param)
     yield request.param
