@@ -814,7 +814,6 @@ extern "C" trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   if (h->gemm != TRACE_GEMM_CUBLASLT) {
-    if (m > 65535LL * 128) return TRACE_ERR_INVALID_ARG;  // 128-row tiles on grid y
     cudaError_t e = begin_call(h, st);
     if (e == cudaSuccess)
       e = timed(h, TRACE_KERNEL_NVFP4_GEMM, st, [&] {
@@ -823,7 +822,7 @@ extern "C" trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes
                                           h->gemm == TRACE_GEMM_TC128    ? tfp4::kGemmTile128
                                           : h->gemm == TRACE_GEMM_TC_PAIR ? tfp4::kGemmTilePair
                                                                           : tfp4::kGemmTile256,
-                                          h->scratch.err, h->wait_ns, st);
+                                          h->scratch.err, h->wait_ns, h->sm_count, st);
       });
     const cudaError_t e2 = end_call(h, st);
     if (e != cudaSuccess) return cuda_fail(h, e);

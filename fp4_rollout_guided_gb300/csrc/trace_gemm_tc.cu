@@ -14,24 +14,31 @@
 // [rows, k/2] (element 2i in the low nibble: the packed E2M1 operand format)
 // and block scales in the 512-byte tile layout the rollout quantiser writes.
 //
-// One CTA per output tile of 128 x BN, one CTA per SM (its shared memory
-// allows no second), 192 threads in three roles:
+// A persistent grid, one CTA per SM (its shared memory allows no second),
+// each CTA taking output tiles of 128 x BN in turn; 320 threads in roles:
 //   - warp 0 (one lane): producer.  Per k-block of 256 elements it loads the
 //     A tile (128 rows x 128 bytes) and the B tile (BN rows x 128 bytes) with
 //     2-D tensor-map copies in 128-byte swizzle, and the block-scale tiles
 //     (512 bytes per 128 rows and 64 elements of k) with bulk copies, into a
 //     ring of stages completing on mbarriers;
-//   - warps 2-5: stagers, then epilogue.  Per stage each warp moves its
-//     quarter of the A rows and the stage's scale lines from shared into
-//     tensor memory (tcgen05.st, warp w owning lane quarter w mod 4), so
-//     that the MMAs read only B from shared memory and no scale copy
-//     occupies the tensor pipe.  After the last stage each thread reads its
-//     accumulator row, multiplies by fl32(gs_a * gs_b), and the warp stores
-//     its 32 rows through shared memory with tensor-map stores (fp32 or
-//     bf16);
+//   - warps 2-5: stagers.  Per stage each warp moves its quarter of the A
+//     rows and the stage's scale lines from shared into tensor memory
+//     (tcgen05.st, warp w owning lane quarter w mod 4), so that the MMAs read
+//     only B from shared memory and no scale copy occupies the tensor pipe;
 //   - warp 1: allocates the tensor memory; one lane issues the block-scaled
 //     MMAs (128 x BN x 64 each, A and the scales in tensor memory, B in
-//     shared memory) and commits each stage back to the producer.
+//     shared memory), commits each stage back to the producer and each tile
+//     to the epilogue;
+//   - warps 6-9: epilogue.  Each thread reads its accumulator row (its
+//     warp's lane quarter), releases the accumulator to the next tile's
+//     MMAs, multiplies by fl32(gs_a * gs_b) and stores fp32 or bf16, while
+//     the next tile's loads and staging already run.
+// On an SM pair (two-CTA cluster, tcgen05 cta_group::2) the tile is 256 x 256:
+// each CTA holds 128 rows of A and of the accumulator and 128 rows of B; the
+// even CTA issues the MMAs and the scale copies for both (paired tcgen05.cp,
+// each CTA's scales from its own shared memory), the MMAs read A and B from
+// both CTAs' shared memory, commits arrive in both CTAs, and a thread of the
+// odd CTA relays its stages' arrival to the even one.
 // Rows and columns past m, n and k are zero-filled by the tensor-map copies
 // (zero codes contribute nothing whatever their scales); scale tiles past the
 // end of a scale tensor are not read (their lanes hold stale scales that
@@ -43,7 +50,7 @@
 // fewer slots than shared-memory stages so that the loads run a stage
 // further ahead) holding the A scales (four columns per k-step), the B
 // scales (BN / 32 columns per k-step) and A (eight columns of packed codes
-// per k-step).  Scales follow the tile layout: line L of a
+// per k-step; a pair's MMAs read A from shared memory instead).  Scales follow the tile layout: line L of a
 // 512-byte tile holds rows L, L + 32, L + 64, L + 96, and lane L of every
 // quarter holds line L, so column c of lane L holds the four scales of row
 // L + 32 c for the k-step.
@@ -64,12 +71,11 @@
 namespace tfp4 {
 namespace {
 
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBK = 256;            // k elements per stage (128 bytes of codes a row)
 constexpr uint32_t kSfTile = 512;        // bytes of one scale tile: 128 rows x 64 k
 constexpr uint32_t kStepsPerStage = 4;   // 64-element MMA k-steps per stage
-constexpr uint32_t kBoxBytes = 4096;     // one output box: 32 rows x 128 bytes
 
 // PAIR: one tile of 256 x BN on an SM pair (tcgen05 cta_group::2): each CTA
 // holds 128 rows of A and of the accumulator and BN / 2 rows of B.
@@ -97,12 +103,9 @@ struct GemmShape {
   static constexpr uint32_t kSfbBase = kSfaBase + kSlots * kStepsPerStage * kSfaCols;
   static constexpr uint32_t kABase = kSfbBase + kSlots * kStepsPerStage * kSfbCols;
   static constexpr uint32_t kColsUsed = kABase + kSlots * kStepsPerStage * kACols;
-  // epilogue staging per warp: 32 rows of BN fp32 values at most
-  static constexpr uint32_t kEpiWarpBytes = (uint32_t)BN * 32 * 4;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(kColsUsed + 8 <= kTmemCols, "tensor-memory columns");
-  static_assert(4 * kEpiWarpBytes <= kStages * kStageBytes, "epilogue staging fits the stages");
   static_assert(kSlots <= kStages, "a slot is refilled only after its stage's MMAs");
 };
 
@@ -373,25 +376,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 
-__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t e) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
-               "r"(e)
-               : "memory");
-}
-
-// One box (32 rows x 128 bytes, 128-byte swizzle) from shared to global memory.
-__device__ __forceinline__ void tensor_store_2d(const CUtensorMap* map, uint32_t src, uint32_t c0,
-                                                uint32_t c1) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(src)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_store_commit_and_drain() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled box.
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
@@ -405,33 +389,56 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 // ---- the kernel ---------------------------------------------------------------
 
+// Bounded wait on a barrier that CTAs of the cluster may also release.
+template <bool PAIR>
+__device__ __forceinline__ bool wait_any(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                         uint32_t* err) {
+  if constexpr (PAIR)
+    return mbar_wait_cluster(bar, parity, limit_ns, err);
+  else
+    return mbar_wait(bar, parity, limit_ns, err);
+}
+
+// Arrive on `bar` of the even CTA (this CTA unless it is a pair's odd CTA).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_even(uint64_t* bar, uint32_t rank) {
+  if (PAIR && rank != 0)
+    mbar_arrive_remote(peer_addr(bar, 0));
+  else
+    mbar_arrive(bar);
+}
+
+// Persistent: each CTA (each pair) takes output tiles u, u + units, ... with
+// u its index; tile t covers rows (t / tiles_n) * TM and columns
+// (t % tiles_n) * BN.  The rings of stages and slots run on across tiles
+// (g counts k-blocks over all of the CTA's tiles).
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_nvfp4_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 const __grid_constant__ CUtensorMap map_d, const uint8_t* __restrict__ sfa,
-                 const uint8_t* __restrict__ sfb, const float* __restrict__ gs_a,
-                 const float* __restrict__ gs_b, uint32_t m, uint32_t n, uint32_t k,
-                 void* __restrict__ d, uint32_t d_bf16, uint32_t tma_out,
+                 const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
+                 const float* __restrict__ gs_a, const float* __restrict__ gs_b, uint32_t m,
+                 uint32_t n, uint32_t k, void* __restrict__ d, uint32_t d_bf16,
                  uint32_t* __restrict__ err, uint64_t wait_ns) {
   using S = GemmShape<BN, PAIR>;
+  constexpr uint32_t TM = PAIR ? 256u : 128u;
   extern __shared__ uint8_t smem_raw[];
   // full: a stage's copies landed; empty: its MMAs completed (its shared
   // memory and its tensor-memory slot are free again); staged: a slot holds
-  // its stage's A and scales; acc_full: the last MMA completed
-  // (pair: staged, in the even CTA, is the odd CTA's stage landing; empty
-  // and acc_full arrive in both CTAs; drain: this CTA's MMAs retired)
+  // its stage's A and scales (pair: the odd CTA's stage landed); acc_full:
+  // a tile's last MMA completed; acc_free: the epilogue read the
+  // accumulator (pair: in both CTAs); drain: this CTA's MMAs retired
   __shared__ __align__(8) uint64_t full[S::kStages], empty[S::kStages], staged[S::kSlots],
-      acc_full, drain;
+      acc_full, acc_free, drain;
   __shared__ uint32_t tmem_base;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
-  // this CTA's A and accumulator rows, the tile's columns, this CTA's B rows
-  const uint32_t m0 = blockIdx.y * (PAIR ? 256u : 128u) + 128u * rank;
-  const uint32_t n0 = (PAIR ? blockIdx.x >> 1 : blockIdx.x) * (uint32_t)BN;
-  const uint32_t nb0 = n0 + S::kBRows * rank;
+  const uint32_t unit = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+  const uint32_t units = PAIR ? gridDim.x >> 1 : gridDim.x;
+  const uint32_t tiles_n = (n + BN - 1) / BN;
+  const uint32_t ntiles = ((m + TM - 1) / TM) * tiles_n;
   const uint32_t nkb = (k + kBK - 1) / kBK;
   const uint32_t tiles_per_row = (k + 63) / 64;  // scale tiles along k (64 elements each)
 
@@ -442,6 +449,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (uint32_t t = 0; t < S::kSlots; ++t) mbar_init(&staged[t], PAIR ? 1 : 4);
     mbar_init(&acc_full, 1);
+    mbar_init(&acc_free, PAIR ? 8 : 4);
     mbar_init(&drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -457,246 +465,250 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---- producer ----
-    const uint32_t band_a = m0 / 128u, band_b0 = n0 / 128u;
-    const uint32_t na = band_a < (m + 127u) / 128u ? 1u : 0u;  // (a pair's odd CTA may lie past m)
-    const uint32_t bands_b = (n + 127u) / 128u;
-    uint32_t kb = 0;
-    for (; kb < nkb; ++kb) {
-      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      if (!mbar_wait(&empty[s], ph ^ 1u, wait_ns, err)) break;
-      uint8_t* st = smem + s * S::kStageBytes;
-      const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
+    const uint32_t bands_a = (m + 127u) / 128u, bands_b = (n + 127u) / 128u;
+    uint32_t g = 0;
+    bool ok = true;
+    for (uint32_t tile = unit; tile < ntiles && ok; tile += units) {
+      // this CTA's A rows, the tile's columns, this CTA's B rows
+      const uint32_t m0 = (tile / tiles_n) * TM + 128u * rank, n0 = (tile % tiles_n) * BN;
+      const uint32_t nb0 = n0 + S::kBRows * rank;
+      const uint32_t band_a = m0 / 128u, band_b0 = n0 / 128u;
+      const uint32_t na = band_a < bands_a ? 1u : 0u;  // (a pair's odd CTA may lie past m)
       uint32_t nb = 0;
       for (uint32_t b = 0; b < S::kBands; ++b) nb += band_b0 + b < bands_b ? 1u : 0u;
-      mbar_expect_tx(&full[s], S::kABytes + S::kBBytes + (na + nb) * steps * kSfTile);
-      tensor_load_2d(st, &map_a, kb * (kBK / 2), m0, &full[s]);
-      tensor_load_2d(st + S::kABytes, &map_b, kb * (kBK / 2), nb0, &full[s]);
-      const uint64_t tile0 = kStepsPerStage * kb;
-      if (na)
-        bulk_load(st + S::kABytes + S::kBBytes,
-                  sfa + ((uint64_t)band_a * tiles_per_row + tile0) * kSfTile, steps * kSfTile,
-                  &full[s]);
-      for (uint32_t b = 0; b < nb; ++b)
-        bulk_load(st + S::kABytes + S::kBBytes + S::kSfaBytes + b * kStepsPerStage * kSfTile,
-                  sfb + ((uint64_t)(band_b0 + b) * tiles_per_row + tile0) * kSfTile,
-                  steps * kSfTile, &full[s]);
+      for (uint32_t kb = 0; kb < nkb; ++kb, ++g) {
+        const uint32_t s = g % S::kStages, ph = (g / S::kStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, wait_ns, err)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * S::kStageBytes;
+        const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
+        mbar_expect_tx(&full[s], S::kABytes + S::kBBytes + (na + nb) * steps * kSfTile);
+        tensor_load_2d(st, &map_a, kb * (kBK / 2), m0, &full[s]);
+        tensor_load_2d(st + S::kABytes, &map_b, kb * (kBK / 2), nb0, &full[s]);
+        const uint64_t tile0 = kStepsPerStage * kb;
+        if (na)
+          bulk_load(st + S::kABytes + S::kBBytes,
+                    sfa + ((uint64_t)band_a * tiles_per_row + tile0) * kSfTile, steps * kSfTile,
+                    &full[s]);
+        for (uint32_t b = 0; b < nb; ++b)
+          bulk_load(st + S::kABytes + S::kBBytes + S::kSfaBytes + b * kStepsPerStage * kSfTile,
+                    sfb + ((uint64_t)(band_b0 + b) * tiles_per_row + tile0) * kSfTile,
+                    steps * kSfTile, &full[s]);
+      }
     }
     // the copies still in flight complete before the CTA may exit
-    const uint32_t first = kb > S::kStages ? kb - S::kStages : 0u;
-    for (uint32_t j = first; j < kb; ++j)
+    for (uint32_t j = g > S::kStages ? g - S::kStages : 0u; j < g; ++j)
       mbar_wait(&full[j % S::kStages], (j / S::kStages) & 1u, wait_ns, err);
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---- MMAs (for a pair: the even CTA, for both) ----
-    constexpr uint32_t idesc = mma_idesc(PAIR ? 256 : 128, BN);
+    constexpr uint32_t idesc = mma_idesc(TM, BN);
+    uint32_t g = 0, it = 0;
     bool ok = true;
-    for (uint32_t kb = 0; kb < nkb; ++kb) {
-      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      const uint32_t t = kb % S::kSlots, pt = (kb / S::kSlots) & 1u;
-      const bool staged_ok = PAIR ? mbar_wait_cluster(&staged[t], pt, wait_ns, err)
-                                  : mbar_wait(&staged[t], pt, wait_ns, err);
-      if (!staged_ok || !mbar_wait(&full[s], ph, wait_ns, err)) {
+    for (uint32_t tile = unit; tile < ntiles && ok; tile += units, ++it) {
+      // the epilogue has read the previous tile's accumulator
+      if (it > 0 && !wait_any<PAIR>(&acc_free, (it - 1) & 1u, wait_ns, err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t a_smem = smem_addr(smem + s * S::kStageBytes);
-      const uint32_t b_smem = a_smem + S::kABytes;
-      const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
-      const uint32_t step0 = t * kStepsPerStage;
-      if constexpr (PAIR) {
-        // scales of both CTAs, each from its own shared memory (paired copies)
-        const uint32_t sf_a = b_smem + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
-        for (uint32_t j = 0; j < steps; ++j) {
-          tmem_copy_scales<true>(tmem + S::kSfaBase + (step0 + j) * S::kSfaCols,
-                                 sf_a + j * kSfTile);
-          for (uint32_t b = 0; b < S::kBands; ++b)
-            tmem_copy_scales<true>(tmem + S::kSfbBase + (step0 + j) * S::kSfbCols + 4u * b,
-                                   sf_b + (b * kStepsPerStage + j) * kSfTile);
+      for (uint32_t kb = 0; kb < nkb; ++kb, ++g) {
+        const uint32_t s = g % S::kStages, ph = (g / S::kStages) & 1u;
+        const uint32_t t = g % S::kSlots, pt = (g / S::kSlots) & 1u;
+        if (!wait_any<PAIR>(&staged[t], pt, wait_ns, err) ||
+            !mbar_wait(&full[s], ph, wait_ns, err)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const uint32_t a_smem = smem_addr(smem + s * S::kStageBytes);
+        const uint32_t b_smem = a_smem + S::kABytes;
+        const uint32_t steps = min(kStepsPerStage, tiles_per_row - kStepsPerStage * kb);
+        const uint32_t step0 = t * kStepsPerStage;
+        if constexpr (PAIR) {
+          // scales of both CTAs, each from its own shared memory (paired copies)
+          const uint32_t sf_a = b_smem + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
+          for (uint32_t j = 0; j < steps; ++j) {
+            tmem_copy_scales<true>(tmem + S::kSfaBase + (step0 + j) * S::kSfaCols,
+                                   sf_a + j * kSfTile);
+            for (uint32_t b = 0; b < S::kBands; ++b)
+              tmem_copy_scales<true>(tmem + S::kSfbBase + (step0 + j) * S::kSfbCols + 4u * b,
+                                     sf_b + (b * kStepsPerStage + j) * kSfTile);
+          }
+        }
+        for (uint32_t j = 0; j < steps; ++j) {
+          // k-step j sits 32 bytes further along each 128-byte row of A and B
+          const uint32_t sfa_t = tmem + S::kSfaBase + (step0 + j) * S::kSfaCols;
+          const uint32_t sfb_t = tmem + S::kSfbBase + (step0 + j) * S::kSfbCols;
+          const uint32_t acc = (kb | j) != 0u ? 1u : 0u;
+          if constexpr (S::kATmem)
+            mma_nvf4<PAIR>(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
+                           operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
+          else
+            mma_nvf4_ss<PAIR>(tmem, operand_desc(a_smem + 32u * j),
+                              operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
+        }
+        tc_commit<PAIR>(&empty[s]);
       }
-      for (uint32_t j = 0; j < steps; ++j) {
-        // k-step j sits 32 bytes further along each 128-byte row of A and B
-        const uint32_t sfa_t = tmem + S::kSfaBase + (step0 + j) * S::kSfaCols;
-        const uint32_t sfb_t = tmem + S::kSfbBase + (step0 + j) * S::kSfbCols;
-        const uint32_t acc = (kb | j) != 0u ? 1u : 0u;
-        if constexpr (S::kATmem)
-          mma_nvf4<PAIR>(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
-                         operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
-        else
-          mma_nvf4_ss<PAIR>(tmem, operand_desc(a_smem + 32u * j), operand_desc(b_smem + 32u * j),
-                            idesc, sfa_t, sfb_t, acc);
-      }
-      tc_commit<PAIR>(&empty[s]);
+      if (ok) tc_commit<PAIR>(&acc_full);
     }
-    if (ok) tc_commit<PAIR>(&acc_full);
     // every MMA issued here has retired before the columns are freed
     tc_commit_local<PAIR>(&drain);
     mbar_wait(&drain, 0, wait_ns, err);
   } else if (PAIR && warp == 1 && lane == 0) {
     // ---- the odd CTA's relay: its stage landed -> the even CTA's staged ----
     const uint32_t remote = peer_addr(&staged[0], 0);
-    for (uint32_t kb = 0; kb < nkb; ++kb) {
-      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      if (!mbar_wait(&full[s], ph, wait_ns, err)) break;
-      mbar_arrive_remote(remote + (kb % S::kSlots) * (uint32_t)sizeof(uint64_t));
-    }
-  } else if (warp >= 2) {
+    uint32_t g = 0;
+    bool ok = true;
+    for (uint32_t tile = unit; tile < ntiles && ok; tile += units)
+      for (uint32_t kb = 0; kb < nkb; ++kb, ++g) {
+        if (!mbar_wait(&full[g % S::kStages], (g / S::kStages) & 1u, wait_ns, err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_remote(remote + (g % S::kSlots) * (uint32_t)sizeof(uint64_t));
+      }
+  } else if (!PAIR && warp >= 2 && warp < 6) {
     // ---- stagers: warp w owns lane quarter q = w mod 4 (tile rows 32 q ..) ----
     const uint32_t q = warp & 3u;
     const uint32_t row = 32u * q + lane;                 // row inside the tile
     const uint32_t lane_base = tmem + ((32u * q) << 16);
+    uint32_t g = 0;
     bool ok = true;
-    // (a pair's scales are copied by the MMA thread: no staging)
-    const uint32_t nstage = PAIR ? 0u : nkb;
-    for (uint32_t kb = 0; kb != nstage && ok; ++kb) {
-      const uint32_t s = kb % S::kStages, ph = (kb / S::kStages) & 1u;
-      const uint32_t t = kb % S::kSlots;
-      // slot t last held k-block kb - kSlots: its MMAs completed once that
-      // k-block's stage was released
-      const uint32_t prev = kb - S::kSlots;
-      if (!mbar_wait(&full[s], ph, wait_ns, err) ||
-          (S::kSlots < S::kStages && kb >= S::kSlots &&
-           !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u, wait_ns, err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t st = smem_addr(smem + s * S::kStageBytes);
-      const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
-      const uint32_t step0 = t * kStepsPerStage;
-      if constexpr (S::kATmem) {
-        // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
-        uint32_t w[32];
-#pragma unroll
-        for (uint32_t c = 0; c < 8; ++c) {
-          const uint4 v = lds128(st + swz128(row, c));
-          w[4 * c] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
+    for (uint32_t tile = unit; tile < ntiles && ok; tile += units)
+      for (uint32_t kb = 0; kb < nkb; ++kb, ++g) {
+        const uint32_t s = g % S::kStages, ph = (g / S::kStages) & 1u;
+        const uint32_t t = g % S::kSlots;
+        // slot t last held k-block g - kSlots: its MMAs completed once that
+        // k-block's stage was released
+        const uint32_t prev = g - S::kSlots;
+        if (!mbar_wait(&full[s], ph, wait_ns, err) ||
+            (S::kSlots < S::kStages && g >= S::kSlots &&
+             !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u, wait_ns, err))) {
+          ok = false;
+          break;
         }
-        tmem_store32(lane_base + S::kABase + step0 * S::kACols, w);
-      }
-      {
-        // A scales: line `lane` of each k-step's tile
-        uint32_t w[16];
+        tc_fence_after();
+        const uint32_t st = smem_addr(smem + s * S::kStageBytes);
+        const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
+        const uint32_t step0 = t * kStepsPerStage;
+        {
+          // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
+          uint32_t w[32];
 #pragma unroll
-        for (uint32_t j = 0; j < 4; ++j) {
-          const uint4 v = lds128(sf_a + j * kSfTile + lane * 16u);
-          w[4 * j] = v.x;
-          w[4 * j + 1] = v.y;
-          w[4 * j + 2] = v.z;
-          w[4 * j + 3] = v.w;
-        }
-        tmem_store16(lane_base + S::kSfaBase + step0 * S::kSfaCols, w);
-      }
-      if constexpr (S::kBands == 2) {
-        // B scales, k-step j: band 0 then band 1
-        uint32_t w[32];
-#pragma unroll
-        for (uint32_t j = 0; j < 4; ++j)
-#pragma unroll
-          for (uint32_t b = 0; b < 2; ++b) {
-            const uint4 v = lds128(sf_b + (b * kStepsPerStage + j) * kSfTile + lane * 16u);
-            w[8 * j + 4 * b] = v.x;
-            w[8 * j + 4 * b + 1] = v.y;
-            w[8 * j + 4 * b + 2] = v.z;
-            w[8 * j + 4 * b + 3] = v.w;
+          for (uint32_t c = 0; c < 8; ++c) {
+            const uint4 v = lds128(st + swz128(row, c));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
           }
-        tmem_store32(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
-      } else {
-        uint32_t w[16];
-#pragma unroll
-        for (uint32_t j = 0; j < 4; ++j) {
-          const uint4 v = lds128(sf_b + j * kSfTile + lane * 16u);
-          w[4 * j] = v.x;
-          w[4 * j + 1] = v.y;
-          w[4 * j + 2] = v.z;
-          w[4 * j + 3] = v.w;
+          tmem_store32(lane_base + S::kABase + step0 * S::kACols, w);
         }
-        tmem_store16(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
+        {
+          // A scales: line `lane` of each k-step's tile
+          uint32_t w[16];
+#pragma unroll
+          for (uint32_t j = 0; j < 4; ++j) {
+            const uint4 v = lds128(sf_a + j * kSfTile + lane * 16u);
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+          }
+          tmem_store16(lane_base + S::kSfaBase + step0 * S::kSfaCols, w);
+        }
+        if constexpr (S::kBands == 2) {
+          // B scales, k-step j: band 0 then band 1
+          uint32_t w[32];
+#pragma unroll
+          for (uint32_t j = 0; j < 4; ++j)
+#pragma unroll
+            for (uint32_t b = 0; b < 2; ++b) {
+              const uint4 v = lds128(sf_b + (b * kStepsPerStage + j) * kSfTile + lane * 16u);
+              w[8 * j + 4 * b] = v.x;
+              w[8 * j + 4 * b + 1] = v.y;
+              w[8 * j + 4 * b + 2] = v.z;
+              w[8 * j + 4 * b + 3] = v.w;
+            }
+          tmem_store32(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (uint32_t j = 0; j < 4; ++j) {
+            const uint4 v = lds128(sf_b + j * kSfTile + lane * 16u);
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+          }
+          tmem_store16(lane_base + S::kSfbBase + step0 * S::kSfbCols, w);
+        }
+        tmem_store_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&staged[t]);
       }
-      tmem_store_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR && rank != 0)
-          mbar_arrive_remote(peer_addr(&staged[t], 0));
-        else
-          mbar_arrive(&staged[t]);
-      }
-    }
-    // ---- epilogue ----
-    if (ok) ok = mbar_wait(&acc_full, 0, wait_ns, err);
-    tc_fence_after();
-    if (ok) {
-      const float alpha = __fmul_rn(gs_a[0], gs_b[0]);
-      if (tma_out) {
-        // stage the warp's 32 rows in 128-byte-swizzled boxes, then store
-        const uint32_t stg = smem_addr(smem) + q * S::kEpiWarpBytes;
-        for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
-          uint32_t v[32];
-          tmem_load32(lane_base + c, v);
-          if (d_bf16) {
-            const uint32_t box = stg + (c / 64) * kBoxBytes, c0 = (c % 64) / 8;
+  } else if (warp >= 6) {
+    // ---- epilogue: warp w reads lane quarter q = w mod 4 ----
+    const uint32_t q = warp & 3u;
+    const uint32_t lane_base = tmem + ((32u * q) << 16);
+    const float alpha = __fmul_rn(gs_a[0], gs_b[0]);
+    const bool vec = d_bf16 ? (n & 7u) == 0 : (n & 3u) == 0;  // 16-byte row pieces aligned
+    uint32_t it = 0;
+    for (uint32_t tile = unit; tile < ntiles; tile += units, ++it) {
+      if (!mbar_wait(&acc_full, it & 1u, wait_ns, err)) break;
+      tc_fence_after();
+      const uint32_t grow = (tile / tiles_n) * TM + 128u * rank + 32u * q + lane;
+      const uint32_t n0 = (tile % tiles_n) * BN;
+      for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
+        uint32_t v[32];
+        tmem_load32(lane_base + c, v);
+        if (c + 32 == (uint32_t)BN) {
+          // the accumulator is read: the next tile's MMAs may start
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_even<PAIR>(&acc_free, rank);
+        }
+        const uint32_t col = n0 + c;
+        if (grow >= m || col >= n) continue;
+        const uint32_t cnt = min(32u, n - col);
+        if (d_bf16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(d) + (uint64_t)grow * n + col;
+          if (vec && cnt == 32) {
 #pragma unroll
             for (uint32_t i = 0; i < 4; ++i) {
               const uint32_t* u = v + 8 * i;
-              sts128(box + swz128(lane, c0 + i),
-                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[0])),
-                            __fmul_rn(alpha, __uint_as_float(u[1]))),
-                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[2])),
-                            __fmul_rn(alpha, __uint_as_float(u[3]))),
-                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[4])),
-                            __fmul_rn(alpha, __uint_as_float(u[5]))),
-                     bf16x2(__fmul_rn(alpha, __uint_as_float(u[6])),
-                            __fmul_rn(alpha, __uint_as_float(u[7]))));
+              reinterpret_cast<uint4*>(out)[i] =
+                  make_uint4(bf16x2(__fmul_rn(alpha, __uint_as_float(u[0])),
+                                    __fmul_rn(alpha, __uint_as_float(u[1]))),
+                             bf16x2(__fmul_rn(alpha, __uint_as_float(u[2])),
+                                    __fmul_rn(alpha, __uint_as_float(u[3]))),
+                             bf16x2(__fmul_rn(alpha, __uint_as_float(u[4])),
+                                    __fmul_rn(alpha, __uint_as_float(u[5]))),
+                             bf16x2(__fmul_rn(alpha, __uint_as_float(u[6])),
+                                    __fmul_rn(alpha, __uint_as_float(u[7]))));
             }
           } else {
-            const uint32_t box = stg + (c / 32) * kBoxBytes;
 #pragma unroll
-            for (uint32_t i = 0; i < 8; ++i) {
-              const uint32_t* u = v + 4 * i;
-              sts128(box + swz128(lane, i),
-                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[0]))),
-                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[1]))),
-                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[2]))),
-                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(u[3]))));
-            }
+            for (uint32_t i = 0; i < 32; ++i)
+              if (i < cnt) out[i] = __float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(v[i])));
           }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t cols_per_box = d_bf16 ? 64u : 32u;
-          const uint32_t y = m0 + 32u * q;
-          if (y < m)
-            for (uint32_t b = 0; b < (uint32_t)BN / cols_per_box; ++b) {
-              const uint32_t x = n0 + b * cols_per_box;
-              if (x < n) tensor_store_2d(&map_d, stg + b * kBoxBytes, x, y);
-            }
-          bulk_store_commit_and_drain();
-        }
-        __syncwarp();
-      } else {
-        // element stores (rows whose pitch is not a multiple of 16 bytes)
-        const uint32_t grow = m0 + row;
-        for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
-          uint32_t v[32];
-          tmem_load32(lane_base + c, v);
-          const uint32_t col = n0 + c;
-          if (grow >= m || col >= n) continue;
-          const uint32_t cnt = min(32u, n - col);
+        } else {
+          float* out = static_cast<float*>(d) + (uint64_t)grow * n + col;
+          if (vec && cnt == 32) {
 #pragma unroll
-          for (uint32_t i = 0; i < 32; ++i) {
-            if (i < cnt) {
-              const float y = __fmul_rn(alpha, __uint_as_float(v[i]));
-              if (d_bf16)
-                static_cast<__nv_bfloat16*>(d)[(uint64_t)grow * n + col + i] =
-                    __float2bfloat16_rn(y);
-              else
-                static_cast<float*>(d)[(uint64_t)grow * n + col + i] = y;
-            }
+            for (uint32_t i = 0; i < 8; ++i)
+              reinterpret_cast<float4*>(out)[i] =
+                  make_float4(__fmul_rn(alpha, __uint_as_float(v[4 * i])),
+                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 1])),
+                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 2])),
+                              __fmul_rn(alpha, __uint_as_float(v[4 * i + 3])));
+          } else {
+#pragma unroll
+            for (uint32_t i = 0; i < 32; ++i)
+              if (i < cnt) out[i] = __fmul_rn(alpha, __uint_as_float(v[i]));
           }
         }
       }
@@ -723,28 +735,11 @@ bool encode_operand_map(const void* codes, int64_t rows, int64_t k, uint32_t box
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// d [m, n] in boxes of 32 rows x 128 bytes, 128-byte swizzle (stores past m
-// or n are dropped); false when a row is not a multiple of 16 bytes.
-bool encode_output_map(void* d, int64_t m, int64_t n, int d_bf16, CUtensorMap* map) {
-  const int64_t esize = d_bf16 ? 2 : 4;
-  if ((n * esize) % 16 != 0) return false;
-  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dim[2] = {(cuuint64_t)n, (cuuint64_t)m};
-  const cuuint64_t stride[1] = {(cuuint64_t)(n * esize)};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), 32};
-  const cuuint32_t estride[2] = {1, 1};
-  return enc(map, d_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-             d, dim, stride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN, bool PAIR>
 cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                       const void* b_codes, const void* b_sf, const float* b_gs, int64_t m,
                       int64_t n, int64_t k, void* d, int d_bf16, uint32_t* err, uint64_t wait_ns,
-                      cudaStream_t st) {
+                      int sm_count, cudaStream_t st) {
   using S = GemmShape<BN, PAIR>;
   static std::mutex mu;
   static bool set_for[64];
@@ -761,15 +756,18 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
       set_for[dev] = true;
     }
   }
-  CUtensorMap ma, mb, md;
+  CUtensorMap ma, mb;
   if (!encode_operand_map(a_codes, m, k, 128, &ma) ||
       !encode_operand_map(b_codes, n, k, S::kBRows, &mb))
     return cudaErrorInvalidValue;
-  const bool tma_out = encode_output_map(d, m, n, d_bf16, &md);
-  if (!tma_out) std::memset(&md, 0, sizeof(md));
+  // one CTA per SM (pair: per two SMs), each taking tiles in turn
   const int64_t tm = PAIR ? 256 : 128;
+  const int64_t ntiles = (m + tm - 1) / tm * ((n + BN - 1) / BN);
+  int64_t units = PAIR ? sm_count / 2 : sm_count;
+  if (units > ntiles) units = ntiles;
+  if (units < 1) units = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((n + BN - 1) / BN * (PAIR ? 2 : 1)), (unsigned)((m + tm - 1) / tm));
+  cfg.gridDim = dim3((unsigned)(units * (PAIR ? 2 : 1)));
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = st;
@@ -780,9 +778,9 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_nvfp4_gemm<BN, PAIR>, ma, mb, md, (const uint8_t*)a_sf,
+  return cudaLaunchKernelEx(&cfg, k_nvfp4_gemm<BN, PAIR>, ma, mb, (const uint8_t*)a_sf,
                             (const uint8_t*)b_sf, a_gs, b_gs, (uint32_t)m, (uint32_t)n,
-                            (uint32_t)k, d, d_bf16 ? 1u : 0u, tma_out ? 1u : 0u, err, wait_ns);
+                            (uint32_t)k, d, d_bf16 ? 1u : 0u, err, wait_ns);
 }
 
 }  // namespace
@@ -790,18 +788,19 @@ cudaError_t launch_tc(const void* a_codes, const void* a_sf, const float* a_gs,
 cudaError_t launch_nvfp4_gemm_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                                  const void* b_codes, const void* b_sf, const float* b_gs,
                                  int64_t m, int64_t n, int64_t k, void* d, int d_bf16,
-                                 int tile, uint32_t* err, uint64_t wait_ns, cudaStream_t st) {
-  if (m <= 0 || n <= 0 || k <= 0 || k % 32 || m > 65535LL * 128 || m > UINT32_MAX ||
-      n > UINT32_MAX || k > UINT32_MAX)
+                                 int tile, uint32_t* err, uint64_t wait_ns, int sm_count,
+                                 cudaStream_t st) {
+  if (m <= 0 || n <= 0 || k <= 0 || k % 32 || m > UINT32_MAX || n > UINT32_MAX ||
+      k > UINT32_MAX)
     return cudaErrorInvalidValue;
   if (tile == kGemmTilePair)
     return launch_tc<256, true>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d, d_bf16,
-                                err, wait_ns, st);
+                                err, wait_ns, sm_count, st);
   return tile == kGemmTile128
              ? launch_tc<128, false>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d,
-                                     d_bf16, err, wait_ns, st)
+                                     d_bf16, err, wait_ns, sm_count, st)
              : launch_tc<256, false>(a_codes, a_sf, a_gs, b_codes, b_sf, b_gs, m, n, k, d,
-                                     d_bf16, err, wait_ns, st);
+                                     d_bf16, err, wait_ns, sm_count, st);
 }
 
 }  // namespace tfp4

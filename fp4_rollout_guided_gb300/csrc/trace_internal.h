@@ -156,7 +156,8 @@ enum { kGemmTile256 = 0, kGemmTile128 = 1, kGemmTilePair = 2 };
 cudaError_t launch_nvfp4_gemm_tc(const void* a_codes, const void* a_sf, const float* a_gs,
                                  const void* b_codes, const void* b_sf, const float* b_gs,
                                  int64_t m, int64_t n, int64_t k, void* d, int d_bf16,
-                                 int tile, uint32_t* err, uint64_t wait_ns, cudaStream_t st);
+                                 int tile, uint32_t* err, uint64_t wait_ns, int sm_count,
+                                 cudaStream_t st);
 // The driver's tensor-map encoder (null if the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool lt_available();
