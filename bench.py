@@ -817,15 +817,29 @@ def run_gemm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    h.profile(True)
-    for _ in range(args.steps):
-        step()
-    t = h.collect()
-    h.profile(False)
-    torch.cuda.synchronize()
+    def gemm_time():
+        h.profile(True)
+        for _ in range(args.steps):
+            step()
+        t = h.collect()
+        h.profile(False)
+        torch.cuda.synchronize()
+        g_n, g_ms = t["nvfp4_gemm"]
+        return g_ms / max(g_n, 1), t
+
+    gemm_ms, t = gemm_time()
     flops = 2.0 * M * N * K
-    g_n, g_ms = t["nvfp4_gemm"]
-    gemm_ms = g_ms / max(g_n, 1)
+    # the library GEMM on the same operands, for comparison (not the metric)
+    lt_ms = None
+    if args.gemm_form != "cublaslt":
+        h.set_option("gemm", "cublaslt")
+        try:
+            for _ in range(args.warmup):
+                step()
+            lt_ms = round(gemm_time()[0], 4)
+        except RuntimeError:
+            lt_ms = None
+        h.set_option("gemm", args.gemm_form)
     peak, src = load_peaks()
     bf16_peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] \
         if src == "measured" else 1900.0
@@ -839,6 +853,10 @@ def run_gemm(args):
             "config": {"workload": f"Y[{M},{N}] = X[{M},{K}] W[{N},{K}]^T, X quantised each step",
                        "out": "bf16", "gemm": args.gemm_form},
             "gemm_ms": round(gemm_ms, 4), "quantise_ms": quant,
+            "cublaslt_gemm_ms": lt_ms,
+            # our kernels per step: the rollout quantiser (amax, quantisation)
+            # and the GEMM kernel, or with cuBLASLt its alpha kernel instead
+            "gpu_launches_per_step": 3,
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1),
                          "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                          "frac": round(tflops / fp4_peak, 4),

@@ -49,7 +49,7 @@ struct trace_ctx {
   const void* scratch_base = nullptr;  // the one scratch allocation
   size_t scratch_bytes = 0;
   bool dbg_shrink = false;  // debug builds: register outputs 16 bytes short
-  int gemm = TRACE_GEMM_CUBLASLT;  // form of trace_nvfp4_gemm
+  int gemm = TRACE_GEMM_TC256;  // form of trace_nvfp4_gemm
 };
 
 namespace {

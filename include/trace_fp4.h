@@ -183,9 +183,9 @@ typedef enum {
                                   short, so the kernels' last stores into it
                                   are counted as out of range and skipped.
                                   Other builds return TRACE_ERR_INVALID_ARG. */
-  TRACE_OPT_GEMM = 5           /* form of trace_nvfp4_gemm: TRACE_GEMM_CUBLASLT
-                                  (default), TRACE_GEMM_TC256, TRACE_GEMM_TC128
-                                  or TRACE_GEMM_TC_PAIR                       */
+  TRACE_OPT_GEMM = 5           /* form of trace_nvfp4_gemm: TRACE_GEMM_TC256
+                                  (default), TRACE_GEMM_TC128,
+                                  TRACE_GEMM_TC_PAIR or TRACE_GEMM_CUBLASLT   */
 } trace_option_t;
 
 /* Values of TRACE_OPT_GEMM. */
@@ -383,11 +383,15 @@ typedef enum { TRACE_OUT_F32 = 0, TRACE_OUT_BF16 = 1 } trace_out_t;
  *   fl32(a_gs[0] * b_gs[0]) * sum_k A[i, k] * B[j, k],
  * A [m, k] and B [n, k] given as codes ([rows, k/2], element 2i in the low
  * nibble) and block scales in the tile layout, a_gs / b_gs device pointers
- * to one global scale each (a single segment per operand).  The
- * contraction is cuBLASLt's block-scaled E2M1 GEMM with FP32 accumulation,
- * loaded at the first call; a handle keeps its cuBLASLt handle and a
- * 32 MiB workspace (allocated at that call).  k must be a multiple of 32.
- * Returns TRACE_ERR_LIBRARY if cuBLASLt is missing or refuses the shape. */
+ * to one global scale each (a single segment per operand).  Block-scaled
+ * E2M1 products with FP32 accumulation on the tensor cores, in the form
+ * TRACE_OPT_GEMM selects: the library's own tcgen05 kernel (default; no
+ * allocation, a wait inside it that runs out is reported by
+ * trace_device_status) or cuBLASLt (loaded at the first such call; the
+ * handle then keeps its cuBLASLt handle and a 32 MiB workspace).  k must be
+ * a multiple of 32; d, the codes and the tile-layout scales 16-byte
+ * aligned.  The cuBLASLt form returns TRACE_ERR_LIBRARY if cuBLASLt is
+ * missing or refuses the shape. */
 TRACE_API trace_status_t trace_nvfp4_gemm(trace_handle_t h, const void* a_codes,
                                           const void* a_scales_mma, const float* a_gs,
                                           const void* b_codes, const void* b_scales_mma,

@@ -716,8 +716,9 @@ def test_fused_equals_split_full_size(h, cfg):
 
 # ---------------------------------------------------------------------------
 # f4: block scales in the tensor-core tile layout, NVFP4 GEMM over rollout
-# codes (cuBLASLt); a wrong tile layout would put wrong scales on whole
-# 16-element blocks and miss the oracle by O(1)
+# codes (the library's tcgen05 kernel in its three tile forms, and cuBLASLt);
+# a wrong tile layout or descriptor would put wrong scales on whole
+# 16-element blocks or wrong codes in whole k-steps and miss the oracle by O(1)
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("rows,cols", [(1, 32), (130, 96), (256, 64), (300, 2048), (4097, 128)])
@@ -744,11 +745,11 @@ GEMM_RAGGED = [(1, 32, 32), (130, 200, 96), (300, 36, 320), (257, 520, 544), (64
                (128, 1, 64), (7, 264, 4128)]
 
 
-@pytest.fixture(params=["cublaslt", "tc256", "tc128", "tc_pair"])
+@pytest.fixture(params=["tc256", "tc128", "tc_pair", "cublaslt"])
 def gemm_form(h, request):
     h.set_option("gemm", request.param)
     yield request.param
-    h.set_option("gemm", "cublaslt")
+    h.set_option("gemm", "tc256")
 
 
 @pytest.mark.parametrize("m,n,k", GEMM_SHAPES + GEMM_RAGGED)
