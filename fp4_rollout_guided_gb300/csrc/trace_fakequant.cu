@@ -356,15 +356,12 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
             asm("cvt.f32.f16 %0, %1;" : "=f"(g1) : "h"((unsigned short)(h >> 16)));
             us = add2_rz(F2{g0, g1}, C);
           }
-          // us clamped to [sz, sp], on the FMA pipe: us - sz is a multiple of
-          // the grid spacing (>= 0.5) or <= 0, so h = sat(4 (us - sz)) is
-          // exactly 1 or 0, and g = glo + h (ghi - glo) is the chosen point
           // the chosen point g: us clamped to [sz, sp], minus C.  With the
-          // compact record the ALU pipe is lighter than the FMA pipe, so the
-          // clamp is two min/max; with the full record the other way round,
-          // so it is done on the FMA pipe: us - sz is a multiple of the grid
-          // spacing (>= 0.5) or <= 0, h = sat(4 (us - sz)) is exactly 1 or 0,
-          // and g = glo + h (ghi - glo).
+          // compact record the clamp is two min/max per element (measured
+          // faster than the form below); with the full record it runs on the
+          // FMA pipe: us - sz is a multiple of the grid spacing (>= 0.5) or
+          // <= 0, so h = sat(4 (us - sz)) is exactly 1 or 0, and
+          // g = glo + h (ghi - glo).
           F2 g;
           if (KIND == TRACE_GUIDE_COMPACT) {
             const F2 yc = {fminf(fmaxf(us.x, sz.x), sp.x), fminf(fmaxf(us.y, sz.y), sp.y)};

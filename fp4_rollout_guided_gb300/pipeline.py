@@ -1,7 +1,12 @@
 """Host-streamed guided-NVFP4 step: inputs and outputs in pinned host memory,
 processed in pieces of whole training segments so that the host->device copy
 of piece k+1, the kernels of piece k and the device->host copy of piece k-1
-overlap on CUDA streams (x and r come in on two, so two copy engines work).
+overlap on CUDA streams.  The host-to-device copies of x and r share one
+stream (two concurrent streams in the same direction only contend for the
+link), the device-to-host copies run on another, so both directions of the
+link work at once.  Pieces default to about a twelfth of the rows: enough to
+overlap, few enough that enqueueing a step costs the host a few
+milliseconds rather than as long as the step itself.
 
 Training segments are independent (each has its own global scale, and the
 rollout segments refine them), so running the step piece by piece gives the
@@ -66,11 +71,13 @@ class HostStreamedStep:
     enqueued; synchronise the device (or the d2h stream) before reading."""
 
     def __init__(self, h: trace.Handle, rows: int, cols: int, seg_t, seg_r,
-                 guide: str = "compact", min_piece_rows: int = 1):
+                 guide: str = "compact", min_piece_rows: Optional[int] = None):
         dev = h.device
         self.h = h
         self.guide = guide
         self.rows, self.cols = rows, cols
+        if min_piece_rows is None:
+            min_piece_rows = max(1, -(-rows // 12))
         self.pieces = plan_pieces(seg_t, seg_r, min_piece_rows)
         n_seg_r = len(seg_r) - 1
         self.x = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
@@ -84,7 +91,6 @@ class HostStreamedStep:
         self.y = torch.empty_like(self.x)
         self.mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
         self.s_in = torch.cuda.Stream(dev)
-        self.s_in2 = torch.cuda.Stream(dev)  # r's copies (a second copy engine)
         self.s_run = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
         self.done = torch.cuda.Event()
@@ -98,20 +104,15 @@ class HostStreamedStep:
         h, kind = self.h, self.guide
         # a new run's copies into x / r wait for the previous run's kernels
         self.s_in.wait_event(self.done)
-        self.s_in2.wait_event(self.done)
         for p in self.pieces:
             a, b = p.r0, p.r1
             with torch.cuda.stream(self.s_in):
-                self.x[a:b].copy_(x_h[a:b], non_blocking=True)
-                ev_x = torch.cuda.Event()
-                ev_x.record(self.s_in)
-            with torch.cuda.stream(self.s_in2):
                 self.r[a:b].copy_(r_h[a:b], non_blocking=True)
-                ev_r = torch.cuda.Event()
-                ev_r.record(self.s_in2)
+                self.x[a:b].copy_(x_h[a:b], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(self.s_in)
             with torch.cuda.stream(self.s_run):
-                self.s_run.wait_event(ev_x)
-                self.s_run.wait_event(ev_r)
+                self.s_run.wait_event(ev_in)
                 xd, rd = self.x[a:b], self.r[a:b]
                 out_r = (self.codes[a:b], self.bs[a:b], self.gs[p.s0:p.s1],
                          self.guide_words[a:b])

@@ -826,7 +826,7 @@ def test_rollout_quant_writes_tile_layout_scales(h, fused, rows, cols, seg):
 # equals the one-call step bit for bit
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("cfg,min_rows", [(2, 1), (3, 1), (3, 5000), (5, 1)])
+@pytest.mark.parametrize("cfg,min_rows", [(2, 1), (3, 1), (3, 5000), (5, 1), (5, None)])
 def test_host_streamed_step_matches_one_call(h, cfg, min_rows):
     from fp4_rollout_guided_gb300 import pipeline
     w = synth.workload(cfg, small=True)
