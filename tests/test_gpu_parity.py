@@ -782,6 +782,48 @@ def test_nvfp4_gemm_against_oracle(h, gemm_form, m, n, k):
     assert np.all(err16 <= bound + 2.0 ** -8 * np.abs(ref)), float(err16.max())
 
 
+def test_nvfp4_gemm_full_size_sampled(h):
+    """The GEMM at the size the benchmark times (16384 x 8192 x 8192, bf16 and
+    fp32 out), every hand-written form; the oracle recomputes sampled rows
+    (all 8192 columns each): the first and last rows of tiles, rows in the
+    middle of the second tile pair, and seeded random rows."""
+    m, n, k = 16384, 8192, 8192
+    g = torch.Generator(device=DEV).manual_seed(5)
+    x = (torch.randn((m, k), generator=g, device=DEV) * 2.0).to(torch.bfloat16)
+    w = (torch.randn((n, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    a, b = h.nvfp4_operand(x), h.nvfp4_operand(w)
+    rows = sorted(set([0, 127, 128, 255, 256, 383, 300, m - 129, m - 128, m - 1] +
+                      np.random.default_rng(7).integers(0, m, 14).tolist()))
+    sel = torch.tensor(rows, device=DEV)
+    # the operands of the sampled rows and all of B, then the oracle
+    a_codes = a[0].index_select(0, sel).cpu().numpy()
+    b_codes = b[0].cpu().numpy()
+    xs = x.index_select(0, sel).cpu()
+    # (the sampled rows quantised with the whole tensor's maximum)
+    o_codes, bs_a, _, _ = oracle.rollout_quant(u16(xs), None, amax=[float(x.abs().max())])
+    assert_same("A codes (sampled rows)", a_codes, o_codes)
+    wb = u16(w.cpu())
+    bc, bbs, bgs, _ = oracle.rollout_quant(wb, None)
+    assert_same("B codes", b_codes, bc)
+    gs_a = np.float32(a[2].cpu().numpy()[0])
+    ref = oracle.nvfp4_gemm(a_codes, bs_a, gs_a, bc, bbs, bgs[0])
+    mag = oracle.nvfp4_gemm(a_codes & 0x77, bs_a, gs_a, bc & 0x77, bbs, bgs[0])
+    bound = k * 2.0 ** -24 * mag + 2.0 ** -126
+    try:
+        for form in ("tc256", "tc_pair", "tc128"):
+            h.set_option("gemm", form)
+            for dt in (torch.bfloat16, torch.float32):
+                d = h.nvfp4_gemm(a, b, out_dtype=dt)
+                torch.cuda.synchronize()
+                assert h.device_status() == 0
+                got = d.index_select(0, sel).cpu().double().numpy()
+                err = np.abs(got - ref)
+                lim = bound + (2.0 ** -8 * np.abs(ref) if dt == torch.bfloat16 else 0.0)
+                assert np.all(err <= lim), (form, dt, float((err / lim).max()))
+    finally:
+        h.set_option("gemm", "tc256")
+
+
 def test_nvfp4_gemm_closed_form(h, gemm_form):
     m, n, k = 128, 128, 256
     x = torch.full((m, k), 1.5, dtype=torch.bfloat16, device=DEV)
