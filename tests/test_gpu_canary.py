@@ -158,3 +158,27 @@ def test_noalloc_entry_point_stays_inside_its_buffers():
         g.check(f"noalloc {rows}x{cols}")
         if rows == 0:
             assert torch.all(gs == 0)
+
+
+@pytest.mark.parametrize("form", ["tc256", "tc128", "tc_pair"])
+@pytest.mark.parametrize("m,n,k", [(130, 200, 96), (7, 36, 320), (257, 520, 544), (1, 8, 32)])
+def test_nvfp4_gemm_stays_inside_its_output(h, form, m, n, k):
+    """The tcgen05 GEMM's stores (tile tails in rows, columns and k; element
+    stores when a row is not a multiple of 16 bytes) stay inside d, for fp32
+    and bf16 outputs; inputs between guards too."""
+    x, w = rand((m, k), m + k, 2.0), rand((n, k), n + 3, 2.0)
+    ref_a, ref_b = h.nvfp4_operand(x.to(DEV)), h.nvfp4_operand(w.to(DEV))
+    g = Guarded()
+    a = tuple(g.tensor(t.shape, t.dtype, 16, t) for t in ref_a)
+    b = tuple(g.tensor(t.shape, t.dtype, 48, t) for t in ref_b)
+    h.set_option("gemm", form)
+    try:
+        for dt in (torch.float32, torch.bfloat16):
+            want = h.nvfp4_gemm(ref_a, ref_b, out_dtype=dt)
+            d = g.tensor((m, n), dt, 16)
+            h.nvfp4_gemm(a, b, out=d)
+            g.check(f"nvfp4_gemm {form} {m}x{n}x{k} {dt}")
+            assert h.device_status() == 0
+            assert torch.equal(d, want), (form, m, n, k, dt)
+    finally:
+        h.set_option("gemm", "tc256")
