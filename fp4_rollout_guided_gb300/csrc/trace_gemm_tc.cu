@@ -48,9 +48,10 @@
 // Tensor memory (512 columns of 32-bit lanes, lane = tile row): the
 // accumulator in columns [0, BN), then a ring of slots (one stage each,
 // fewer slots than shared-memory stages so that the loads run a stage
-// further ahead) holding the A scales (four columns per k-step), the B
-// scales (BN / 32 columns per k-step) and A (eight columns of packed codes
-// per k-step; a pair's MMAs read A from shared memory instead).  Scales follow the tile layout: line L of a
+// further ahead; a pair has a slot per stage) holding the A scales (four
+// columns per k-step), the B scales (BN / 32 columns per k-step) and A
+// (eight columns of packed codes per k-step; a pair's MMAs read A from
+// shared memory instead).  Scales follow the tile layout: line L of a
 // 512-byte tile holds rows L, L + 32, L + 64, L + 96, and lane L of every
 // quarter holds line L, so column c of lane L holds the four scales of row
 // L + 32 c for the k-step.
@@ -62,7 +63,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include <cstring>
 #include <mutex>
 
 #include "trace_async.cuh"
