@@ -49,6 +49,7 @@ METRIC = "guided NVFP4 fake-quant GB/s (bytes in+out) and % of GB300 HBM peak"
 # (the fused rollout kernel moves x once through HBM: its quantisation pass
 # re-reads x from L2)
 KERNEL_BYTES = {"amax": 2.0, "rollout_quant": 2.8125, "rollout_fused": 2.8125,
+                "rollout_delayed": 2.8125,
                 "guide_pack": 0.75, "guide_unpack": 2.8125, "fakequant_compact": 4.4375,
                 "fakequant_full": 4.6875, "ste_backward": 4.125}
 
@@ -372,7 +373,7 @@ def mem_available_bytes():
 class StepRunner:
     """Device buffers and the step of one workload through the public API."""
 
-    def __init__(self, h, w, x, r, kind, dev):
+    def __init__(self, h, w, x, r, kind, dev, delayed=False):
         from fp4_rollout_guided_gb300 import trace
         self.h, self.w, self.x, self.r, self.kind, self.dev = h, w, x, r, kind, dev
         rows, cols = w.rows, w.cols
@@ -385,13 +386,29 @@ class StepRunner:
         self.y = torch.empty_like(x)
         self.mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
         self.trace = trace
+        # delayed scaling: the rollout side scaled by the maxima the previous
+        # step returned (one kernel, x read once); a first call here supplies
+        # them (r is the same every step, so from then on the scales equal
+        # the exact path's)
+        self.delayed = delayed
+        if delayed:
+            self.amax_prev = torch.ones((w.n_seg_r,), dtype=torch.float32, device=dev)
+            self.amax_next = torch.empty_like(self.amax_prev)
+            h.rollout_quant_delayed(r, w.seg_r, self.amax_prev,
+                                    out=(self.codes, self.bs, self.gs, self.guide, self.amax_next))
+            self.amax_prev, self.amax_next = self.amax_next, self.amax_prev
 
     def step(self, xd=None, rd=None, stats=None, kind=None):
         xd = self.x if xd is None else xd
         rd = self.r if rd is None else rd
         kind = kind or self.kind
         w, h = self.w, self.h
-        h.rollout_quant(rd, w.seg_r, out=(self.codes, self.bs, self.gs, self.guide))
+        if self.delayed:
+            h.rollout_quant_delayed(rd, w.seg_r, self.amax_prev,
+                                    out=(self.codes, self.bs, self.gs, self.guide, self.amax_next))
+            self.amax_prev, self.amax_next = self.amax_next, self.amax_prev
+        else:
+            h.rollout_quant(rd, w.seg_r, out=(self.codes, self.bs, self.gs, self.guide))
         h.guide_pack(self.codes, out=self.packed)
         h.guide_unpack(rd, self.guide, self.bs, self.gs, w.seg_r, out=self.unpacked)
         h.train_fakequant(xd, w.seg_t, kind, self.guide if kind == "compact" else self.codes,
@@ -519,7 +536,7 @@ def run_ours(args, w0):
     t_gen = time.perf_counter()
     x, r = synth.make_inputs(w, dev)
     kind = args.guide
-    run = StepRunner(h, w, x, r, kind, dev)
+    run = StepRunner(h, w, x, r, kind, dev, delayed=args.delayed)
     torch.cuda.synchronize()
     t_gen = time.perf_counter() - t_gen
 
@@ -535,6 +552,9 @@ def run_ours(args, w0):
     if waits != 0:
         raise SystemExit("an in-kernel wait ran out during the timed steps")
     launches = sum(n for n, _ in times.values())
+    # the delayed quantiser's call also launches the kernel that turns the
+    # given maxima into global scales
+    launches += times.get("rollout_delayed", (0, 0.0))[0]
     peak, peak_src = load_peaks()
     kernels = kernel_table(times, kind, elems, peak)
     # the metric: the guided fake quantiser's bytes over its own launch time
@@ -571,7 +591,9 @@ def run_ours(args, w0):
             "config": {"workload": w.name, "elements_per_gpu": elems,
                        "segments_train": w.n_seg_t, "segments_rollout": w.n_seg_r,
                        "guide": kind,
-                       "step": ("rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
+                       "step": ("rollout_delayed(quant, maxima of the previous step)"
+                                if args.delayed else
+                                "rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
                        + ", guide_pack, guide_unpack, amax+guided_fakequant",
                        "value_bytes_per_elem": KERNEL_BYTES["fakequant_" + kind],
                        "step_bytes_per_elem": bpe,
@@ -879,6 +901,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload report of the other four workloads")
+    ap.add_argument("--delayed", action="store_true",
+                    help="rollout side scaled by the previous step's maxima (one kernel)")
     ap.add_argument("--no-fuse", action="store_true",
                     help="rollout side as two kernels (amax, then quantiser)")
     ap.add_argument("--backward", action="store_true",

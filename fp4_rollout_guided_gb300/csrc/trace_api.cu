@@ -326,11 +326,14 @@ trace_status_t trace_device_status(trace_handle_t h, trace_stream_t stream) {
 namespace {
 
 // trace_rollout_quant and trace_rollout_quant_mma: block scales row-major
-// (bs_e4m3) and/or in the tensor-core tile layout (bs_mma).
+// (bs_e4m3) and/or in the tensor-core tile layout (bs_mma).  With amax_prev
+// (trace_rollout_quant_delayed) the global scales come from those maxima,
+// one kernel, and amax_out receives this tensor's maxima.
 trace_status_t rollout_quant_impl(trace_handle_t h, const void* x_bf16, int64_t rows,
                                   int64_t cols, trace_segments_t seg, void* codes_u8,
                                   void* bs_e4m3, void* bs_mma, float* gs_f32,
-                                  uint32_t* guide_bits, trace_stream_t stream) {
+                                  uint32_t* guide_bits, trace_stream_t stream,
+                                  const float* amax_prev = nullptr, float* amax_out = nullptr) {
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
@@ -343,6 +346,8 @@ trace_status_t rollout_quant_impl(trace_handle_t h, const void* x_bf16, int64_t 
   if (guide_bits && (s = check_tensor(guide_bits)) != TRACE_OK) return s;
   if (!gs_f32) return TRACE_ERR_INVALID_ARG;
   if (!aligned(gs_f32, 4)) return TRACE_ERR_ALIGNMENT;
+  if ((amax_prev && !aligned(amax_prev, 4)) || (amax_out && !aligned(amax_out, 4)))
+    return TRACE_ERR_ALIGNMENT;
   static thread_local tfp4::SegParam sp;
   if ((s = make_segments(seg, rows, &sp)) != TRACE_OK) return s;
 
@@ -358,12 +363,22 @@ trace_status_t rollout_quant_impl(trace_handle_t h, const void* x_bf16, int64_t 
                              {bs_e4m3, rows * cols / 16, true},
                              {bs_mma, bs_mma ? tfp4::mma_scales_bytes(rows, cols) : 0, true},
                              {gs_f32, (int64_t)sizeof(float) * sp.n, true},
-                             {guide_bits, rows * cols / 4, true}});
+                             {guide_bits, rows * cols / 4, true},
+                             {amax_prev, amax_prev ? (int64_t)sizeof(float) * sp.n : 0, false},
+                             {amax_out, amax_out ? (int64_t)sizeof(float) * sp.n : 0, true}});
   // the tile layout's padding (rows past a multiple of 128, scale columns
   // past a multiple of 4) is zero
   if (bs_mma && (rows % 128 != 0 || (cols / 16) % 4 != 0))
     e = cudaMemsetAsync(bs_mma, 0, (size_t)tfp4::mma_scales_bytes(rows, cols), st);
-  if (e == cudaSuccess && nchunks == 0) {
+  if (e == cudaSuccess && amax_out)
+    e = cudaMemsetAsync(amax_out, 0, sizeof(float) * sp.n, st);
+  if (e == cudaSuccess && amax_prev) {
+    e = timed(h, TRACE_KERNEL_ROLLOUT_DELAYED, st, [&] {
+      return tfp4::launch_rollout_quant_delayed(x_bf16, nchunks, cpr, sp, amax_prev, gs_f32,
+                                                codes_u8, bs_e4m3, mma, guide_bits, amax_out,
+                                                h->sm_count, st);
+    });
+  } else if (e == cudaSuccess && nchunks == 0) {
     e = cudaMemsetAsync(gs_f32, 0, sizeof(float) * sp.n, st);
   } else if (e == cudaSuccess) {
     static thread_local tfp4::WaveParam wv;
@@ -417,6 +432,16 @@ trace_status_t trace_rollout_quant_mma(trace_handle_t h, const void* x_bf16, int
                                        uint32_t* guide_bits, trace_stream_t stream) {
   return rollout_quant_impl(h, x_bf16, rows, cols, seg, codes_u8, bs_e4m3, bs_mma, gs_f32,
                             guide_bits, stream);
+}
+
+trace_status_t trace_rollout_quant_delayed(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                           int64_t cols, trace_segments_t seg,
+                                           const float* amax_prev, void* codes_u8,
+                                           void* bs_e4m3, float* gs_f32, uint32_t* guide_bits,
+                                           float* amax_out, trace_stream_t stream) {
+  if (!amax_prev || (!bs_e4m3 && rows > 0)) return TRACE_ERR_INVALID_ARG;
+  return rollout_quant_impl(h, x_bf16, rows, cols, seg, codes_u8, bs_e4m3, nullptr, gs_f32,
+                            guide_bits, stream, amax_prev, amax_out);
 }
 
 trace_status_t trace_guide_pack(trace_handle_t h, const void* codes_u8, int64_t rows,

@@ -101,6 +101,14 @@ cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
                                  MmaOut mma, uint32_t* guide, int sm_count, cudaStream_t st);
 
+// a2 with the global scales from given maxima (gs = amax_in / 2688, written
+// to gs) instead of this tensor's; amax_out (zeroed by the caller, may be
+// null) receives this tensor's segment maxima for a later call.
+cudaError_t launch_rollout_quant_delayed(const void* x, int64_t nchunks, int32_t cpr,
+                                         const SegParam& seg, const float* amax_in, float* gs,
+                                         void* codes, void* bs, MmaOut mma, uint32_t* guide,
+                                         float* amax_out, int sm_count, cudaStream_t st);
+
 // a1 + a2 in one cooperative launch (see k_rollout_fused).  plan_waves
 // groups whole segments into waves of about wave_bytes of x; it returns
 // false when a segment is too large to stay in L2 between the two phases.

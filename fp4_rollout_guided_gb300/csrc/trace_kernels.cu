@@ -156,11 +156,10 @@ __device__ __forceinline__ void build_inv_tab(float* inv, float gs, int tid, int
 }
 
 // Block-scale codes of a chunk and their reciprocal scales, with the
-// segment's constants (den = gs * 6, rden = 1 / den) and 1/S table.
-__device__ __forceinline__ PairScale chunk_scale_tab(const Chunk& cur, float gs, float den,
+// segment's constants (den = gs * 6, rden = 1 / den) and 1/S table, from the
+// chunk's two block maxima.
+__device__ __forceinline__ PairScale bamax_scale_tab(float b0, float b1, float gs, float den,
                                                      float rden, const float* inv_tab) {
-  float b0, b1;
-  chunk_bamax(cur, b0, b1);
   PairScale ps;
   ps.codes = pair_codes(b0, b1, gs, den, rden);
   ps.inv[0] = inv_tab[ps.codes & 0x7Fu];
@@ -168,11 +167,21 @@ __device__ __forceinline__ PairScale chunk_scale_tab(const Chunk& cur, float gs,
   return ps;
 }
 
-// The same from the global scale alone (a step that straddles segments).
+// Block-scale codes and reciprocal scales of a chunk from the global scale
+// alone (a step that straddles segments).
 __device__ __forceinline__ PairScale chunk_scale(const Chunk& cur, float gs) {
   float b0, b1;
   chunk_bamax(cur, b0, b1);
   return pair_scale(b0, b1, gs);
+}
+
+// Per-thread maximum of |x| over one segment, folded into the segment's word
+// (binary32 bits of a non-negative float, so unsigned order is float order)
+// by one atomic per warp; called by whole warps.
+__device__ __forceinline__ void flush_seg_max(uint32_t& m, uint32_t* dst) {
+  const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31u) == 0 && wm && TFP4_OK(dst, 4)) atomicMax(dst, wm);
+  m = 0u;
 }
 
 // Per-segment constants of the rollout scale (den, rden, 1/S table).
@@ -218,11 +227,15 @@ __device__ __forceinline__ void quant_chunk(const Chunk& cur, const PairScale& p
     st_stream2(guide + (uint64_t)c * 8u, compact_word(out[0], out[1]), compact_word(out[2], out[3]));
 }
 
+// AMAX_OUT: also the segment maxima of x into amax_out (zeroed by the
+// caller), for a later call that quantises with them (delayed scaling).
+template <bool AMAX_OUT>
 __global__ void __launch_bounds__(kThreads)
     k_rollout_quant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
                     uint32_t steps_per_cta, const __grid_constant__ SegParam seg,
                     const float* __restrict__ gs, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide) {
+                    uint8_t* __restrict__ bs, MmaOut mma, uint8_t* __restrict__ guide,
+                    uint32_t* __restrict__ amax_out) {
   const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
   uint32_t step = blockIdx.x * steps_per_cta;
   const uint32_t step_end = min(step + steps_per_cta, nsteps);
@@ -231,6 +244,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float inv_tab[128];
   int tseg = -1;
   SegScale sc = {0.f, 0.f, 0.f};
+  uint32_t mseg = 0u;  // AMAX_OUT: this thread's maximum in segment fseg
+  int fseg = -1;
 
   Chunk cur, nxt;
   if (step < step_end) {
@@ -246,6 +261,10 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint32_t last = min(c0 + kThreads, nchunks) - 1;
     const bool uniform = ss.update(seg, cpr.div(c0), cpr.div(last));
+    if (AMAX_OUT && uniform && ss.cur != fseg) {
+      if (fseg >= 0) flush_seg_max(mseg, amax_out + fseg);
+      fseg = ss.cur;
+    }
     if (uniform && ss.cur != tseg) {
       __syncthreads();
       tseg = ss.cur;
@@ -254,12 +273,33 @@ __global__ void __launch_bounds__(kThreads)
       __syncthreads();
     }
     if (c < nchunks) {
-      const PairScale ps =
-          uniform ? chunk_scale_tab(cur, sc.gs, sc.den, sc.rden, inv_tab)
-                  : chunk_scale(cur, ldf(gs + seg_advance(seg, ss.cur, cpr.div(c))));
+      float b0, b1;
+      chunk_bamax(cur, b0, b1);
+      PairScale ps;
+      if (uniform) {
+        ps = bamax_scale_tab(b0, b1, sc.gs, sc.den, sc.rden, inv_tab);
+        if (AMAX_OUT) mseg = max(mseg, max(__float_as_uint(b0), __float_as_uint(b1)));
+      } else {
+        // a step across segments: each chunk (part of one row) is in one
+        const int cs = seg_advance(seg, ss.cur, cpr.div(c));
+        ps = pair_scale(b0, b1, ldf(gs + cs));
+        const uint32_t mb = max(__float_as_uint(b0), __float_as_uint(b1));
+        if (AMAX_OUT && mb && TFP4_OK(amax_out + cs, 4)) atomicMax(amax_out + cs, mb);
+      }
       quant_chunk(cur, ps, c, codes, bs, mma, cpr, guide);
     }
     cur = nxt;
+  }
+  if (AMAX_OUT && fseg >= 0) flush_seg_max(mseg, amax_out + fseg);
+}
+
+// Delayed scaling: gs[s] = amax[s] / 2688 from given maxima (binary32; a
+// maximum that is not positive gives 0), as the amax kernel computes it.
+__global__ void k_scales_from_amax(const float* __restrict__ amax, int32_t n,
+                                   float* __restrict__ gs) {
+  for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    if (!TFP4_OK(amax + i, 4) || !TFP4_OK(gs + i, 4)) continue;
+    gs[i] = global_scale_of(__float_as_uint(amax[i]));
   }
 }
 
@@ -1010,12 +1050,30 @@ cudaError_t launch_amax(const void* x, int64_t nchunks, int32_t cpr, const SegPa
 cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
                                  MmaOut mma, uint32_t* guide, int sm_count, cudaStream_t st) {
-  const Plan p = plan_for((const void*)k_rollout_quant, steps_of(nchunks, kThreads), sm_count);
-  k_rollout_quant<<<p.grid, kThreads, 0, st>>>((const uint8_t*)x, (uint32_t)nchunks,
-                                               FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
-                                               (uint8_t*)codes, (uint8_t*)bs, mma,
-                                               (uint8_t*)guide);
+  const Plan p =
+      plan_for((const void*)k_rollout_quant<false>, steps_of(nchunks, kThreads), sm_count);
+  k_rollout_quant<false><<<p.grid, kThreads, 0, st>>>(
+      (const uint8_t*)x, (uint32_t)nchunks, FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
+      (uint8_t*)codes, (uint8_t*)bs, mma, (uint8_t*)guide, nullptr);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rollout_quant_delayed(const void* x, int64_t nchunks, int32_t cpr,
+                                         const SegParam& seg, const float* amax_in, float* gs,
+                                         void* codes, void* bs, MmaOut mma, uint32_t* guide,
+                                         float* amax_out, int sm_count, cudaStream_t st) {
+  k_scales_from_amax<<<(seg.n + 255) / 256, 256, 0, st>>>(amax_in, seg.n, gs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || nchunks == 0) return e;
+  if (amax_out) {
+    const Plan p =
+        plan_for((const void*)k_rollout_quant<true>, steps_of(nchunks, kThreads), sm_count);
+    k_rollout_quant<true><<<p.grid, kThreads, 0, st>>>(
+        (const uint8_t*)x, (uint32_t)nchunks, FastDivU((uint32_t)cpr), p.steps_per_cta, seg, gs,
+        (uint8_t*)codes, (uint8_t*)bs, mma, (uint8_t*)guide, reinterpret_cast<uint32_t*>(amax_out));
+    return cudaGetLastError();
+  }
+  return launch_rollout_quant(x, nchunks, cpr, seg, gs, codes, bs, mma, guide, sm_count, st);
 }
 
 // Largest x bytes a single segment may hold on the fused path: two waves of

@@ -25,7 +25,7 @@ from . import build as _build
 GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
 KERNELS = ("amax", "rollout_quant", "guide_pack", "guide_unpack", "fakequant", "ste_backward",
-           "rollout_fused", "mma_scales", "nvfp4_gemm")
+           "rollout_fused", "mma_scales", "nvfp4_gemm", "rollout_delayed")
 OPTIONS = {"fused_amax": 0, "wave_bytes": 1, "wait_limit_ns": 2, "wait_extra": 3,
            "debug_shrink": 4, "gemm": 5}
 # values of the "gemm" option: the form of nvfp4_gemm
@@ -78,6 +78,7 @@ SIGNATURES = {
     "trace_debug_bounds": (INT, [P, ctypes.POINTER(ctypes.c_int),
                                  ctypes.POINTER(ctypes.c_uint64)]),
     "trace_rollout_quant_mma": (INT, [P, P, I64, I64, Segments, P, P, P, P, P, P]),
+    "trace_rollout_quant_delayed": (INT, [P, P, I64, I64, Segments, P, P, P, P, P, P, P]),
     "trace_block_scales_mma_bytes": (ctypes.c_size_t, [I64, I64]),
     "trace_block_scales_mma": (INT, [P, P, I64, I64, P, P]),
     "trace_nvfp4_gemm": (INT, [P, P, P, P, P, P, P, I64, I64, I64, P, INT, P]),
@@ -212,6 +213,39 @@ class Handle:
                                        _ptr(codes), _ptr(bs), _ptr(gs), _ptr(gd), _stream())
         self._check("trace_rollout_quant", st)
         return codes, bs, gs, gd
+
+    def rollout_quant_delayed(self, x: torch.Tensor, seg, amax_prev: torch.Tensor, *,
+                              guide: bool = True, amax_out: bool = True, out=None):
+        """Rollout quantisation scaled by given per-segment maxima (delayed
+        scaling): -> (codes, bs, gs, guide or None, this tensor's maxima
+        float32[n_seg] or None)."""
+        rows, cols = x.shape
+        n_seg = 1 if seg is None else len(seg) - 1
+        if out is None:
+            out = (torch.empty((rows, cols // 2), dtype=torch.uint8, device=self.device),
+                   torch.empty((rows, cols // 16), dtype=torch.uint8, device=self.device),
+                   torch.empty((n_seg,), dtype=torch.float32, device=self.device),
+                   torch.empty((rows, cols // 16), dtype=torch.int32, device=self.device)
+                   if guide else None,
+                   torch.empty((n_seg,), dtype=torch.float32, device=self.device)
+                   if amax_out else None)
+        codes, bs, gs, gd, am = out
+        _need(x, torch.bfloat16, (rows, cols), "x", self.device)
+        _need(amax_prev, torch.float32, (n_seg,), "amax_prev", self.device)
+        _need(codes, torch.uint8, (rows, cols // 2), "codes", self.device)
+        _need(bs, torch.uint8, (rows, cols // 16), "bs", self.device)
+        _need(gs, torch.float32, (n_seg,), "gs", self.device)
+        if gd is not None:
+            _need(gd, torch.int32, (rows, cols // 16), "guide", self.device)
+        if am is not None:
+            _need(am, torch.float32, (n_seg,), "amax_out", self.device)
+        keep = []
+        st = lib().trace_rollout_quant_delayed(self._h, _ptr(x), rows, cols,
+                                               _segments(seg, rows, keep), _ptr(amax_prev),
+                                               _ptr(codes), _ptr(bs), _ptr(gs), _ptr(gd),
+                                               _ptr(am), _stream())
+        self._check("trace_rollout_quant_delayed", st)
+        return codes, bs, gs, gd, am
 
     # -- a3 ----------------------------------------------------------------------
     def guide_pack(self, codes: torch.Tensor, out: Optional[torch.Tensor] = None):

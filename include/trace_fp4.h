@@ -137,8 +137,10 @@ typedef enum {
   TRACE_KERNEL_STE_BACKWARD = 5,
   TRACE_KERNEL_ROLLOUT_FUSED = 6, /* amax + quantisation in one launch */
   TRACE_KERNEL_MMA_SCALES = 7,    /* block scales -> tensor-core tile layout */
-  TRACE_KERNEL_NVFP4_GEMM = 8,    /* the cuBLASLt GEMM (all of its kernels)  */
-  TRACE_KERNEL_COUNT = 9
+  TRACE_KERNEL_NVFP4_GEMM = 8,    /* the GEMM (the tcgen05 kernel, or all of
+                                     cuBLASLt's kernels)                     */
+  TRACE_KERNEL_ROLLOUT_DELAYED = 9, /* quantisation with given maxima        */
+  TRACE_KERNEL_COUNT = 10
 } trace_kernel_id_t;
 
 typedef struct {
@@ -376,6 +378,31 @@ TRACE_API trace_status_t trace_rollout_quant_mma(trace_handle_t h, const void* x
                                                  trace_segments_t seg, void* codes_u8,
                                                  void* bs_e4m3, void* bs_mma, float* gs_f32,
                                                  uint32_t* guide_bits, trace_stream_t stream);
+
+/* Rollout-side quantisation with delayed scaling: the same codes, block
+ * scales and compact words as trace_rollout_quant, but each segment's global
+ * scale comes from a given maximum, gs = amax_prev[s] / 2688 (binary32, the
+ * division trace_rollout_quant applies to the segment's own maximum), so x is
+ * read once, by one kernel, with no pass over the segment first.  The pages
+ * define gs from the segment's own maximum ([EN] "TRACE Core Concept");
+ * taking it from an earlier step, such as the same activations one rollout
+ * step before, is a deployment option of this library: elements whose
+ * magnitude exceeds amax_prev saturate (block scale 448, code magnitude 6),
+ * exactly as the oracle with that maximum given.
+ *   amax_prev  [n_seg] device, the maxima to scale by (a maximum that is not
+ *              positive gives gs = 0: the segment quantises to zero)
+ *   gs_f32     [n_seg] out (device), the global scales used
+ *   amax_out   [n_seg] out (device, may be NULL): this tensor's segment
+ *              maxima, bit-exact with trace_segment_amax, for the next call
+ * Other arguments, layouts and errors as trace_rollout_quant.  amax_prev and
+ * amax_out must not overlap. */
+TRACE_API trace_status_t trace_rollout_quant_delayed(trace_handle_t h, const void* x_bf16,
+                                                     int64_t rows, int64_t cols,
+                                                     trace_segments_t seg,
+                                                     const float* amax_prev, void* codes_u8,
+                                                     void* bs_e4m3, float* gs_f32,
+                                                     uint32_t* guide_bits, float* amax_out,
+                                                     trace_stream_t stream);
 
 typedef enum { TRACE_OUT_F32 = 0, TRACE_OUT_BF16 = 1 } trace_out_t;
 

@@ -320,6 +320,68 @@ def test_non_finite_inputs_leave_other_segments_exact(h):
         assert_same(f"{kind} y (mask only)", u16(outs[kind + "/mask"][0][:192]), oy)
 
 
+# ---------------------------------------------------------------------------
+# f1 (delayed form): rollout quantisation scaled by given maxima, one kernel
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols,seg", [(1, 32, None), (130, 96, [0, 0, 64, 130]),
+                                           (4099, 128, [0, 2048, 2048, 4099]),
+                                           (300, 2048, [0, 1, 299, 300]), (517, 224, None),
+                                           (300, 64, [0, 50, 100, 150, 200, 300])])
+def test_rollout_quant_delayed_matches_oracle(h, rows, cols, seg):
+    """Codes, block scales, gs and compact words equal the oracle's with the
+    given maxima (smaller than the segments' own: saturation; larger; equal;
+    zero: the segment quantises to zero), and the maxima it returns are the
+    segments' own."""
+    seg = None if seg is None else np.array(seg, np.int64)
+    x = rand_bf16((rows, cols), rows + 3 * cols, scale=2.0)
+    xu = u16(x)
+    own = oracle.segment_amax(xu, seg)
+    factors = np.array([0.37, 1.0, 1.9, 0.0, 0.8], np.float32)
+    prev = (own * factors[np.arange(len(own)) % len(factors)]).astype(np.float32)
+    codes, bs, gs, gd, am = h.rollout_quant_delayed(x.to(DEV), seg,
+                                                    torch.from_numpy(prev).to(DEV))
+    torch.cuda.synchronize()
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(xu, seg, amax=prev)
+    assert_same("codes", codes.cpu().numpy(), o_codes)
+    assert_same("bs", bs.cpu().numpy(), o_bs)
+    assert_same("gs", gs.cpu().numpy().view(np.uint32), o_gs.view(np.uint32))
+    assert_same("guide", u32(gd), o_guide)
+    assert_same("amax out", am.cpu().numpy().view(np.uint32), own.view(np.uint32))
+    # the same without the maxima output, and without the compact words
+    c2, b2, _, g2, a2 = h.rollout_quant_delayed(x.to(DEV), seg, torch.from_numpy(prev).to(DEV),
+                                                guide=False, amax_out=False)
+    torch.cuda.synchronize()
+    assert g2 is None and a2 is None
+    assert_same("codes (no maxima out)", c2.cpu().numpy(), o_codes)
+    assert_same("bs (no maxima out)", b2.cpu().numpy(), o_bs)
+
+
+def test_rollout_quant_delayed_chain_and_empty(h):
+    """Step t quantised with step t-1's maxima, as a loop would: each step's
+    output maxima feed the next; a step of zero rows writes only gs and
+    zeroes the maxima."""
+    seg = np.array([0, 700, 700, 1500], np.int64)
+    prev = torch.zeros(3, dtype=torch.float32, device=DEV)
+    for t in range(3):
+        x = rand_bf16((1500, 256), 40 + t, scale=1.0 + t)
+        xu = u16(x)
+        codes, bs, gs, gd, am = h.rollout_quant_delayed(x.to(DEV), seg, prev)
+        torch.cuda.synchronize()
+        o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(xu, seg, amax=prev.cpu().numpy())
+        assert_same(f"codes step {t}", codes.cpu().numpy(), o_codes)
+        assert_same(f"guide step {t}", u32(gd), o_guide)
+        prev = am.clone()
+    e = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    prev2 = torch.tensor([3.0, 0.5], dtype=torch.float32, device=DEV)
+    _, _, gs, _, am = h.rollout_quant_delayed(e, np.array([0, 0, 0], np.int64), prev2)
+    torch.cuda.synchronize()
+    want = np.array([oracle.global_scale(np.float32(3.0)), oracle.global_scale(np.float32(0.5))],
+                    np.float32)
+    assert_same("gs (empty)", gs.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert torch.all(am == 0)
+
+
 def test_empty_input(h):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
     codes, bs, gs, guide = h.rollout_quant(x, np.array([0, 0, 0], np.int64))
