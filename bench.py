@@ -386,17 +386,17 @@ class StepRunner:
         self.y = torch.empty_like(x)
         self.mask = torch.empty((rows, cols // 32), dtype=torch.int32, device=dev)
         self.trace = trace
-        # delayed scaling: the rollout side scaled by the maxima the previous
-        # step returned (one kernel, x read once); a first call here supplies
-        # them (r is the same every step, so from then on the scales equal
-        # the exact path's)
+        # delayed scaling: both sides scaled by the maxima the previous step
+        # returned (one kernel each, the input read once); a first step here
+        # supplies them (x and r are the same every step, so from then on the
+        # scales equal the exact path's)
         self.delayed = delayed
         if delayed:
             self.amax_prev = torch.ones((w.n_seg_r,), dtype=torch.float32, device=dev)
             self.amax_next = torch.empty_like(self.amax_prev)
-            h.rollout_quant_delayed(r, w.seg_r, self.amax_prev,
-                                    out=(self.codes, self.bs, self.gs, self.guide, self.amax_next))
-            self.amax_prev, self.amax_next = self.amax_next, self.amax_prev
+            self.amax_prev_t = torch.ones((w.n_seg_t,), dtype=torch.float32, device=dev)
+            self.amax_next_t = torch.empty_like(self.amax_prev_t)
+            self.step()
 
     def step(self, xd=None, rd=None, stats=None, kind=None):
         xd = self.x if xd is None else xd
@@ -411,8 +411,14 @@ class StepRunner:
             h.rollout_quant(rd, w.seg_r, out=(self.codes, self.bs, self.gs, self.guide))
         h.guide_pack(self.codes, out=self.packed)
         h.guide_unpack(rd, self.guide, self.bs, self.gs, w.seg_r, out=self.unpacked)
-        h.train_fakequant(xd, w.seg_t, kind, self.guide if kind == "compact" else self.codes,
-                          self.bs, self.gs, w.seg_r, out=(self.y, self.mask, None), stats=stats)
+        g = self.guide if kind == "compact" else self.codes
+        if self.delayed and stats is None:
+            h.train_fakequant_delayed(xd, w.seg_t, self.amax_prev_t, kind, g, self.bs, self.gs,
+                                      w.seg_r, out=(self.y, self.mask, self.amax_next_t))
+            self.amax_prev_t, self.amax_next_t = self.amax_next_t, self.amax_prev_t
+        else:
+            h.train_fakequant(xd, w.seg_t, kind, g, self.bs, self.gs, w.seg_r,
+                              out=(self.y, self.mask, None), stats=stats)
 
     def check(self):
         """One step with the counters: the record's round trip and the
@@ -552,9 +558,10 @@ def run_ours(args, w0):
     if waits != 0:
         raise SystemExit("an in-kernel wait ran out during the timed steps")
     launches = sum(n for n, _ in times.values())
-    # the delayed quantiser's call also launches the kernel that turns the
-    # given maxima into global scales
-    launches += times.get("rollout_delayed", (0, 0.0))[0]
+    if args.delayed:
+        # each delayed call also launches the kernel that turns the given
+        # maxima into global scales
+        launches += times.get("rollout_delayed", (0, 0.0))[0] + times.get("fakequant", (0, 0.0))[0]
     peak, peak_src = load_peaks()
     kernels = kernel_table(times, kind, elems, peak)
     # the metric: the guided fake quantiser's bytes over its own launch time
@@ -591,10 +598,11 @@ def run_ours(args, w0):
             "config": {"workload": w.name, "elements_per_gpu": elems,
                        "segments_train": w.n_seg_t, "segments_rollout": w.n_seg_r,
                        "guide": kind,
-                       "step": ("rollout_delayed(quant, maxima of the previous step)"
-                                if args.delayed else
-                                "rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
-                       + ", guide_pack, guide_unpack, amax+guided_fakequant",
+                       "step": ("rollout_delayed(quant, maxima of the previous step), "
+                                "guide_pack, guide_unpack, guided_fakequant(maxima of the "
+                                "previous step)" if args.delayed else
+                                ("rollout_fused(amax+quant)" if fused else "amax+rollout_quant")
+                                + ", guide_pack, guide_unpack, amax+guided_fakequant"),
                        "value_bytes_per_elem": KERNEL_BYTES["fakequant_" + kind],
                        "step_bytes_per_elem": bpe,
                        "l2": "inputs larger than L2 (no flush needed)",

@@ -503,13 +503,16 @@ trace_status_t trace_guide_unpack(trace_handle_t h, const void* x_ref_bf16,
 namespace {
 
 // The training-side fake quantiser; gs_t == nullptr: the call first runs the
-// amax pass over x into the handle's training scales.
+// amax pass over x into the handle's training scales, or with amax_prev
+// (delayed scaling) turns those maxima into them, and amax_out then receives
+// x's own maxima from the fake-quant kernel itself.
 trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t rows, int64_t cols,
                                     trace_segments_t seg_t, const float* gs_t,
                                     trace_guide_kind_t kind, const void* guide, const void* bs_r,
                                     const float* gs_r, trace_segments_t seg_r, void* y_bf16,
                                     uint32_t* ste_mask, void* codes_t_u8,
-                                    trace_stats_t* stats_dev, trace_stream_t stream) {
+                                    trace_stats_t* stats_dev, trace_stream_t stream,
+                                    const float* amax_prev = nullptr, float* amax_out = nullptr) {
   if (!h) return TRACE_ERR_INVALID_ARG;
   trace_status_t s = check_shape(rows, cols);
   if (s != TRACE_OK) return s;
@@ -522,6 +525,9 @@ trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t ro
   if (codes_t_u8 && (s = check_tensor(codes_t_u8)) != TRACE_OK) return s;
   if (stats_dev && !aligned(stats_dev, 8)) return TRACE_ERR_ALIGNMENT;
   if (gs_t && !aligned(gs_t, 4)) return TRACE_ERR_ALIGNMENT;
+  if ((amax_prev && !aligned(amax_prev, 4)) || (amax_out && !aligned(amax_out, 4)))
+    return TRACE_ERR_ALIGNMENT;
+  if (amax_out && (codes_t_u8 || stats_dev)) return TRACE_ERR_INVALID_ARG;
   static thread_local tfp4::SegParam spt, spr;
   if ((s = make_segments(seg_t, rows, &spt)) != TRACE_OK) return s;
   if (kind != TRACE_GUIDE_NONE) {
@@ -536,13 +542,15 @@ trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t ro
     spr.off[1] = (int32_t)rows;
   }
   const int64_t nchunks = rows * (cols / 32);
-  if (nchunks == 0) return TRACE_OK;
+  if (nchunks == 0 && !amax_out) return TRACE_OK;
 
   DeviceGuard g(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = begin_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
   const int32_t cpr = (int32_t)(cols / 32);
+  if (e == cudaSuccess && amax_out)
+    e = cudaMemsetAsync(amax_out, 0, sizeof(float) * spt.n, st);
   if (e == cudaSuccess)
     e = dbg_register(h, st, {{x_bf16, rows * cols * 2, false}, {y_bf16, rows * cols * 2, true},
                              {ste_mask, rows * cols / 8, true}, {codes_t_u8, rows * cols / 2, true},
@@ -551,7 +559,14 @@ trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t ro
                               false},
                              {bs_r, rows * cols / 16, false},
                              {gs_r, (int64_t)sizeof(float) * spr.n, false},
-                             {gs_t, (int64_t)sizeof(float) * spt.n, false}});
+                             {gs_t, (int64_t)sizeof(float) * spt.n, false},
+                             {amax_prev, amax_prev ? (int64_t)sizeof(float) * spt.n : 0, false},
+                             {amax_out, amax_out ? (int64_t)sizeof(float) * spt.n : 0, true},
+                             {h->scratch.gs_train, (int64_t)sizeof(float) * spt.n, true}});
+  if (e == cudaSuccess && amax_prev) {
+    e = tfp4::launch_scales_from_amax(amax_prev, spt.n, h->scratch.gs_train, st);
+    gs_t = h->scratch.gs_train;
+  }
   if (e == cudaSuccess && !gs_t) {
     e = timed(h, TRACE_KERNEL_AMAX, st, [&] {
       return tfp4::launch_amax(x_bf16, nchunks, cpr, spt, h->scratch, h->scratch.gs_train,
@@ -573,8 +588,10 @@ trace_status_t train_fakequant_impl(trace_ctx* h, const void* x_bf16, int64_t ro
     a.mask = ste_mask;
     a.codes_t = codes_t_u8;
     a.stats = stats_dev;
-    e = timed(h, TRACE_KERNEL_FAKEQUANT, st,
-              [&] { return tfp4::launch_fakequant(a, spt, spr, h->sm_count, st); });
+    a.amax_out = reinterpret_cast<uint32_t*>(amax_out);
+    if (nchunks > 0)
+      e = timed(h, TRACE_KERNEL_FAKEQUANT, st,
+                [&] { return tfp4::launch_fakequant(a, spt, spr, h->sm_count, st); });
   }
   const cudaError_t e2 = end_call(h, st);
   if (e != cudaSuccess) return cuda_fail(h, e);
@@ -607,6 +624,19 @@ trace_status_t trace_train_fakequant_gs(trace_handle_t h, const void* x_bf16, in
   if (!gs_t) return TRACE_ERR_INVALID_ARG;
   return train_fakequant_impl(h, x_bf16, rows, cols, seg_t, gs_t, kind, guide, bs_r, gs_r,
                               seg_r, y_bf16, ste_mask, codes_t_u8, stats_dev, stream);
+}
+
+trace_status_t trace_train_fakequant_delayed(trace_handle_t h, const void* x_bf16, int64_t rows,
+                                             int64_t cols, trace_segments_t seg_t,
+                                             const float* amax_prev_t, trace_guide_kind_t kind,
+                                             const void* guide, const void* bs_r,
+                                             const float* gs_r, trace_segments_t seg_r,
+                                             void* y_bf16, uint32_t* ste_mask, float* amax_out_t,
+                                             trace_stream_t stream) {
+  if (!amax_prev_t) return TRACE_ERR_INVALID_ARG;
+  return train_fakequant_impl(h, x_bf16, rows, cols, seg_t, nullptr, kind, guide, bs_r, gs_r,
+                              seg_r, y_bf16, ste_mask, nullptr, nullptr, stream, amax_prev_t,
+                              amax_out_t);
 }
 
 trace_status_t trace_segment_amax(trace_handle_t h, const void* x_bf16, int64_t rows,

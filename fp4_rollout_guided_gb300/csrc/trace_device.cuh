@@ -210,6 +210,15 @@ __device__ __forceinline__ float e4m3_decode(uint32_t code) {
   return __fmul_rn(__uint_as_float(code << 20), 0x1p120f);
 }
 
+// Per-thread maximum of |x| over one segment, folded into the segment's word
+// (binary32 bits of a non-negative float, so unsigned order is float order)
+// by one atomic per warp, then reset; called by whole warps.
+__device__ __forceinline__ void flush_seg_max(uint32_t& m, uint32_t* dst) {
+  const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31u) == 0 && wm && TFP4_OK(dst, 4)) atomicMax(dst, wm);
+  m = 0u;
+}
+
 __device__ __forceinline__ float global_scale_of(uint32_t amax_bits) {
   const float amax = __uint_as_float(amax_bits);
   if (!(amax > 0.0f)) return 0.0f;

@@ -197,7 +197,9 @@ __device__ __forceinline__ float sat4(float a) {
 #ifndef TFP4_FQ_MIN_CTAS
 #define TFP4_FQ_MIN_CTAS 4
 #endif
-template <int KIND, bool MASK, bool CODES, bool STATS>
+// AMAX: also the training segments' maxima of x into amax_out (zeroed by the
+// caller), for a later call scaled by them (delayed scaling).
+template <int KIND, bool MASK, bool CODES, bool STATS, bool AMAX = false>
 __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     k_fakequant(const uint8_t* __restrict__ x, uint32_t nchunks, FastDivU cpr,
                 uint32_t steps_per_cta, const __grid_constant__ SegParam seg_t,
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
                 const uint8_t* __restrict__ guide, const uint8_t* __restrict__ bs_r,
                 const float* __restrict__ gs_r, uint8_t* __restrict__ y,
                 uint8_t* __restrict__ mask, uint8_t* __restrict__ codes_t,
-                trace_stats_t* __restrict__ stats, float nzero) {
+                trace_stats_t* __restrict__ stats, float nzero, uint32_t* __restrict__ amax_out) {
   constexpr bool GUIDED = KIND != TRACE_GUIDE_NONE;
   const uint32_t nsteps = (nchunks + kThreads - 1) / kThreads;
   uint32_t step = blockIdx.x * steps_per_cta;
@@ -222,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   uint32_t n_done = 0;
   __shared__ ScaleTab tab_t, tab_r;
   int tseg = -1, rseg = -1;                 // segments the tables hold
+  uint32_t mseg = 0u;                       // AMAX: this thread's maximum in segment aseg
+  int aseg = -1;
   float seg_gs = 0.0f, seg_den = 0.0f, seg_rden = 0.0f;
 
   // the next step's inputs are loaded at the end of the current step
@@ -248,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
     const uint32_t r0 = cpr.div(c0), r1 = cpr.div(min(c0 + kThreads, nchunks) - 1);
     const bool uni_t = st.update(seg_t, r0, r1);
     const bool uni_r = GUIDED ? sr.update(seg_r, r0, r1) : true;
+    if (AMAX && uni_t && st.cur != aseg) {
+      if (aseg >= 0) flush_seg_max(mseg, amax_out + aseg);
+      aseg = st.cur;
+    }
     // refresh the scale tables when the (uniform) segment changes
     const bool new_t = uni_t && st.cur != tseg;
     const bool new_r = GUIDED && uni_r && sr.cur != rseg;
@@ -279,6 +287,13 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
       float bam0, bam1;
       chunk_bamax(cur, bam0, bam1);
+      if (AMAX && c < nchunks) {
+        const uint32_t mb = max(__float_as_uint(bam0), __float_as_uint(bam1));
+        if (uni_t)
+          mseg = max(mseg, mb);
+        else if (mb && TFP4_OK(amax_out + s_t, 4))
+          atomicMax(amax_out + s_t, mb);
+      }
       if (uni_t) {
         pt.codes = pair_codes(bam0, bam1, seg_gs, seg_den, seg_rden);
 #pragma unroll
@@ -453,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
       }
     }
   }
+  if (AMAX && aseg >= 0) flush_seg_max(mseg, amax_out + aseg);
   if (STATS) {
     const uint32_t v[11] = {n_done,       cnt.mm_rtn,   cnt.mm_g,     cnt.h_rtn[0],
                             cnt.h_rtn[1], cnt.h_rtn[2], cnt.h_rtn[3], cnt.h_g[0],
@@ -468,16 +484,16 @@ __global__ void __launch_bounds__(kThreads, TFP4_FQ_MIN_CTAS)
   }
 }
 
-template <int KIND, bool MASK, bool CODES, bool STATS>
+template <int KIND, bool MASK, bool CODES, bool STATS, bool AMAX = false>
 cudaError_t fq_launch(const FakequantArgs& a, const SegParam& seg_t, const SegParam& seg_r,
                       int sm_count, cudaStream_t st) {
-  auto kern = k_fakequant<KIND, MASK, CODES, STATS>;
+  auto kern = k_fakequant<KIND, MASK, CODES, STATS, AMAX>;
   const Plan p = plan_for((const void*)kern, steps_of(a.nchunks, kThreads), sm_count);
   kern<<<p.grid, kThreads, 0, st>>>((const uint8_t*)a.x, (uint32_t)a.nchunks,
                                     FastDivU((uint32_t)a.cpr), p.steps_per_cta, seg_t, a.gs_t,
                                     seg_r, (const uint8_t*)a.guide, (const uint8_t*)a.bs_r,
                                     a.gs_r, (uint8_t*)a.y, (uint8_t*)a.mask,
-                                    (uint8_t*)a.codes_t, a.stats, -0.0f);
+                                    (uint8_t*)a.codes_t, a.stats, -0.0f, a.amax_out);
   return cudaGetLastError();
 }
 
@@ -485,6 +501,12 @@ template <int KIND>
 cudaError_t fq_dispatch(const FakequantArgs& a, const SegParam& t, const SegParam& r, int sm,
                         cudaStream_t st) {
   const int sel = ((a.mask != nullptr) << 2) | ((a.codes_t != nullptr) << 1) | (a.stats != nullptr);
+  if (a.amax_out) {
+    // delayed scaling: y and the mask (or y alone)
+    if (sel == 4) return fq_launch<KIND, true, false, false, true>(a, t, r, sm, st);
+    if (sel == 0) return fq_launch<KIND, false, false, false, true>(a, t, r, sm, st);
+    return cudaErrorInvalidValue;
+  }
   switch (sel) {
     case 0: return fq_launch<KIND, false, false, false>(a, t, r, sm, st);
     case 1: return fq_launch<KIND, false, false, true>(a, t, r, sm, st);

@@ -101,6 +101,9 @@ cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
                                  const SegParam& seg, const float* gs, void* codes, void* bs,
                                  MmaOut mma, uint32_t* guide, int sm_count, cudaStream_t st);
 
+// gs[s] = amax[s] / 2688 from given maxima (delayed scaling).
+cudaError_t launch_scales_from_amax(const float* amax, int32_t n, float* gs, cudaStream_t st);
+
 // a2 with the global scales from given maxima (gs = amax_in / 2688, written
 // to gs) instead of this tensor's; amax_out (zeroed by the caller, may be
 // null) receives this tensor's segment maxima for a later call.
@@ -146,6 +149,7 @@ struct FakequantArgs {
   uint32_t* mask;
   void* codes_t;
   trace_stats_t* stats;
+  uint32_t* amax_out = nullptr;  // delayed scaling: the training maxima (y and mask only)
 };
 cudaError_t launch_fakequant(const FakequantArgs& a, const SegParam& seg_t,
                              const SegParam& seg_r, int sm_count, cudaStream_t st);

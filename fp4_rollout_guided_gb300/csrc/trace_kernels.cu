@@ -175,14 +175,6 @@ __device__ __forceinline__ PairScale chunk_scale(const Chunk& cur, float gs) {
   return pair_scale(b0, b1, gs);
 }
 
-// Per-thread maximum of |x| over one segment, folded into the segment's word
-// (binary32 bits of a non-negative float, so unsigned order is float order)
-// by one atomic per warp; called by whole warps.
-__device__ __forceinline__ void flush_seg_max(uint32_t& m, uint32_t* dst) {
-  const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, m);
-  if ((threadIdx.x & 31u) == 0 && wm && TFP4_OK(dst, 4)) atomicMax(dst, wm);
-  m = 0u;
-}
 
 // Per-segment constants of the rollout scale (den, rden, 1/S table).
 struct SegScale {
@@ -1058,12 +1050,17 @@ cudaError_t launch_rollout_quant(const void* x, int64_t nchunks, int32_t cpr,
   return cudaGetLastError();
 }
 
+cudaError_t launch_scales_from_amax(const float* amax, int32_t n, float* gs, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  k_scales_from_amax<<<(n + 255) / 256, 256, 0, st>>>(amax, n, gs);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rollout_quant_delayed(const void* x, int64_t nchunks, int32_t cpr,
                                          const SegParam& seg, const float* amax_in, float* gs,
                                          void* codes, void* bs, MmaOut mma, uint32_t* guide,
                                          float* amax_out, int sm_count, cudaStream_t st) {
-  k_scales_from_amax<<<(seg.n + 255) / 256, 256, 0, st>>>(amax_in, seg.n, gs);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_scales_from_amax(amax_in, seg.n, gs, st);
   if (e != cudaSuccess || nchunks == 0) return e;
   if (amax_out) {
     const Plan p =

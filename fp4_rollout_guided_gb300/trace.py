@@ -71,6 +71,8 @@ SIGNATURES = {
                                     P, P, P]),
     "trace_train_fakequant_gs": (INT, [P, P, I64, I64, Segments, P, INT, P, P, P, Segments, P,
                                        P, P, P, P]),
+    "trace_train_fakequant_delayed": (INT, [P, P, I64, I64, Segments, P, INT, P, P, P,
+                                             Segments, P, P, P, P]),
     "trace_segment_amax": (INT, [P, P, I64, I64, Segments, P, P]),
     "trace_ste_backward": (INT, [P, P, P, I64, I64, P, P]),
     "trace_set_option": (INT, [P, INT, I64]),
@@ -335,6 +337,43 @@ class Handle:
                 _stream())
             self._check("trace_train_fakequant_gs", st)
         return y, m, c, stats
+
+    def train_fakequant_delayed(self, x, seg_t, amax_prev, kind="none", guide=None, bs_r=None,
+                                gs_r=None, seg_r=None, *, mask: bool = True,
+                                amax_out: bool = True, out=None):
+        """Training-side fake quantisation scaled by given per-segment maxima
+        (delayed scaling): -> (y, mask or None, x's own training-segment
+        maxima float32[n_seg_t] or None)."""
+        k = _KINDS[kind] if isinstance(kind, str) else int(kind)
+        rows, cols = x.shape
+        n_seg = 1 if seg_t is None else len(seg_t) - 1
+        if out is None:
+            out = (torch.empty((rows, cols), dtype=torch.bfloat16, device=self.device),
+                   torch.empty((rows, cols // 32), dtype=torch.int32, device=self.device)
+                   if mask else None,
+                   torch.empty((n_seg,), dtype=torch.float32, device=self.device)
+                   if amax_out else None)
+        y, m, am = out
+        _need(x, torch.bfloat16, (rows, cols), "x", self.device)
+        _need(y, torch.bfloat16, (rows, cols), "y", self.device)
+        _need(amax_prev, torch.float32, (n_seg,), "amax_prev", self.device)
+        if m is not None:
+            _need(m, torch.int32, (rows, cols // 32), "mask", self.device)
+        if am is not None:
+            _need(am, torch.float32, (n_seg,), "amax_out", self.device)
+        if k != GUIDE_NONE:
+            if k == GUIDE_FULL:
+                _need(guide, torch.uint8, (rows, cols // 2), "guide", self.device)
+            else:
+                _need(guide, torch.int32, (rows, cols // 16), "guide", self.device)
+            _need(bs_r, torch.uint8, (rows, cols // 16), "bs_r", self.device)
+        keep = []
+        st = lib().trace_train_fakequant_delayed(
+            self._h, _ptr(x), rows, cols, _segments(seg_t, rows, keep), _ptr(amax_prev), k,
+            _ptr(guide), _ptr(bs_r), _ptr(gs_r), _segments(seg_r, rows, keep), _ptr(y), _ptr(m),
+            _ptr(am), _stream())
+        self._check("trace_train_fakequant_delayed", st)
+        return y, m, am
 
     # -- backward ---------------------------------------------------------------
     def ste_backward(self, grad_out: torch.Tensor, mask: torch.Tensor, out=None):

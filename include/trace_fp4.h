@@ -285,6 +285,24 @@ TRACE_API trace_status_t trace_train_fakequant_gs(trace_handle_t h, const void* 
                                                   trace_stats_t* stats_dev,
                                                   trace_stream_t stream);
 
+/* The training-side fake quantiser with delayed scaling: as
+ * trace_train_fakequant_gs with gs_t[s] = amax_prev_t[s] / 2688 (binary32;
+ * a maximum that is not positive gives 0), but with the maxima given instead
+ * of the scales and, if amax_out_t != NULL, x's own training-segment maxima
+ * returned by the fake-quant kernel itself (bit-exact with a separate amax
+ * pass) for the next call, so that x is read once.  Delayed scaling is a
+ * deployment option of this library, not the pages' definition (see
+ * trace_rollout_quant_delayed).  y and the STE mask (which may be NULL) only:
+ * no training codes, no counters.  The handle's training-scale scratch holds
+ * the scales, so calls through one handle run one after another.
+ *   amax_prev_t [n_seg_t] device; amax_out_t [n_seg_t] out (device, may be
+ *   NULL; zero rows zeroes it).  Other arguments as trace_train_fakequant. */
+TRACE_API trace_status_t trace_train_fakequant_delayed(
+    trace_handle_t h, const void* x_bf16, int64_t rows, int64_t cols, trace_segments_t seg_t,
+    const float* amax_prev_t, trace_guide_kind_t kind, const void* guide, const void* bs_r,
+    const float* gs_r, trace_segments_t seg_r, void* y_bf16, uint32_t* ste_mask,
+    float* amax_out_t, trace_stream_t stream);
+
 /* Per-segment amax and global scale alone ([EN] "TRACE Core Concept": one
  * FP32 global scale per segment, gs = amax / (448 * 6)); the first pass of
  * trace_rollout_quant's two-kernel form and of trace_train_fakequant.

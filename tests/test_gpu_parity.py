@@ -357,6 +357,45 @@ def test_rollout_quant_delayed_matches_oracle(h, rows, cols, seg):
     assert_same("bs (no maxima out)", b2.cpu().numpy(), o_bs)
 
 
+@pytest.mark.parametrize("kind", ["compact", "full", "none"])
+@pytest.mark.parametrize("rows,cols,seg_t,seg_r", [
+    (1, 32, None, None), (300, 64, [0, 50, 100, 150, 200, 300], [0, 50, 100, 150, 200, 300]),
+    (4099, 128, [0, 2048, 2048, 4099], [0, 1000, 2048, 2048, 3000, 4099]),
+    (517, 224, None, [0, 100, 517])])
+def test_train_fakequant_delayed_matches_oracle(h, kind, rows, cols, seg_t, seg_r):
+    """y and the STE mask equal the oracle's with the training scales from
+    the given maxima (smaller: saturated blocks; larger; equal; zero), with
+    and without the mask, and the maxima returned are the segments' own."""
+    seg_t = None if seg_t is None else np.array(seg_t, np.int64)
+    seg_r = None if seg_r is None else np.array(seg_r, np.int64)
+    x = rand_bf16((rows, cols), rows + 5 * cols, scale=2.0)
+    r = drift(x, rows + 1, 2.0 ** -6)
+    xu, ru = u16(x), u16(r)
+    own = oracle.segment_amax(xu, seg_t)
+    factors = np.array([0.37, 1.0, 1.9, 0.0, 0.8], np.float32)
+    prev = (own * factors[np.arange(len(own)) % len(factors)]).astype(np.float32)
+    o_codes, o_bs, o_gs, o_guide = oracle.rollout_quant(ru, seg_r)
+    okind = {"none": oracle.GUIDE_NONE, "full": oracle.GUIDE_FULL,
+             "compact": oracle.GUIDE_COMPACT}[kind]
+    oargs = (xu, seg_t, okind) + (() if kind == "none" else (
+        o_guide if kind == "compact" else o_codes, o_bs, o_gs, seg_r))
+    oy, om, _, _ = oracle.train_fakequant(*oargs, amax_t=prev)
+    g = {"compact": torch.from_numpy(o_guide.view(np.int32)), "full": torch.from_numpy(o_codes),
+         "none": None}[kind]
+    gargs = () if kind == "none" else (g.to(DEV), torch.from_numpy(o_bs).to(DEV),
+                                       torch.from_numpy(o_gs).to(DEV), seg_r)
+    y, m, am = h.train_fakequant_delayed(x.to(DEV), seg_t, torch.from_numpy(prev).to(DEV), kind,
+                                         *gargs)
+    y2, m2, am2 = h.train_fakequant_delayed(x.to(DEV), seg_t, torch.from_numpy(prev).to(DEV),
+                                            kind, *gargs, mask=False, amax_out=False)
+    torch.cuda.synchronize()
+    assert m2 is None and am2 is None
+    assert_same("y", u16(y), oy)
+    assert_same("mask", u32(m), om)
+    assert_same("y (no mask, no maxima)", u16(y2), oy)
+    assert_same("amax out", am.cpu().numpy().view(np.uint32), own.view(np.uint32))
+
+
 def test_rollout_quant_delayed_chain_and_empty(h):
     """Step t quantised with step t-1's maxima, as a loop would: each step's
     output maxima feed the next; a step of zero rows writes only gs and
