@@ -38,9 +38,11 @@ def training_segment(seg_t, row):
     return int(np.searchsorted(seg_t, row, side="right") - 1)
 
 
-def rollout_quant(ru, seg_r):
-    """Whole-tensor rollout record (codes, bs, gs, guide), piecewise."""
-    amax = maxima(ru, seg_r)
+def rollout_quant(ru, seg_r, amax=None):
+    """Whole-tensor rollout record (codes, bs, gs, guide), piecewise; amax
+    (float32[n_seg]) replaces the segments' own maxima (delayed scaling)."""
+    if amax is None:
+        amax = maxima(ru, seg_r)
     ps = pieces_of(seg_r, ru.shape[0])
     res = oracle.parallel_map(lambda q: oracle.rollout_quant(ru[q[0]:q[1]], None,
                                                              amax=amax[q[2]:q[2] + 1]), ps)

@@ -21,6 +21,7 @@ import pytest
 import torch
 
 import oracle
+import oracle_pieces as op
 from oracle_pieces import maxima, pieces_of
 from fp4_rollout_guided_gb300 import synth
 
@@ -168,3 +169,37 @@ def test_long_rollout_stream_every_segment(h):
     for kind in ("compact", "full"):
         assert stats[kind][0] == w.elems
         assert stats[kind][2] <= stats[kind][1]
+
+
+def test_delayed_scaling_every_element(h):
+    """Both delayed forms on the KV-row workload (537 M elements), every
+    element: the rollout side and the training side scaled by given maxima
+    (90 % of the segments' own in alternate segments, so blocks saturate at
+    scale, and 130 % in the others), and the maxima each call returns."""
+    w = synth.workload(3)
+    x, r = synth.make_inputs(w, DEV)
+    xu, ru = host(x), host(r)
+    own_r, own_t = maxima(ru, w.seg_r), maxima(xu, w.seg_t)
+    f_r = np.where(np.arange(len(own_r)) % 2 == 0, 0.9, 1.3).astype(np.float32)
+    f_t = np.where(np.arange(len(own_t)) % 2 == 0, 1.3, 0.9).astype(np.float32)
+    prev_r, prev_t = (own_r * f_r).astype(np.float32), (own_t * f_t).astype(np.float32)
+    codes, bs, gs, guide, am_r = h.rollout_quant_delayed(r, w.seg_r,
+                                                         torch.from_numpy(prev_r).to(DEV))
+    y, m, am_t = h.train_fakequant_delayed(x, w.seg_t, torch.from_numpy(prev_t).to(DEV),
+                                           "compact", guide, bs, gs, w.seg_r)
+    torch.cuda.synchronize()
+    got = {"codes": host(codes), "bs": host(bs), "gs": host(gs), "guide": host(guide),
+           "y": host(y), "mask": host(m)}
+    am_r, am_t = host(am_r), host(am_t)
+    del x, r, codes, bs, gs, guide, y, m
+    torch.cuda.empty_cache()
+    o_codes, o_bs, o_gs, o_guide = op.rollout_quant(ru, w.seg_r, amax=prev_r)
+    for name, want in (("codes", o_codes), ("bs", o_bs), ("guide", o_guide)):
+        assert np.array_equal(got[name], want), name
+    assert np.array_equal(got["gs"].view(np.uint32), o_gs.view(np.uint32))
+    assert np.array_equal(am_r.view(np.uint32), own_r.view(np.uint32))
+    oy, om, _, _ = op.train_fakequant(xu, w.seg_t, oracle.GUIDE_COMPACT, o_guide, o_bs, o_gs,
+                                      w.seg_r, amax_t=prev_t)
+    assert np.array_equal(got["y"], oy)
+    assert np.array_equal(got["mask"], om)
+    assert np.array_equal(am_t.view(np.uint32), own_t.view(np.uint32))
