@@ -662,11 +662,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t grow = (tile / tiles_n) * TM + 128u * rank + 32u * q + lane;
       const uint32_t n0 = (tile % tiles_n) * BN;
+      if (d_bf16 && vec && n0 + BN <= n) {
+        // A whole bf16 tile: the accumulator row, scaled and rounded to bf16
+        // pairs, is held in registers before the accumulator is released, so
+        // the next tile's MMAs run while this tile's rows are stored (a
+        // lane's row pieces make 32 separate pieces per store instruction,
+        // slow enough to hold the tensor pipe idle if they came first).
+        uint32_t p[BN / 2];
+#pragma unroll
+        for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
+          uint32_t v[32];
+          tmem_load32(lane_base + c, v);
+#pragma unroll
+          for (uint32_t i = 0; i < 16; ++i)
+            p[c / 2 + i] = bf16x2(__fmul_rn(alpha, __uint_as_float(v[2 * i])),
+                                  __fmul_rn(alpha, __uint_as_float(v[2 * i + 1])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_even<PAIR>(&acc_free, rank);
+        if (grow < m) {
+          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(d) +
+                                                (uint64_t)grow * n + n0);
+#pragma unroll
+          for (uint32_t j = 0; j < (uint32_t)BN / 8; ++j)
+            out[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+        }
+        continue;
+      }
+      // fp32 output, or a tile cut by n: chunk by chunk, the accumulator
+      // released after its last chunk is read
       for (uint32_t c = 0; c < (uint32_t)BN; c += 32) {
         uint32_t v[32];
         tmem_load32(lane_base + c, v);
         if (c + 32 == (uint32_t)BN) {
-          // the accumulator is read: the next tile's MMAs may start
           tc_fence_before();
           __syncwarp();
           if (lane == 0) arrive_even<PAIR>(&acc_free, rank);
