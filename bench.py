@@ -619,10 +619,12 @@ def run_ours(args, w0):
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_v, 3), "scope": e2e["scope"],
                 "measures": "the fake quantiser's bytes per element over the time of the whole "
-                            "step through the public API, inputs from and outputs to pinned "
-                            "host memory",
+                            "step through the public API, inputs from and outputs to "
+                            "page-locked host memory",
+                "host_memory": "page-locked, huge-page backed (hostmem.host_empty)",
                 "step_gbs": round(bpe * e2e["elems"] * world / (e2e_v * 1e-3) / 1e9, 1),
-                "pipeline": "per training segment: H2D (x, r on two streams), kernels, D2H overlap",
+                "pipeline": "pieces of whole training segments: H2D (one stream), kernels, D2H "
+                            "(another stream) overlap",
                 "matches_device_step": e2e["matches_device_step"]},
             "mismatch": mismatch_of(stats),
             "record_round_trip_ok": record_ok,
@@ -665,11 +667,12 @@ def _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope, step=None, outs=None):
     r go in and y, the STE mask and the compact record (words, block scales,
     global scales) come back, streamed per training segment on three CUDA
     streams (fp4_rollout_guided_gb300.pipeline), all inside the timed region."""
-    from fp4_rollout_guided_gb300 import pipeline
+    from fp4_rollout_guided_gb300 import hostmem, pipeline
     seg_t = w.seg_t[w.seg_t <= rows]
     seg_r = w.seg_r[w.seg_r <= rows]
-    x_h = torch.empty((rows, w.cols), dtype=torch.bfloat16, pin_memory=True)
-    r_h = torch.empty_like(x_h, pin_memory=True)
+    # page-locked, huge-page-backed host buffers (the library's host allocator)
+    x_h = hostmem.host_empty((rows, w.cols), torch.bfloat16)
+    r_h = hostmem.host_empty((rows, w.cols), torch.bfloat16)
     x_h.copy_(x[:rows])
     r_h.copy_(r[:rows])
     streamer = pipeline.HostStreamedStep(h, rows, w.cols, seg_t, seg_r, args.guide)
@@ -703,7 +706,7 @@ def run_transport(args, w):
     device (import), for the full record (4-bit codes) and the compact one
     (2 bits per element), on the same rollout output.  Prints one JSON line."""
     import tempfile
-    from fp4_rollout_guided_gb300 import build, synth, trace
+    from fp4_rollout_guided_gb300 import build, hostmem, synth, trace
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     build.build()
@@ -719,7 +722,7 @@ def run_transport(args, w):
     try:
         for kind, g in (("full", codes), ("compact", guide)):
             size = trace.record_size(kind, w.rows, w.cols, w.n_seg_r)
-            host = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+            host = hostmem.host_empty((size,), torch.uint8)
             out = (torch.empty_like(g), torch.empty_like(bs), torch.empty_like(gs))
             for _ in range(args.warmup):
                 h.record_export(g, bs, gs, w.seg_r, out=host)

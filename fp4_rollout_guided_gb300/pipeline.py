@@ -21,7 +21,7 @@ from typing import List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import trace
+from . import hostmem, trace
 
 
 @dataclass
@@ -66,9 +66,11 @@ class HostStreamedStep:
     over host-resident x and r, streamed in pieces.
 
     Device buffers (all full size, on the handle's device) are allocated
-    here; run() reads x_h, r_h (pinned, bf16 [rows, cols]) and writes y_h,
-    mask_h, guide_h, bs_h, gs_h (pinned) and returns once everything is
-    enqueued; synchronise the device (or the d2h stream) before reading."""
+    here; run() reads x_h, r_h (page-locked, bf16 [rows, cols]) and writes
+    y_h, mask_h, guide_h, bs_h, gs_h (page-locked) and returns once everything
+    is enqueued; synchronise the device (or the d2h stream) before reading.
+    hostmem.host_empty gives host buffers whose copies keep the link's rate
+    however fragmented the host's memory is."""
 
     def __init__(self, h: trace.Handle, rows: int, cols: int, seg_t, seg_r,
                  guide: str = "compact", min_piece_rows: Optional[int] = None):
@@ -136,8 +138,11 @@ class HostStreamedStep:
         return self.s_out
 
     def host_outputs(self, pin: bool = True):
-        """Pinned host tensors matching outputs()."""
-        return [torch.empty(t.shape, dtype=t.dtype, pin_memory=pin) for t in self.outputs()]
+        """Host tensors matching outputs(): page-locked and backed by huge
+        pages (hostmem.host_empty), or pageable with pin=False."""
+        if not pin:
+            return [torch.empty(t.shape, dtype=t.dtype) for t in self.outputs()]
+        return [hostmem.host_empty(t.shape, t.dtype) for t in self.outputs()]
 
 
 __all__ = ["Piece", "plan_pieces", "HostStreamedStep"]

@@ -21,6 +21,7 @@ import numpy as np
 import torch
 
 from . import build as _build
+from . import hostmem
 
 GUIDE_NONE, GUIDE_FULL, GUIDE_COMPACT = 0, 1, 2
 _KINDS = {"none": GUIDE_NONE, "full": GUIDE_FULL, "compact": GUIDE_COMPACT}
@@ -410,7 +411,7 @@ class Handle:
         _need(gs, torch.float32, (n_seg,), "gs", self.device)
         size = record_size(k, rows, cols, n_seg)
         if out is None:
-            out = torch.empty(size, dtype=torch.uint8, pin_memory=True)
+            out = hostmem.host_empty((size,), torch.uint8)
         p, n = _host_ptr(out)
         keep = []
         st = lib().trace_record_export(self._h, k, _ptr(guide), _ptr(bs), _ptr(gs), rows, cols,
@@ -600,9 +601,10 @@ def save_record(buf, path: str) -> None:
 
 
 def load_record(path: str, pin: bool = True) -> torch.Tensor:
-    """Reads a record file into a (pinned) uint8 host tensor and validates it."""
+    """Reads a record file into a uint8 host tensor (page-locked, huge-page
+    backed unless pin=False) and validates it."""
     size = os.path.getsize(path)
-    buf = torch.empty(size, dtype=torch.uint8, pin_memory=pin)
+    buf = hostmem.host_empty((size,), torch.uint8) if pin else torch.empty(size, dtype=torch.uint8)
     with open(path, "rb") as f:
         got = f.readinto(memoryview(buf.numpy()))
     if got != size:
