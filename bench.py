@@ -639,8 +639,8 @@ def run_ours(args, w0):
 
 
 def measure_e2e(args, h, w, x, r, step, dev, bpe, outs):
-    """Same step through the public API with the inputs in pinned host memory
-    (see _e2e_rows), on the whole workload when the host can pin it."""
+    """Same step through the public API with the inputs in page-locked host
+    memory (see _e2e_rows), on the whole workload when the host can hold it."""
     y, mask, guide, bs, gs = outs
     in_bytes = x.numel() * 2 * 2
     out_bytes = sum(t.numel() * t.element_size() for t in (y, mask, guide, bs, gs))
@@ -651,7 +651,7 @@ def measure_e2e(args, h, w, x, r, step, dev, bpe, outs):
     scope = "whole workload"
     rows = w.rows
     if avail and need * 1.6 > avail:
-        # keep pinned memory within the host's means: a leading row range of
+        # keep page-locked memory within the host's means: a leading row range of
         # whole training segments (same kernels, fewer rows)
         frac = avail / (need * 1.6)
         k = max(1, int(w.n_seg_t * frac))
@@ -663,10 +663,11 @@ def measure_e2e(args, h, w, x, r, step, dev, bpe, outs):
 
 
 def _e2e_rows(args, h, w, x, r, dev, bpe, rows, scope, step=None, outs=None):
-    """The step through the public API on host-resident inputs: pinned x and
-    r go in and y, the STE mask and the compact record (words, block scales,
-    global scales) come back, streamed per training segment on three CUDA
-    streams (fp4_rollout_guided_gb300.pipeline), all inside the timed region."""
+    """The step through the public API on host-resident inputs: page-locked
+    x and r go in and y, the STE mask and the compact record (words, block
+    scales, global scales) come back, streamed in pieces of whole training
+    segments on three CUDA streams (fp4_rollout_guided_gb300.pipeline), all
+    inside the timed region."""
     from fp4_rollout_guided_gb300 import hostmem, pipeline
     seg_t = w.seg_t[w.seg_t <= rows]
     seg_r = w.seg_r[w.seg_r <= rows]
