@@ -21,13 +21,12 @@
 //     2-D tensor-map copies in 128-byte swizzle, and the block-scale tiles
 //     (512 bytes per 128 rows and 64 elements of k) with bulk copies, into a
 //     ring of stages completing on mbarriers;
-//   - warps 2-5: stagers.  Per stage each warp moves its quarter of the A
-//     rows and the stage's scale lines from shared into tensor memory
-//     (tcgen05.st, warp w owning lane quarter w mod 4), so that the MMAs read
-//     only B from shared memory and no scale copy occupies the tensor pipe;
+//   - warps 2-5: stagers.  Per stage each warp moves the stage's scale lines
+//     from shared into tensor memory (tcgen05.st, warp w owning lane quarter
+//     w mod 4), so that no scale copy occupies the tensor pipe;
 //   - warp 1: allocates the tensor memory; one lane issues the block-scaled
-//     MMAs (128 x BN x 64 each, A and the scales in tensor memory, B in
-//     shared memory), commits each stage back to the producer and each tile
+//     MMAs (128 x BN x 64 each, A and B in shared memory, the scales in
+//     tensor memory), commits each stage back to the producer and each tile
 //     to the epilogue;
 //   - warps 6-9: epilogue.  Each thread reads its accumulator row (its
 //     warp's lane quarter), releases the accumulator to the next tile's
@@ -46,12 +45,11 @@
 // columns inside d are stored.
 //
 // Tensor memory (512 columns of 32-bit lanes, lane = tile row): the
-// accumulator in columns [0, BN), then a ring of slots (one stage each,
-// fewer slots than shared-memory stages so that the loads run a stage
-// further ahead; a pair has a slot per stage) holding the A scales (four
-// columns per k-step), the B scales (BN / 32 columns per k-step) and A
-// (eight columns of packed codes per k-step; a pair's MMAs read A from
-// shared memory instead).  Scales follow the tile layout: line L of a
+// accumulator in columns [0, BN), then a slot per shared-memory stage
+// holding the stage's A scales (four columns per k-step) and B scales
+// (BN / 32 columns per k-step).  (A staged in tensor memory instead, read
+// by the MMAs from there, left room for fewer slots than stages, and the
+// stagers then waited for slots: slower.)  Scales follow the tile layout: line L of a
 // 512-byte tile holds rows L, L + 32, L + 64, L + 96, and lane L of every
 // quarter holds line L, so column c of lane L holds the four scales of row
 // L + 32 c for the k-step.
@@ -90,19 +88,14 @@ struct GemmShape {
   static constexpr uint32_t kSfbBytes = kBands * kStepsPerStage * kSfTile;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr uint32_t kStages = PAIR ? 5 : BN == 256 ? 4 : 6;  // shared-memory ring
-  // A in tensor memory (single CTA) or read from shared memory by the MMAs
-  // (pair: the stagers then move only scales, and every stage has a slot)
-  static constexpr bool kATmem = !PAIR;
-  static constexpr uint32_t kSlots = PAIR ? kStages : BN == 256 ? 3 : 5;  // tensor-memory ring
+  static constexpr uint32_t kSlots = kStages;  // tensor-memory scale slots, one per stage
   static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
   // tensor-memory columns per k-step and their regions
   static constexpr uint32_t kSfaCols = 4;
   static constexpr uint32_t kSfbCols = 4 * kBands;
-  static constexpr uint32_t kACols = kATmem ? 8 : 0;  // 64 packed E2M1 codes
   static constexpr uint32_t kSfaBase = BN;
   static constexpr uint32_t kSfbBase = kSfaBase + kSlots * kStepsPerStage * kSfaCols;
-  static constexpr uint32_t kABase = kSfbBase + kSlots * kStepsPerStage * kSfbCols;
-  static constexpr uint32_t kColsUsed = kABase + kSlots * kStepsPerStage * kACols;
+  static constexpr uint32_t kColsUsed = kSfbBase + kSlots * kStepsPerStage * kSfbCols;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(kColsUsed + 8 <= kTmemCols, "tensor-memory columns");
@@ -232,35 +225,12 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t m, uint32_t n) {
   return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-// d (tensor memory) (+)= A B^T over one 64-element k-step, A in tensor
-// memory at a_tmem, B in shared memory, both scaled per 16-element block by
-// the UE4M3 scales in tensor memory at sfa / sfb.  For a pair, the same
-// addresses name both CTAs' tensor and shared memory.
+// d (tensor memory) (+)= A B^T over one 64-element k-step, A and B in shared
+// memory (descriptors adesc, bdesc), both scaled per 16-element block by the
+// UE4M3 scales in tensor memory at sfa / sfb.  For a pair, the same addresses
+// name both CTAs' tensor and shared memory.
 template <bool PAIR>
-__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                         uint32_t accumulate) {
-  if constexpr (PAIR)
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-        "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
-        "r"(accumulate)
-        : "memory");
-}
-
-// The same with A in shared memory (descriptor adesc).
-template <bool PAIR>
-__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                             uint32_t accumulate) {
   if constexpr (PAIR)
@@ -376,11 +346,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 
-
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled box.
-__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
-  return row * 128u + ((chunk ^ (row & 7u)) << 4);
-}
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -542,12 +507,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sfa_t = tmem + S::kSfaBase + (step0 + j) * S::kSfaCols;
           const uint32_t sfb_t = tmem + S::kSfbBase + (step0 + j) * S::kSfbCols;
           const uint32_t acc = (kb | j) != 0u ? 1u : 0u;
-          if constexpr (S::kATmem)
-            mma_nvf4<PAIR>(tmem, tmem + S::kABase + (step0 + j) * S::kACols,
-                           operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
-          else
-            mma_nvf4_ss<PAIR>(tmem, operand_desc(a_smem + 32u * j),
-                              operand_desc(b_smem + 32u * j), idesc, sfa_t, sfb_t, acc);
+          mma_nvf4<PAIR>(tmem, operand_desc(a_smem + 32u * j), operand_desc(b_smem + 32u * j),
+                         idesc, sfa_t, sfb_t, acc);
         }
         tc_commit<PAIR>(&empty[s]);
       }
@@ -572,20 +533,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (!PAIR && warp >= 2 && warp < 6) {
     // ---- stagers: warp w owns lane quarter q = w mod 4 (tile rows 32 q ..) ----
     const uint32_t q = warp & 3u;
-    const uint32_t row = 32u * q + lane;                 // row inside the tile
     const uint32_t lane_base = tmem + ((32u * q) << 16);
     uint32_t g = 0;
     bool ok = true;
     for (uint32_t tile = unit; tile < ntiles && ok; tile += units)
       for (uint32_t kb = 0; kb < nkb; ++kb, ++g) {
+        // slot t = stage s: the stage's copies land only after the MMAs of
+        // its previous use (which read the slot) completed
         const uint32_t s = g % S::kStages, ph = (g / S::kStages) & 1u;
         const uint32_t t = g % S::kSlots;
-        // slot t last held k-block g - kSlots: its MMAs completed once that
-        // k-block's stage was released
-        const uint32_t prev = g - S::kSlots;
-        if (!mbar_wait(&full[s], ph, wait_ns, err) ||
-            (S::kSlots < S::kStages && g >= S::kSlots &&
-             !mbar_wait(&empty[prev % S::kStages], (prev / S::kStages) & 1u, wait_ns, err))) {
+        if (!mbar_wait(&full[s], ph, wait_ns, err)) {
           ok = false;
           break;
         }
@@ -593,19 +550,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t st = smem_addr(smem + s * S::kStageBytes);
         const uint32_t sf_a = st + S::kABytes + S::kBBytes, sf_b = sf_a + S::kSfaBytes;
         const uint32_t step0 = t * kStepsPerStage;
-        {
-          // A row: eight 16-byte chunks in k order (undoing the 128-byte swizzle)
-          uint32_t w[32];
-#pragma unroll
-          for (uint32_t c = 0; c < 8; ++c) {
-            const uint4 v = lds128(st + swz128(row, c));
-            w[4 * c] = v.x;
-            w[4 * c + 1] = v.y;
-            w[4 * c + 2] = v.z;
-            w[4 * c + 3] = v.w;
-          }
-          tmem_store32(lane_base + S::kABase + step0 * S::kACols, w);
-        }
         {
           // A scales: line `lane` of each k-step's tile
           uint32_t w[16];
