@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   // full: a stage's copies landed; empty: its MMAs completed (its shared
   // memory and its tensor-memory slot are free again); staged: a slot holds
-  // its stage's A and scales (pair: the odd CTA's stage landed); acc_full:
+  // its stage's scales (pair: the odd CTA's stage landed); acc_full:
   // a tile's last MMA completed; acc_free: the epilogue read the
   // accumulator (pair: in both CTAs); drain: this CTA's MMAs retired
   __shared__ __align__(8) uint64_t full[S::kStages], empty[S::kStages], staged[S::kSlots],
